@@ -1,0 +1,98 @@
+// mx_common.cuh -- device helpers shared by the library's kernels.
+//
+// Operand convention of the warp-level quantized GEMM (decode path):
+//   A = the quantized integers q of 16 weight rows, as exact BF16 integers
+//       (0..15), built in registers from the packed nibbles;
+//   B = activations (or the gated hidden vector) as BF16, optionally split into
+//       2-3 BF16 parts whose sum carries fp32 precision;
+//   the per-group affine terms are applied outside the MMA in fp32:
+//       y_r += s[r,g] * (sum_{c in g} q[r,c] x_c) + b[r,g] * (sum_{c in g} x_c)
+//   which is exactly the dequantized dot product sum_c (s q + b) x_c
+//   ("Mference System design" page, "Why the runtime has this shape": BF16
+//   scale and bias per group of 64; "Metal execution": kernels consume the
+//   packed values, BF16 scales and BF16 biases directly).
+//
+// Column order inside each 8-column block of a B operand row: [0,4,1,5,2,6,3,7].
+// With it, the two BF16 pairs a lane feeds one m16n8k16 k-step come out of a
+// packed word with one shift-and-mask each, and its B values are one 64-bit
+// load.  Producers of B rows (x preparation, the gated hidden vector) write in
+// this order; weights stay in the checkpoint's order.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+constexpr int kGroup = 64;
+
+__device__ __forceinline__ float bf2f(uint16_t h) { return __uint_as_float(((uint32_t)h) << 16); }
+
+__device__ __forceinline__ uint16_t f2bf(float f) { return __bfloat16_as_ushort(__float2bfloat16_rn(f)); }
+
+// Position of column c in the operand order [0,4,1,5,2,6,3,7] of its 8-block.
+__device__ __forceinline__ int perm8(int c)
+{
+    const int a = c & 7;
+    return (c & ~7) | (a < 4 ? 2 * a : 2 * (a - 4) + 1);
+}
+
+// Streaming load of packed weights: read once, keep out of L1.
+__device__ __forceinline__ uint2 ld_stream_u2(const void *p)
+{
+    uint2 r;
+    asm("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ld_stream_u4(const void *p)
+{
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ uint4 ldg_u4(const void *p) { return __ldg(reinterpret_cast<const uint4 *>(p)); }
+
+// Nibbles j and j+4 of w as a BF16x2 pair of exact integers (low half = nibble j).
+// 0x4300 is BF16 128.0, whose 7 mantissa bits count units; OR-ing a nibble into
+// them gives 128+q exactly, and one fma (x*1 - 128) leaves q exactly.
+template <int J>
+__device__ __forceinline__ uint32_t nib_pair(uint32_t w)
+{
+    const uint32_t v = ((w >> (4 * J)) & 0x000F000Fu) | 0x43004300u;
+    uint32_t r;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(v), "r"(0x3F803F80u), "r"(0xC300C300u));
+    return r;
+}
+
+// D += A(16x16, bf16, row) * B(16x8, bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// GELU, tanh form (the reading taken for the pages' "GeGLU").
+__device__ __forceinline__ float gelu_tanh(float z)
+{
+    const float k0 = 0.7978845608028654f;
+    const float k1 = 0.044715f;
+    const float inner = k0 * (z + k1 * z * z * z);
+    return 0.5f * z * (1.0f + tanhf(inner));
+}
+
+// One packed router byte as an exact float: 2^23 + q built in the mantissa, minus 2^23.
+template <int J>
+__device__ __forceinline__ float byte_f(uint32_t w)
+{
+    return __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7540u | J)) - 8388608.0f;
+}
+
+} // namespace mx

@@ -1,0 +1,82 @@
+// mx_internal.h -- kernel argument blocks and launchers shared by the
+// library's translation units (host side).  Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+// Tokens per FFN work tile of the decode path (one expert's tokens per tile).
+constexpr int kTileTokens = 64;
+// Largest T one pass of the decode path handles; longer inputs run in chunks.
+constexpr int kDecodeChunk = 64;
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 32;
+constexpr int kMaxDim = 16384;
+
+struct RouteArgs {
+    const void *x;          // [T][D] act dtype
+    int x_dtype;            // 0 fp32, 1 bf16
+    int T, D, E, K;
+    const uint32_t *rw;     // router packed bytes [E][D/4]
+    const uint16_t *rs;     // router scales [E][D/64]
+    const uint16_t *rb;     // router biases [E][D/64]
+    int pre_norm;
+    float eps;
+    const float *pes;       // per-expert scale, nullable
+    int32_t *topk_idx;      // [T][K]
+    float *topk_w;          // [T][K]
+    float *logits;          // [T][E]
+    int32_t *counts;        // [E]
+    int32_t *offsets;       // [E+1]
+    int32_t *perm;          // [T*K]
+    int32_t *tiles;         // [3][n] (expert, begin, end) triples, nullable
+    int32_t *n_tiles;       // nullable
+    unsigned *tickets;      // [n_token_tiles + 1], zero on entry, zero on exit
+    uint16_t *xp;           // FFN operand: [nsplit][T][D] bf16 in operand column order, nullable
+    int nsplit;             // 1 (bf16 activations) or 3 (fp32 activations)
+    int ET, GC;             // experts per CTA, groups per chunk
+};
+
+struct FfnArgs {
+    int T, D, I, S, K;
+    const uint8_t *blob;
+    uint64_t stride;
+    uint64_t off_w[3], off_s[3], off_b[3];  // gate, up, down inside a record
+    const uint32_t *sw[3];                  // shared gate, up, down packed words
+    const uint16_t *ss[3];
+    const uint16_t *sb[3];
+    const uint16_t *xp;                     // [nsplit][T][D]
+    int nsplit;
+    const int32_t *perm;
+    const int32_t *tiles;
+    const int32_t *n_tiles;
+    const float *topk_w;
+    uint16_t *hr[2];                        // routed hidden, hi/lo [T*K][I]
+    uint16_t *hs[2];                        // shared hidden, hi/lo [T][S]
+    const void *residual;                   // nullable
+    void *out;
+    int act_dtype;
+    float lam;
+};
+
+// Launch configuration of the routing kernel for T tokens.
+struct RouteLaunch {
+    int TT, ET, GC, n_tt, n_et;
+    size_t smem;
+};
+RouteLaunch route_plan(int T, int D, int E);
+cudaError_t launch_route(const RouteArgs &a, const RouteLaunch &L, cudaStream_t s);
+
+// Decode-path FFN: gate/up + GeGLU, then down + combine.  The two launches are
+// bracketed by prof_begin/prof_end (no-ops unless stage profiling is on).
+cudaError_t launch_ffn_decode(const FfnArgs &a, int max_tiles, int num_sms, cudaStream_t s);
+
+// Stage profiler (mx_moe_profile_*): event pair around one launch.
+enum Stage { kStageRoute = 0, kStageGateUp = 1, kStageDown = 2 };
+void prof_begin(int stage, cudaStream_t s);
+void prof_end(int stage, cudaStream_t s);
+
+} // namespace mx

@@ -1,0 +1,421 @@
+// mx_route.cu -- router GEMV (8-bit affine) + top-k + softmax + grouping of
+// token/expert pairs, in one launch.
+//
+// "Mference System design" page, section "Decode": logits = int8_affine(x),
+// top8 = highest_8(logits), weights = softmax(logits[top8]) *
+// per_expert_scale[top8]; section "Prefill": token/expert pairs are grouped
+// into bounded per-expert work.
+//
+// Logit order (fixed so the discrete top-k decision is reproducible bit for bit;
+// "TinyTitan_Datacenter Architecture" page, "Invariants", items 1-2):
+//   per group g of 64 columns:  X = ((x0 + x1) + x2) + ...        (fp32 adds)
+//                               P = fma(q63, x63, ... fma(q0, x0, 0))
+//   over groups, ascending:     acc = fma(s_g, P, acc); acc = fma(b_g, X, acc)
+//
+// Grid: (expert tiles, token tiles).  Each CTA computes the logits of TT tokens
+// x ET experts; the last CTA of a token tile (atomic ticket, no waiting) picks
+// the top-k of those tokens; the last token tile groups all T*K slots by
+// expert.  Tickets return to zero, so the workspace is ready for the next call.
+#include "mx_common.cuh"
+#include "mx_internal.h"
+
+#include <climits>
+
+namespace mx {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kXPad = 68;  // floats per staged group row (64 + 4): conflict-free 16-byte reads
+
+__device__ __forceinline__ float load_x(const RouteArgs &a, int t, int col)
+{
+    const size_t i = (size_t)t * a.D + col;
+    if (a.x_dtype == 1)
+        return bf2f(__ldg(reinterpret_cast<const uint16_t *>(a.x) + i));
+    return __ldg(reinterpret_cast<const float *>(a.x) + i);
+}
+
+// Top-k of the logits of tokens [t0, t0+nt): one warp per token.
+__device__ void topk_tokens(const RouteArgs &a, int t0, int nt, float *sm)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = a.E, K = a.K, nwords = (E + 31) >> 5;
+    float *lg = sm + warp * E;
+    uint32_t *taken = reinterpret_cast<uint32_t *>(sm + kWarps * E) + warp * nwords;
+    for (int t = warp; t < nt; t += kWarps) {
+        const size_t row = (size_t)(t0 + t);
+        for (int e = lane; e < E; e += 32) {
+            const float v = __ldcg(a.logits + row * E + e);
+            lg[e] = isnan(v) ? -INFINITY : v;
+        }
+        for (int j = lane; j < nwords; j += 32)
+            taken[j] = 0u;
+        __syncwarp();
+        int my_idx = 0;
+        float my_val = 0.0f;
+        for (int k = 0; k < K; ++k) {
+            float bv = -INFINITY;
+            int bi = INT_MAX;
+            for (int e = lane; e < E; e += 32) {
+                if ((taken[e >> 5] >> (e & 31)) & 1u)
+                    continue;
+                const float v = lg[e];
+                if (bi == INT_MAX || v > bv) {
+                    bv = v;
+                    bi = e;
+                }
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+                if (oi != INT_MAX && (bi == INT_MAX || ov > bv || (ov == bv && oi < bi))) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (lane == 0)
+                taken[bi >> 5] |= 1u << (bi & 31);
+            if (lane == k) {
+                my_idx = bi;
+                my_val = bv;
+            }
+            __syncwarp();
+        }
+        // softmax over the selected logits, shifted by the largest (lane 0's)
+        const float m = __shfl_sync(0xffffffffu, my_val, 0);
+        float ev = (lane < K) ? expf(my_val - m) : 0.0f;
+        float sum = ev;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        if (lane < K) {
+            float w = ev / sum;
+            if (a.pes)
+                w = w * __ldg(a.pes + my_idx);
+            a.topk_idx[row * K + lane] = my_idx;
+            a.topk_w[row * K + lane] = w;
+        }
+        __syncwarp();
+    }
+}
+
+// Group all T*K slots by expert, ascending slot id inside an expert.
+__device__ void group_slots(const RouteArgs &a, float *sm)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int E = a.E, n = a.T * a.K;
+    int *wc = reinterpret_cast<int *>(sm);   // [kWarps][E] per-warp counts
+    int *base = wc + kWarps * E;             // [kWarps][E] per-warp running bases
+    int *cnt = base + kWarps * E;            // [E]
+    int *off = cnt + E;                      // [E]
+    for (int i = threadIdx.x; i < kWarps * E; i += kThreads)
+        wc[i] = 0;
+    __syncthreads();
+    const int chunk = (n + kWarps - 1) / kWarps;
+    const int lo = min(n, warp * chunk), hi = min(n, lo + chunk);
+    for (int s0 = lo; s0 < hi; s0 += 32) {
+        const int s = s0 + lane;
+        const int e = (s < hi) ? __ldcg(a.topk_idx + s) : -1;
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(m) - 1)
+            wc[warp * E + e] += __popc(m);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads) {
+        int run = 0;
+        for (int w = 0; w < kWarps; ++w) {
+            base[w * E + e] = run;
+            run += wc[w * E + e];
+        }
+        cnt[e] = run;
+        a.counts[e] = run;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int o = 0;
+        for (int e = 0; e < E; ++e) {
+            off[e] = o;
+            a.offsets[e] = o;
+            o += cnt[e];
+        }
+        a.offsets[E] = o;
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int s0 = lo; s0 < hi; s0 += 32) {
+        const int s = s0 + lane;
+        const int e = (s < hi) ? __ldcg(a.topk_idx + s) : -1;
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        if (e >= 0)
+            a.perm[off[e] + base[warp * E + e] + __popc(m & lt)] = s;
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(m) - 1)
+            base[warp * E + e] += __popc(m);
+        __syncwarp();
+    }
+    if (a.tiles && threadIdx.x == 0) {
+        int nt = 0;
+        for (int e = 0; e < E; ++e)
+            for (int b = 0; b < cnt[e]; b += kTileTokens) {
+                a.tiles[3 * nt + 0] = e;
+                a.tiles[3 * nt + 1] = off[e] + b;
+                a.tiles[3 * nt + 2] = off[e] + min(b + kTileTokens, cnt[e]);
+                ++nt;
+            }
+        *a.n_tiles = nt;
+    }
+}
+
+template <int TT>
+__global__ void __launch_bounds__(kThreads) route_kernel(const RouteArgs a)
+{
+    extern __shared__ __align__(16) float sm[];
+    __shared__ int s_last;
+    const int tid = threadIdx.x;
+    const int D = a.D, G = D / kGroup, E = a.E, ET = a.ET, GC = a.GC;
+    const int t0 = blockIdx.y * TT, nt = min(TT, a.T - t0);
+    const int e0 = blockIdx.x * ET, ne = min(ET, E - e0);
+    float *xs = sm;                         // [TT][GC][kXPad]
+    float *Ps = xs + TT * GC * kXPad;       // [TT][ET][GC]
+    float *Xs = Ps + TT * ET * GC;          // [TT][G]
+    float *sS = Xs + TT * G;                // [ET][G]
+    float *sB = sS + ET * G;                // [ET][G]
+    float *rn = sB + ET * G;                // [TT]
+    const bool prep = (blockIdx.x == 0) && a.xp != nullptr;
+
+    for (int i = tid; i < ne * G; i += kThreads) {
+        const size_t j = (size_t)e0 * G + i;
+        sS[i] = bf2f(__ldg(a.rs + j));
+        sB[i] = bf2f(__ldg(a.rb + j));
+    }
+    if (a.pre_norm) {
+        // rmsnorm_no_scale, canonical order: per group an fma chain of squares,
+        // groups summed ascending, r = 1/sqrtf(ss/D + eps).
+        float *tmp = Xs;  // [TT][G]; Xs is filled only after this
+        for (int i = tid; i < nt * G; i += kThreads) {
+            const int t = i / G, g = i % G;
+            float p = 0.0f;
+            for (int k = 0; k < kGroup; ++k) {
+                const float v = load_x(a, t0 + t, g * kGroup + k);
+                p = fmaf(v, v, p);
+            }
+            tmp[t * G + g] = p;
+        }
+        __syncthreads();
+        if (tid < nt) {
+            float ss = 0.0f;
+            for (int g = 0; g < G; ++g)
+                ss = ss + tmp[tid * G + g];
+            rn[tid] = 1.0f / sqrtf(ss / (float)D + a.eps);
+        }
+        __syncthreads();
+    }
+
+    constexpr int kAcc = 4;  // logit accumulators per thread: TT*ET <= 1024
+    float acc[kAcc];
+#pragma unroll
+    for (int i = 0; i < kAcc; ++i)
+        acc[i] = 0.0f;
+    const int npairs = nt * ne;
+    const size_t TD = (size_t)a.T * D;
+
+    for (int c0 = 0; c0 < G; c0 += GC) {
+        const int gc = min(GC, G - c0);
+        // stage x (normalised and rounded to the act dtype when asked)
+        for (int i = tid; i < nt * gc * kGroup; i += kThreads) {
+            const int t = i / (gc * kGroup), r = i % (gc * kGroup), gl = r / kGroup, k = r % kGroup;
+            const int col = (c0 + gl) * kGroup + k;
+            float v = load_x(a, t0 + t, col);
+            if (a.pre_norm) {
+                v = v * rn[t];
+                if (a.x_dtype == 1)
+                    v = bf2f(f2bf(v));
+            }
+            xs[(t * GC + gl) * kXPad + k] = v;
+            if (prep) {
+                const size_t o = (size_t)(t0 + t) * D + perm8(col);
+                const uint16_t h1 = f2bf(v);
+                a.xp[o] = h1;
+                if (a.nsplit > 1) {
+                    const float r1 = v - bf2f(h1);
+                    const uint16_t h2 = f2bf(r1);
+                    a.xp[TD + o] = h2;
+                    a.xp[2 * TD + o] = f2bf(r1 - bf2f(h2));
+                }
+            }
+        }
+        __syncthreads();
+        for (int i = tid; i < nt * gc; i += kThreads) {
+            const int t = i / gc, gl = i % gc;
+            const float *xr = xs + (t * GC + gl) * kXPad;
+            float s = 0.0f;
+            for (int k = 0; k < kGroup; ++k)
+                s = s + xr[k];
+            Xs[t * G + c0 + gl] = s;
+        }
+        if (tid < ET * gc) {
+            const int el = tid % ET, gl = tid / ET;
+            if (el < ne) {
+                const uint32_t *q = a.rw + (size_t)(e0 + el) * (D / 4) + (size_t)(c0 + gl) * 16;
+                uint4 qv[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    qv[j] = ldg_u4(q + 4 * j);
+                float P[TT];
+#pragma unroll
+                for (int t = 0; t < TT; ++t)
+                    P[t] = 0.0f;
+                const float *xr = xs + gl * kXPad;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t w = (j % 4 == 0) ? qv[j / 4].x : (j % 4 == 1) ? qv[j / 4].y
+                                     : (j % 4 == 2) ? qv[j / 4].z : qv[j / 4].w;
+                    const float q0 = byte_f<0>(w), q1 = byte_f<1>(w), q2 = byte_f<2>(w), q3 = byte_f<3>(w);
+#pragma unroll
+                    for (int t = 0; t < TT; ++t) {
+                        if (t < nt) {
+                            const float4 xv = *reinterpret_cast<const float4 *>(xr + t * GC * kXPad + 4 * j);
+                            P[t] = fmaf(q0, xv.x, P[t]);
+                            P[t] = fmaf(q1, xv.y, P[t]);
+                            P[t] = fmaf(q2, xv.z, P[t]);
+                            P[t] = fmaf(q3, xv.w, P[t]);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < TT; ++t)
+                    if (t < nt)
+                        Ps[(t * ET + el) * GC + gl] = P[t];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kAcc; ++i) {
+            const int p = tid + i * kThreads;
+            if (p < npairs) {
+                const int t = p / ne, el = p % ne;
+                float v = acc[i];
+                for (int gl = 0; gl < gc; ++gl) {
+                    const int g = c0 + gl;
+                    v = fmaf(sS[el * G + g], Ps[(t * ET + el) * GC + gl], v);
+                    v = fmaf(sB[el * G + g], Xs[t * G + g], v);
+                }
+                acc[i] = v;
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < kAcc; ++i) {
+        const int p = tid + i * kThreads;
+        if (p < npairs) {
+            const int t = p / ne, el = p % ne;
+            a.logits[(size_t)(t0 + t) * E + e0 + el] = acc[i];
+        }
+    }
+
+    // last expert tile of this token tile: top-k
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&a.tickets[blockIdx.y], 1u);
+        s_last = (prev == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    if (tid == 0)
+        a.tickets[blockIdx.y] = 0u;
+    topk_tokens(a, t0, nt, sm);
+
+    // last token tile: grouping of all slots
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned prev = atomicAdd(&a.tickets[gridDim.y], 1u);
+        s_last = (prev == gridDim.y - 1);
+    }
+    __syncthreads();
+    if (!s_last)
+        return;
+    __threadfence();
+    if (tid == 0)
+        a.tickets[gridDim.y] = 0u;
+    group_slots(a, sm);
+}
+
+template <int TT>
+cudaError_t launch_tt(const RouteArgs &a, const RouteLaunch &L, cudaStream_t s)
+{
+    auto k = route_kernel<TT>;
+    static size_t configured = 0;  // largest dynamic smem opted into so far
+    if (L.smem > 48 * 1024 && L.smem > configured) {
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
+        if (e != cudaSuccess)
+            return e;
+        configured = L.smem;
+    }
+    k<<<dim3(L.n_et, L.n_tt), kThreads, L.smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+RouteLaunch route_plan(int T, int D, int E)
+{
+    RouteLaunch L{};
+    const int G = D / kGroup;
+    if (T <= 1)
+        L.TT = 1;
+    else if (T <= 4)
+        L.TT = 4;
+    else if (T <= 128)
+        L.TT = 8;
+    else
+        L.TT = 32;
+    if (L.TT <= 4) {
+        L.GC = G;
+    } else if (L.TT == 8) {
+        L.GC = G < 32 ? G : 32;
+    } else {
+        L.GC = G < 8 ? G : 8;
+    }
+    int et = kThreads / L.GC;
+    if (et * L.TT > 1024)
+        et = 1024 / L.TT;
+    if (et > E)
+        et = E;
+    if (et < 1)
+        et = 1;
+    L.ET = et;
+    L.n_tt = (T + L.TT - 1) / L.TT;
+    L.n_et = (E + et - 1) / et;
+    const size_t main_f = (size_t)L.TT * L.GC * kXPad + (size_t)L.TT * L.ET * L.GC + (size_t)L.TT * G +
+                          2 * (size_t)L.ET * G + L.TT;
+    const size_t topk_f = (size_t)kWarps * E + (size_t)kWarps * ((E + 31) / 32);
+    const size_t group_f = 2 * (size_t)kWarps * E + 2 * (size_t)E;
+    size_t f = main_f;
+    if (topk_f > f)
+        f = topk_f;
+    if (group_f > f)
+        f = group_f;
+    L.smem = f * sizeof(float);
+    return L;
+}
+
+cudaError_t launch_route(const RouteArgs &a, const RouteLaunch &L, cudaStream_t s)
+{
+    switch (L.TT) {
+    case 1: return launch_tt<1>(a, L, s);
+    case 4: return launch_tt<4>(a, L, s);
+    case 8: return launch_tt<8>(a, L, s);
+    default: return launch_tt<32>(a, L, s);
+    }
+}
+
+} // namespace mx

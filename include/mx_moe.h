@@ -1,0 +1,227 @@
+/*
+ * mx_moe.h -- C ABI of the GB300 (sm_103a) routed Mixture-of-Experts FFN block
+ * over MLX-affine group-64 quantized weights.
+ *
+ * The block ("Mference System design" page):
+ *   - section "Why the runtime has this shape": each layer has 128 routed
+ *     experts, the router selects 8 per token; a dense shared expert is a
+ *     separate branch whose output is added without a routing weight; MLX
+ *     affine quantization, packed 4-bit values with a BF16 scale and BF16 bias
+ *     per group of 64 weights; 8-bit router, 4-bit shared and routed experts;
+ *     parallel shared and routed FFNs and a learned layer scalar;
+ *   - section "Decode": logits = int8_affine(x); top8 = highest_8(logits);
+ *     weights = softmax(logits[top8]) * per_expert_scale[top8];
+ *   - section "Metal execution": routed kernels fuse affine decode, GeGLU and
+ *     the weighted expert reduction;
+ *   - section "The .gturbo directory": one fixed-stride, page-aligned record
+ *     per routed expert, each sub-tensor at its own offset; invalid alignment
+ *     and unknown format flags are rejected.
+ *
+ * Per token t:
+ *   out[t] = residual[t] + layer_scalar * ( shared(x_t) + sum_k w[t,k] * expert_{idx[t,k]}(x_t) )
+ *   expert(x) = W_down ( gelu_tanh(W_gate x) * (W_up x) )
+ * with residual = 0 unless given (mx_moe_options), and x optionally replaced by
+ * rmsnorm_no_scale(x) rounded to the activation dtype (mx_moe_options).
+ *
+ * Quantized matrix W [rows, cols] (row-major, groups of 64 along cols, the
+ * input dimension):
+ *   4-bit: uint32 [rows][cols/8], element c in word c/8 at bits 4*(c%8);
+ *   8-bit: uint32 [rows][cols/4], element c in word c/4 at bits 8*(c%4);
+ *   scales, biases: BF16 [rows][cols/64]; w[r,c] = s[r,c/64]*q[r,c] + b[r,c/64].
+ *
+ * Top-k order: descending logit, ties to the lower expert index; NaN logits
+ * rank as -inf.  Routing logits are computed in a fixed fp32 order (per group
+ * of 64: P = fma chain of q*x, X = add chain of x; then per group, ascending,
+ * acc = fma(s, P, acc), acc = fma(b, X, acc)) so the top-k choice is
+ * reproducible bit for bit.
+ *
+ * Ownership: the caller owns every buffer (inputs, weights, outputs,
+ * workspace).  All pointers named "device" are CUDA device pointers; host
+ * structs are read only during the call.  Calls are asynchronous on the given
+ * stream; outputs are valid after the stream is synchronised.
+ * Errors: every argument is validated on the host before anything is
+ * launched; on an error nothing is written and the call returns a negative
+ * mx_status (mx_last_error_string() gives the reason, per calling thread).
+ */
+#ifndef MX_MOE_H
+#define MX_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MX_API __attribute__((visibility("default")))
+#else
+#define MX_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MX_OK = 0,
+    MX_ERR_INVALID_ARG = -1,    /* null pointer, bad size, bad dtype, bad magic/version */
+    MX_ERR_ALIGNMENT = -2,      /* pointer, offset or stride misaligned                */
+    MX_ERR_UNSUPPORTED = -3,    /* valid but unsupported shape / bit width / group     */
+    MX_ERR_WORKSPACE = -4,      /* workspace too small or could not be allocated       */
+    MX_ERR_CUDA = -5,           /* a CUDA runtime call failed                          */
+    MX_ERR_DEVICE_TIMEOUT = -6  /* a device-side bounded wait gave up                  */
+} mx_status;
+
+typedef enum { MX_F32 = 0, MX_BF16 = 1 } mx_dtype;
+
+/* One quantized matrix (device pointers; each 16-byte aligned). */
+typedef struct {
+    const void *w;          /* packed uint32 words                   */
+    const void *scales;     /* BF16 [rows][cols/64]                  */
+    const void *biases;     /* BF16 [rows][cols/64]                  */
+    int32_t rows, cols, bits;
+} mx_qlinear;
+
+/* The dense shared expert: gate [S,D], up [S,D], down [D,S], 4-bit. */
+typedef struct {
+    mx_qlinear gate, up, down;
+} mx_ffn;
+
+/* Byte offsets of one sub-tensor's packed words, scales and biases inside an
+ * expert record. */
+typedef struct {
+    uint64_t w, s, b;
+} mx_sub;
+
+#define MX_MOE_LAYOUT_MAGIC 0x4D584D45u /* "EMXM" little-endian */
+#define MX_MOE_LAYOUT_VERSION 1u
+
+/* Layout of one layer's expert blob: n_experts records of record_stride bytes.
+ * Record e holds gate [d_expert, d_model], up [d_expert, d_model] and down
+ * [d_model, d_expert] matrices (4-bit) at the offsets given.  d_shared is the
+ * intermediate width of the layer's shared expert (mx_ffn). */
+typedef struct {
+    uint32_t magic;              /* MX_MOE_LAYOUT_MAGIC                          */
+    uint32_t version;            /* MX_MOE_LAYOUT_VERSION                        */
+    int32_t d_model;             /* D, multiple of 64                            */
+    int32_t d_expert;            /* I, multiple of 64                            */
+    int32_t n_experts;           /* E, 1 <= E <= 512                             */
+    int32_t top_k;               /* K, 1 <= K <= min(E, 32)                      */
+    int32_t d_shared;            /* S, shared-expert width, multiple of 64       */
+    int32_t group;               /* 64                                           */
+    int32_t bits;                /* 4                                            */
+    uint64_t record_stride;      /* bytes, multiple of 4096                      */
+    mx_sub gate, up, down;       /* offsets: 16-byte aligned, inside the stride */
+    int32_t act_dtype;           /* mx_dtype of x, out and residual              */
+    float layer_scalar;          /* lambda                                       */
+    const float *per_expert_scale; /* device [E], nullable = all ones            */
+} mx_moe_layout;
+
+/* Per-call options (all optional; pass NULL for the plain block). */
+typedef struct {
+    const void *residual;        /* device [T][D] act dtype, nullable: out = residual + block  */
+    int32_t pre_rmsnorm;         /* 1: the block reads rmsnorm_no_scale(x) rounded to the act
+                                    dtype (canonical order: per group of 64 an fma chain of
+                                    squares, groups summed ascending, r = 1/sqrtf(ss/D + eps)) */
+    float rms_eps;               /* epsilon of pre_rmsnorm                                      */
+} mx_moe_options;
+
+/*
+ * The block, as in the pages' "Decode"/"Prefill" sections: router GEMV, top-k,
+ * softmax, routed gated experts, shared expert, weighted combine, layer scalar.
+ *   x          device [T][D], act dtype (layout->act_dtype), 16-byte aligned
+ *   T          tokens, >= 1
+ *   router     8-bit [E, D]
+ *   shared     4-bit gate/up [S, D], down [D, S]
+ *   expert_blob device, E * record_stride bytes, 256-byte aligned
+ *   out        device [T][D] act dtype (may not alias x)
+ *   topk_idx   device int32 [T][K]
+ *   topk_w     device fp32  [T][K]
+ * Runs on the legacy default stream with a workspace the library allocates
+ * and keeps (grown on demand; freed at process exit).  Not for use under CUDA
+ * graph capture; use mx_moe_layer_forward_ex there.
+ */
+MX_API mx_status mx_moe_layer_forward(const void *x, int T, const mx_qlinear *router, const mx_ffn *shared,
+                               const void *expert_blob, const mx_moe_layout *layout,
+                               void *out, int32_t *topk_idx, float *topk_w);
+
+/*
+ * Same block with explicit options, stream and workspace.
+ *   opt        nullable
+ *   stream     cudaStream_t (NULL = legacy default stream)
+ *   ws         device workspace of ws_bytes >= mx_moe_workspace_bytes(layout, T),
+ *              256-byte aligned, zero-filled before its first use (see
+ *              mx_moe_workspace_init); every call leaves it ready for the next.
+ * Allocates nothing.  Calls sharing one workspace must be ordered on the GPU
+ * (same stream, or explicit events).
+ */
+MX_API mx_status mx_moe_layer_forward_ex(const void *x, int T, const mx_qlinear *router, const mx_ffn *shared,
+                                  const void *expert_blob, const mx_moe_layout *layout,
+                                  void *out, int32_t *topk_idx, float *topk_w,
+                                  const mx_moe_options *opt, void *stream, void *ws, size_t ws_bytes);
+
+/* Workspace bytes for up to T_max tokens of this layout (0 on invalid layout). */
+MX_API size_t mx_moe_workspace_bytes(const mx_moe_layout *layout, int T_max);
+
+/* Zero-fill a workspace on the stream (cudaMemsetAsync); call once after allocating it. */
+MX_API mx_status mx_moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Routing alone (router GEMV + top-k + softmax + grouping), for exact checks.
+ *   topk_idx  device int32 [T][K];  topk_w device fp32 [T][K]
+ *   counts    device int32 [E]      tokens per expert
+ *   offsets   device int32 [E+1]    exclusive scan of counts
+ *   perm      device int32 [T*K]    slot ids s = t*K + k grouped by expert,
+ *                                   ascending s within an expert
+ *   logits    device fp32 [T][E], nullable: the router logits
+ * Grouping follows the "Prefill" section ("groups token/expert pairs into
+ * bounded routed-MoE work").  opt may request pre_rmsnorm; residual is ignored.
+ */
+MX_API mx_status mx_moe_route(const void *x, int T, const mx_qlinear *router, const mx_moe_layout *layout,
+                       int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *offsets,
+                       int32_t *perm, float *logits, const mx_moe_options *opt,
+                       void *stream, void *ws, size_t ws_bytes);
+
+/*
+ * Decode stack without attention: for l in 0..n_layers-1,
+ *   x <- round_act(x + block_l(rmsnorm_no_scale(x)))
+ * i.e. the block with pre_rmsnorm (eps) and residual = x, ping-ponging between
+ * x_io and an internal buffer of the workspace; the final x is written back to
+ * x_io.  All per-layer arrays have n_layers entries.
+ *   x_io      device [T][D] act dtype (BF16 or fp32), updated in place
+ *   topk_idx  device int32 [n_layers][T][K], topk_w device fp32 [n_layers][T][K]
+ *   ws        >= mx_moe_stack_workspace_bytes(layouts[0], T), prepared by
+ *             mx_moe_workspace_init
+ * Every layer must share D, I, E, K, dtype and the shared-expert shape.
+ * Allocates nothing; safe to capture into a CUDA graph.
+ */
+MX_API mx_status mx_moe_stack_forward(void *x_io, int T, int n_layers, const mx_qlinear *routers,
+                               const mx_ffn *shareds, const void *const *expert_blobs,
+                               const mx_moe_layout *layouts, int32_t *topk_idx, float *topk_w,
+                               float rms_eps, void *stream, void *ws, size_t ws_bytes);
+
+MX_API size_t mx_moe_stack_workspace_bytes(const mx_moe_layout *layout, int T);
+
+/*
+ * Per-stage timing, after the stage-timing profiler of the gem "Native
+ * architecture" page (section "profiling": stage-boundary timestamps sampled
+ * without changing the ordinary route).  While enabled, every block call
+ * records a CUDA event pair around each of its kernels on the call's own
+ * stream.  Stages: 0 = routing (router GEMV + top-k + grouping), 1 = gate/up +
+ * GeGLU, 2 = down + combine.  mx_moe_profile_read synchronises on the recorded
+ * events and returns, per stage, the summed milliseconds and the number of
+ * launches (arrays of MX_PROFILE_STAGES), then clears them if reset != 0.
+ * Not for use under CUDA graph capture; off by default; process-wide.
+ */
+#define MX_PROFILE_STAGES 3
+MX_API mx_status mx_moe_profile_enable(int on);
+MX_API mx_status mx_moe_profile_read(double *ms, int *launches, int reset);
+
+/* Human-readable status and the last error of the calling thread. */
+MX_API const char *mx_status_string(mx_status s);
+MX_API const char *mx_last_error_string(void);
+
+/* Library version "major.minor.patch". */
+MX_API const char *mx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MX_MOE_H */

@@ -111,9 +111,9 @@ def rng_for(seed: int, layer: int, role: int, index: int = 0) -> np.random.Gener
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
-    """Round fp32 values to BF16 (nearest, ties to even); returns uint16 bit patterns."""
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    """Round finite fp32 values to BF16 (nearest, ties to even); returns uint16 bit patterns."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    u = (u + np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
     return u.astype(np.uint16)
 
 
@@ -127,8 +127,11 @@ def uniform_bf16(rng: np.random.Generator, lo: float, hi: float, shape) -> np.nd
 
 
 def random_words(rng: np.random.Generator, shape) -> np.ndarray:
-    """Uniform uint32 words: every nibble (and byte) is uniform and independent."""
-    return rng.integers(0, 2**32, size=shape, dtype=np.uint32)
+    """Uniform uint32 words (raw generator output): every nibble and byte is
+    uniform and independent."""
+    n = int(np.prod(shape))
+    raw = rng.bit_generator.random_raw((n + 1) // 2).view(np.uint32)[:n]
+    return raw.reshape(shape)
 
 
 def make_qmat(rng: np.random.Generator, rows: int, cols: int, bits: int,

@@ -1,0 +1,191 @@
+"""The C-ABI library builds, loads, exports every symbol include/mx_moe.h
+declares, and rejects invalid arguments on the host with the documented status
+codes (no GPU needed: validation runs before any CUDA call)."""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import re
+import subprocess
+
+import pytest
+
+import expert_ffn_gb300 as mx
+from expert_ffn_gb300 import build as mxbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mx_moe.h")
+
+OK, INVALID, ALIGN, UNSUP, WS = 0, -1, -2, -3, -4
+
+
+@pytest.fixture(scope="module")
+def L():
+    mxbuild.build()
+    return mx.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MX_API\s+[\w\s\*]+?\b(mx_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_symbols()
+    assert len(names) >= 10
+    assert sorted(mx.EXPORTED) == names
+    out = subprocess.run(["nm", "-D", "--defined-only", mxbuild.LIB], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT\s+(\w+)$", out, flags=re.M))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(L, n)
+    # nothing else leaks out of the library with default visibility
+    ours = {s for s in exported if s.startswith("mx_")}
+    assert ours == set(names)
+
+
+def test_strings(L):
+    assert L.mx_version().decode().count(".") == 2
+    assert L.mx_status_string(-2).decode() == "MX_ERR_ALIGNMENT"
+
+
+# ------------------------------------------------------------- validation
+
+D, I, E, K, S = 256, 128, 16, 2, 128
+FAKE = 0x7F0000000000  # aligned, never dereferenced: validation fails first or T == 0
+
+
+def layout(**kw):
+    import synth
+    off, stride = synth.default_layout(D, I)
+    lay = mx.make_layout(D, I, E, K, S, stride, off, mx.MX_BF16, 0.5)
+    for k, v in kw.items():
+        setattr(lay, k, v)
+    return lay
+
+
+def q(rows, cols, bits, base=FAKE):
+    return mx.make_qlinear(base, base + 0x100000, base + 0x200000, rows, cols, bits)
+
+
+def call(L, lay, T=4, x=FAKE + 0x1000000, out=FAKE + 0x2000000, router=None, shared=None, blob=FAKE + 0x3000000,
+         idx=FAKE + 0x4000000, w=FAKE + 0x5000000, opt=None, ws=None, ws_bytes=0, ex=True):
+    router = router or q(E, D, 8)
+    shared = shared or mx.Ffn(q(S, D, 4), q(S, D, 4), q(D, S, 4))
+    args = [x, T, C.byref(router), C.byref(shared), blob, C.byref(lay), out, idx, w]
+    if ex:
+        return L.mx_moe_layer_forward_ex(*args, C.byref(opt) if opt else None, None, ws, ws_bytes)
+    return L.mx_moe_layer_forward(*args)
+
+
+def test_valid_call_with_zero_tokens_is_a_noop(L):
+    assert call(L, layout(), T=0) == OK
+    assert call(L, layout(), T=0, ex=False) == OK
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("magic", 0x12345678, INVALID),
+    ("version", 2, INVALID),
+    ("group", 32, UNSUP),
+    ("bits", 8, UNSUP),
+    ("d_model", 250, UNSUP),
+    ("d_expert", 100, UNSUP),
+    ("d_shared", 96, UNSUP),
+    ("n_experts", 0, UNSUP),
+    ("n_experts", 1000, UNSUP),
+    ("top_k", 0, INVALID),
+    ("top_k", 17, INVALID),
+    ("act_dtype", 7, INVALID),
+    ("record_stride", 4096 * 14 + 256, ALIGN),
+    ("record_stride", 4096, INVALID),
+])
+def test_layout_rejections(L, field, value, status):
+    assert call(L, layout(**{field: value})) == status
+    assert call(L, layout(**{field: value}), ex=False) == status
+    assert len(L.mx_last_error_string()) > 0
+
+
+@pytest.mark.parametrize("name", ["gate", "up", "down"])
+@pytest.mark.parametrize("which", ["w", "s", "b"])
+def test_misaligned_or_outside_sub_offsets(L, name, which):
+    lay = layout()
+    sub = getattr(lay, name)
+    setattr(sub, which, getattr(sub, which) + 8)
+    setattr(lay, name, sub)
+    assert call(L, lay) == ALIGN
+    lay = layout()
+    sub = getattr(lay, name)
+    setattr(sub, which, lay.record_stride - 16)
+    setattr(lay, name, sub)
+    assert call(L, lay) == INVALID
+
+
+def test_pointer_rejections(L):
+    lay = layout()
+    assert call(L, lay, x=0) == INVALID
+    assert call(L, lay, out=0) == INVALID
+    assert call(L, lay, idx=0) == INVALID
+    assert call(L, lay, blob=0) == INVALID
+    assert call(L, lay, x=FAKE + 0x1000008) == ALIGN
+    assert call(L, lay, blob=FAKE + 0x3000080) == ALIGN
+    assert call(L, lay, w=FAKE + 0x5000002) == ALIGN
+    assert call(L, lay, T=-1) == INVALID
+    # out overlapping x
+    assert call(L, lay, x=FAKE, out=FAKE + 512) == INVALID
+
+
+def test_matrix_rejections(L):
+    lay = layout()
+    assert call(L, lay, router=q(E, D, 4)) == UNSUP          # router must be 8-bit
+    assert call(L, lay, router=q(E + 1, D, 8)) == INVALID     # wrong expert count
+    assert call(L, lay, router=q(E, D, 8, base=FAKE + 4)) == ALIGN
+    bad = mx.Ffn(q(S, D, 4), q(S, D, 4), q(S, D, 4))           # transposed down
+    assert call(L, lay, shared=bad) == INVALID
+    nul = mx.Ffn(q(S, D, 4), mx.make_qlinear(FAKE, 0, FAKE, S, D, 4), q(D, S, 4))
+    assert call(L, lay, shared=nul) == INVALID
+
+
+def test_workspace_rules(L):
+    lay = layout()
+    need = L.mx_moe_workspace_bytes(C.byref(lay), 4)
+    assert need > 0
+    assert L.mx_moe_workspace_bytes(C.byref(layout(group=32)), 4) == 0
+    assert call(L, lay, ws=FAKE, ws_bytes=need - 1) == WS
+    assert call(L, lay, ws=None, ws_bytes=need) == WS
+    assert call(L, lay, ws=FAKE + 128, ws_bytes=need) == ALIGN
+    # sizes grow with T up to the decode chunk and with the route arrays beyond it
+    sizes = [L.mx_moe_workspace_bytes(C.byref(lay), t) for t in (1, 8, 64, 65, 4096)]
+    assert sizes == sorted(sizes)
+
+
+def test_route_rejections(L):
+    lay = layout()
+    r = q(E, D, 8)
+    args = lambda T=4, x=FAKE, ws=FAKE, nb=1 << 30, perm=FAKE: L.mx_moe_route(
+        x, T, C.byref(r), C.byref(lay), FAKE, FAKE, FAKE, FAKE, perm, None, None, None, ws, nb)
+    assert args(T=0) == OK
+    assert args(x=0) == INVALID
+    assert args(perm=0) == INVALID
+    assert args(nb=16) == WS
+    assert args(x=FAKE + 2) == ALIGN
+
+
+def test_stack_rejections(L):
+    lay = layout()
+    n = 2
+    routers = (mx.QLinear * n)(q(E, D, 8), q(E, D, 8))
+    shareds = (mx.Ffn * n)(*[mx.Ffn(q(S, D, 4), q(S, D, 4), q(D, S, 4)) for _ in range(n)])
+    blobs = (C.c_void_p * n)(FAKE + 0x3000000, FAKE + 0x3000000)
+    lay2 = layout()
+    lay2.d_expert = 192
+    layouts = (mx.Layout * n)(lay, lay2)
+    need = L.mx_moe_stack_workspace_bytes(C.byref(lay), 1)
+    rc = L.mx_moe_stack_forward(FAKE, 1, n, routers, shareds, blobs, layouts, FAKE, FAKE, 1e-6, None, FAKE, need)
+    assert rc == INVALID and b"layer 1" in L.mx_last_error_string()
+    layouts = (mx.Layout * n)(lay, lay)
+    rc = L.mx_moe_stack_forward(FAKE, 1, n, routers, shareds, blobs, layouts, FAKE, FAKE, -1.0, None, FAKE, need)
+    assert rc == INVALID
+    rc = L.mx_moe_stack_forward(FAKE, 1, n, routers, shareds, blobs, layouts, FAKE, FAKE, 1e-6, None, FAKE, need - 1)
+    assert rc == WS
+    rc = L.mx_moe_stack_forward(FAKE, 0, n, routers, shareds, blobs, layouts, FAKE, FAKE, 1e-6, None, FAKE, need)
+    assert rc == OK

@@ -1,0 +1,189 @@
+"""GPU parity: the CUDA path (through the C-ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars: top-k indices, counts, offsets and the expert permutation bit-exact;
+fp32 outputs rel-L2 <= 1e-4 and max|diff| <= 2e-2; BF16 outputs compared with
+the oracle's output rounded once to BF16, rel-L2 <= 1e-3 and max|diff| /
+max|oracle| <= 2e-2; routing weights rel-L2 <= 1e-4."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import synth
+from tests.helpers import max_abs_rel, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from expert_ffn_gb300 import build
+    build.build()
+
+
+@pytest.fixture(scope="module")
+def gu():
+    from tests import gpu_util
+    return gpu_util
+
+
+def check_out(got, ref, act):
+    from tests.gpu_util import as_f32
+    g, r = as_f32(got).astype(np.float64), as_f32(ref).astype(np.float64)
+    assert np.all(np.isfinite(g))
+    if act == "f32":
+        assert rel_l2(g, r) <= 1e-4, rel_l2(g, r)
+        assert np.max(np.abs(g - r)) <= 2e-2
+    else:
+        assert rel_l2(g, r) <= 1e-3, rel_l2(g, r)
+        assert max_abs_rel(g, r) <= 2e-2, max_abs_rel(g, r)
+
+
+def check_block(orc, gu, cfg, layer, x, **kw):
+    dev = __import__("expert_ffn_gb300").DeviceLayer(layer, gu.act_code(cfg))
+    out, idx, w = gu.run_block(dev, x, **kw)
+    ref, ridx, rw = orc.block_forward(layer, x)
+    assert np.array_equal(idx, ridx)
+    assert rel_l2(w, rw) <= 1e-4
+    check_out(out, ref, cfg.act)
+    return dev, out, idx, w
+
+
+# ------------------------------------------------------------- small shapes
+
+SHAPES = [
+    # T, D, E, K, I, S, act
+    (4, 256, 16, 2, 128, 128, "f32"),      # the tiny workload
+    (1, 256, 16, 2, 128, 128, "bf16"),
+    (13, 320, 24, 3, 192, 128, "bf16"),    # ragged token tiles, odd group counts
+    (64, 512, 32, 8, 128, 256, "bf16"),    # a full decode chunk
+    (65, 256, 16, 4, 128, 64, "f32"),      # one past the chunk: two passes
+    (40, 192, 8, 8, 64, 64, "bf16"),       # K = E: every expert gets every token
+    (3, 64, 4, 1, 64, 64, "f32"),          # one group per row, K = 1
+    (150, 384, 64, 6, 320, 192, "bf16"),   # several chunks, ragged tail
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[f"T{s[0]}_D{s[1]}_E{s[2]}_K{s[3]}_{s[6]}" for s in SHAPES])
+def test_block_small_shapes(orc, gu, shape):
+    T, D, E, K, I, S, act = shape
+    cfg = synth.small_config(T=T, D=D, E=E, K=K, I=I, S=S, act=act, seed=T + D)
+    layer = synth.make_layer(cfg)
+    x = synth.make_x(cfg)
+    check_block(orc, gu, cfg, layer, x)
+
+
+def test_tiny_workload_route_exact(orc, gu):
+    cfg = synth.CONFIGS[0]
+    layer = synth.make_layer(cfg)
+    x = synth.make_x(cfg)
+    dev = __import__("expert_ffn_gb300").DeviceLayer(layer, gu.act_code(cfg))
+    idx, w, counts, offsets, perm, logits = gu.run_route(dev, x)
+    rl = orc.router_logits(layer.router, gu.as_f32(x))
+    assert np.array_equal(logits, rl)          # canonical order: bit-exact
+    ridx, rw = orc.topk_softmax(rl, cfg.K)
+    rc, ro, rp = orc.permute(ridx, cfg.E)
+    assert np.array_equal(idx, ridx) and np.array_equal(counts, rc)
+    assert np.array_equal(offsets, ro) and np.array_equal(perm, rp)
+    assert rel_l2(w, rw) <= 1e-4
+
+
+def test_determinism_and_entry_points_agree(orc, gu):
+    cfg = synth.small_config(T=24, D=512, E=32, K=4, I=128, S=128, act="bf16", seed=9)
+    layer = synth.make_layer(cfg)
+    x = synth.make_x(cfg)
+    dev = __import__("expert_ffn_gb300").DeviceLayer(layer, gu.act_code(cfg))
+    a = gu.run_block(dev, x)
+    b = gu.run_block(dev, x)
+    c = gu.run_block(dev, x, ex=False)
+    for u, v in zip(a, b):
+        assert np.array_equal(u, v)
+    for u, v in zip(a, c):
+        assert np.array_equal(u, v)
+
+
+def test_residual_and_prenorm_options(orc, gu):
+    cfg = synth.small_config(T=5, D=256, E=16, K=2, I=128, S=128, act="bf16", seed=21)
+    layer = synth.make_layer(cfg)
+    x = synth.make_x(cfg)
+    dev = __import__("expert_ffn_gb300").DeviceLayer(layer, gu.act_code(cfg))
+    out, idx, w = gu.run_block(dev, x, residual=x, pre_norm=True, eps=1e-6)
+    xn = orc.rmsnorm_bf16(x, 1e-6)
+    ref, ridx, rw = orc.block_forward(layer, xn, residual=x)
+    assert np.array_equal(idx, ridx)
+    check_out(out, ref, "bf16")
+
+
+def test_zero_tokens_writes_nothing(gu):
+    import expert_ffn_gb300 as mx
+    cfg = synth.small_config(T=2, act="bf16")
+    dev = mx.DeviceLayer(synth.make_layer(cfg), mx.MX_BF16)
+    out = torch.full((2, cfg.D), 7, dtype=torch.int16, device="cuda")
+    x = torch.zeros((2, cfg.D), dtype=torch.int16, device="cuda")
+    idx = torch.full((2, cfg.K), -5, dtype=torch.int32, device="cuda")
+    w = torch.zeros((2, cfg.K), dtype=torch.float32, device="cuda")
+    mx.layer_forward(x, 0, dev, out, idx, w)
+    torch.cuda.synchronize()
+    assert bool((out == 7).all()) and bool((idx == -5).all())
+
+
+# ------------------------------------------------------------ full workloads
+
+def test_skewed_decode_T64_full(orc, gu):
+    cfg = synth.CONFIGS[3]
+    layer = synth.make_layer(cfg)
+    x = synth.make_x(cfg)
+    check_block(orc, gu, cfg, layer, x)
+
+
+def _sample_tokens(T, n, seed):
+    rng = np.random.default_rng(seed)
+    return np.unique(np.concatenate([[0, T - 1], rng.choice(T, n, replace=False)]))
+
+
+@pytest.mark.parametrize("ci", [2, 4])
+def test_prefill_route_exact_and_sampled_outputs(orc, gu, ci):
+    """Full-size prefill: every token's top-k, the counts and the permutation
+    exact (the oracle routes all T tokens); outputs on a sample of tokens."""
+    import expert_ffn_gb300 as mx
+    cfg = synth.CONFIGS[ci]
+    layer = synth.make_layer(cfg)
+    x = synth.make_x(cfg)
+    dev = mx.DeviceLayer(layer, gu.act_code(cfg))
+    out, idx, w = gu.run_block(dev, x)
+    ridx_all, rw_all = orc.topk_softmax(orc.router_logits(layer.router, gu.as_f32(x)), cfg.K)
+    assert np.array_equal(idx, ridx_all)
+    assert rel_l2(w, rw_all) <= 1e-4
+    ridx, _, _, _, perm, _ = gu.run_route(dev, x)
+    rc, ro, rp = orc.permute(ridx_all, cfg.E)
+    assert np.array_equal(ridx, ridx_all) and np.array_equal(perm, rp)
+    tok = _sample_tokens(cfg.T, 10 if ci == 2 else 6, ci)
+    ref, _, _ = orc.block_forward(layer, x[tok])
+    check_out(out[tok], ref, cfg.act)
+
+
+def test_decode_stack_30_layers(orc, gu):
+    """Single-token decode through the 30-layer stack (RMSNorm -> block ->
+    residual), free-running on both sides from the same input."""
+    import expert_ffn_gb300 as mx
+    cfg = synth.CONFIGS[1]
+    layers = [synth.make_layer(cfg, l) for l in range(cfg.layers)]
+    x = synth.make_x(cfg)
+    devs = [mx.DeviceLayer(l, mx.MX_BF16) for l in layers]
+    stack = mx.Stack(devs)
+    T, K, n = cfg.T, cfg.K, cfg.layers
+    xd = gu.to_dev(x)
+    idx = torch.full((n, T, K), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((n, T, K), dtype=torch.float32, device="cuda")
+    ws = gu.Workspace(mx.stack_workspace_bytes(devs[0].layout, T))
+    mx.stack_forward(xd, T, stack, idx, w, ws.t, ws.nbytes, rms_eps=1e-6, stream=torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    xs_ref, idx_ref, w_ref = orc.stack_forward(layers, x, 1e-6)
+    assert np.array_equal(idx.cpu().numpy(), idx_ref)
+    assert rel_l2(w.cpu().numpy(), w_ref) <= 1e-4
+    check_out(gu.to_host(xd, np.uint16), xs_ref[-1], "bf16")
