@@ -24,7 +24,8 @@ MX_F32, MX_BF16 = 0, 1
 # Every symbol include/mx_moe.h declares.
 EXPORTED = ("mx_moe_layer_forward", "mx_moe_layer_forward_ex", "mx_moe_workspace_bytes", "mx_moe_workspace_init",
             "mx_moe_route", "mx_moe_stack_forward", "mx_moe_stack_workspace_bytes", "mx_status_string",
-            "mx_last_error_string", "mx_version", "mx_moe_profile_enable", "mx_moe_profile_read")
+            "mx_last_error_string", "mx_version", "mx_moe_profile_enable", "mx_moe_profile_read",
+            "mx_moe_workspace_check")
 
 
 class MxError(RuntimeError):
@@ -87,9 +88,11 @@ def lib():
             L.mx_last_error_string.restype = C.c_char_p
             L.mx_version.restype = C.c_char_p
             L.mx_moe_profile_enable.argtypes = [I32]
+            L.mx_moe_workspace_check.argtypes = [P, P]
             L.mx_moe_profile_read.argtypes = [C.POINTER(C.c_double), C.POINTER(C.c_int), I32]
             for name in ("mx_moe_layer_forward", "mx_moe_layer_forward_ex", "mx_moe_workspace_init",
-                         "mx_moe_route", "mx_moe_stack_forward", "mx_moe_profile_enable", "mx_moe_profile_read"):
+                         "mx_moe_route", "mx_moe_stack_forward", "mx_moe_profile_enable", "mx_moe_profile_read",
+                         "mx_moe_workspace_check"):
                 getattr(L, name).restype = C.c_int
             _lib = L
     return _lib
@@ -187,6 +190,11 @@ def stack_workspace_bytes(layout: Layout, T: int) -> int:
 
 def workspace_init(ws, nbytes: int, stream=None):
     _check(lib().mx_moe_workspace_init(_ptr(ws), nbytes, _stream_handle(stream)))
+
+
+def workspace_check(ws, stream=None):
+    """Raise MxError(MX_ERR_DEVICE_TIMEOUT) if a device-side wait gave up."""
+    _check(lib().mx_moe_workspace_check(_ptr(ws), _stream_handle(stream)))
 
 
 def layer_forward(x, T, layer: DeviceLayer, out, topk_idx, topk_w):

@@ -113,7 +113,7 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb)
 // Workspace plan.  Offsets are 256-byte aligned; the ticket counters come first
 // so mx_moe_workspace_init only needs to clear the front.
 struct Plan {
-    size_t tickets, logits, counts, offsets, perm, tiles, ntiles, xp, hr0, hr1, hs0, hs1, total;
+    size_t err, tickets, logits, counts, offsets, perm, tiles, ntiles, xp, xg, hr0, hr1, hs0, hs1, total;
     int max_tiles_route;
 };
 
@@ -127,6 +127,7 @@ Plan make_plan(const mx_moe_layout *L, int T_route, int T_ffn)
         o += up256(bytes);
         return at;
     };
+    p.err = take(sizeof(unsigned));  // offset 0: device error word (bounded waits)
     p.tickets = take(((size_t)T_route + 2) * sizeof(unsigned));
     p.logits = take((size_t)T_route * E * 4);
     p.counts = take(E * 4);
@@ -136,6 +137,7 @@ Plan make_plan(const mx_moe_layout *L, int T_route, int T_ffn)
     p.tiles = take((size_t)3 * p.max_tiles_route * 4);
     p.ntiles = take(4);
     p.xp = take((size_t)3 * T_ffn * D * 2);
+    p.xg = take((size_t)T_ffn * (D / 64) * 4);
     p.hr0 = take((size_t)T_ffn * K * I * 2);
     p.hr1 = take((size_t)T_ffn * K * I * 2);
     p.hs0 = take((size_t)T_ffn * S * 2);
@@ -241,7 +243,9 @@ RouteArgs route_args(const void *x, int T, const mx_qlinear *router, const mx_mo
     a.tiles = reinterpret_cast<int32_t *>(ws + p.tiles);
     a.n_tiles = reinterpret_cast<int32_t *>(ws + p.ntiles);
     a.tickets = reinterpret_cast<unsigned *>(ws + p.tickets);
+    a.err = reinterpret_cast<unsigned *>(ws + p.err);
     a.xp = reinterpret_cast<uint16_t *>(ws + p.xp);
+    a.xg = reinterpret_cast<float *>(ws + p.xg);
     a.nsplit = L->act_dtype == MX_BF16 ? 1 : 3;
     return a;
 }
@@ -254,9 +258,11 @@ mx_status run_pass(const void *x, int T, const mx_qlinear *router, const mx_ffn 
     RouteArgs ra = route_args(x, T, router, L, opt, p, ws);
     ra.topk_idx = topk_idx;
     ra.topk_w = topk_w;
-    const RouteLaunch rl = route_plan(T, L->d_model, L->n_experts);
+    ra.logits_only = 0;
+    const RouteLaunch rl = route_plan(T, L->d_model, L->n_experts, L->top_k);
     ra.ET = rl.ET;
     ra.GC = rl.GC;
+    ra.cluster = rl.cluster;
     prof_begin(kStageRoute, s);
     cudaError_t e = launch_route(ra, rl, s);
     prof_end(kStageRoute, s);
@@ -268,6 +274,7 @@ mx_status run_pass(const void *x, int T, const mx_qlinear *router, const mx_ffn 
     f.D = L->d_model;
     f.I = L->d_expert;
     f.S = L->d_shared;
+    f.E = L->n_experts;
     f.K = L->top_k;
     f.blob = static_cast<const uint8_t *>(blob);
     f.stride = L->record_stride;
@@ -284,11 +291,15 @@ mx_status run_pass(const void *x, int T, const mx_qlinear *router, const mx_ffn 
         f.sb[j] = static_cast<const uint16_t *>(sq[j]->biases);
     }
     f.xp = ra.xp;
+    f.xg = ra.xg;
     f.nsplit = ra.nsplit;
+    f.logits = ra.logits;
+    f.pes = L->per_expert_scale;
+    f.topk_idx = topk_idx;
+    f.topk_w = topk_w;
     f.perm = ra.perm;
     f.tiles = ra.tiles;
     f.n_tiles = ra.n_tiles;
-    f.topk_w = topk_w;
     f.hr[0] = reinterpret_cast<uint16_t *>(ws + p.hr0);
     f.hr[1] = reinterpret_cast<uint16_t *>(ws + p.hr1);
     f.hs[0] = reinterpret_cast<uint16_t *>(ws + p.hs0);
@@ -297,6 +308,7 @@ mx_status run_pass(const void *x, int T, const mx_qlinear *router, const mx_ffn 
     f.out = out;
     f.act_dtype = L->act_dtype == MX_BF16 ? 1 : 0;
     f.lam = L->layer_scalar;
+    f.err = ra.err;
     const int max_tiles = T * L->top_k < L->n_experts ? T * L->top_k : L->n_experts;
     e = launch_ffn_decode(f, max_tiles, num_sms(), s);
     if (e != cudaSuccess)
@@ -387,6 +399,22 @@ mx_status mx_moe_workspace_init(void *ws, size_t ws_bytes, void *stream)
     return MX_OK;
 }
 
+mx_status mx_moe_workspace_check(const void *ws, void *stream)
+{
+    if (!ws)
+        return fail(MX_ERR_INVALID_ARG, "workspace is NULL");
+    unsigned word = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "reading the workspace error word");
+    if (word != 0)
+        return fail(MX_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (error word 0x%x)", word);
+    return MX_OK;
+}
+
 mx_status mx_moe_layer_forward_ex(const void *x, int T, const mx_qlinear *router, const mx_ffn *shared,
                                   const void *expert_blob, const mx_moe_layout *layout, void *out,
                                   int32_t *topk_idx, float *topk_w, const mx_moe_options *opt, void *stream,
@@ -466,9 +494,10 @@ mx_status mx_moe_route(const void *x, int T, const mx_qlinear *router, const mx_
     if (logits)
         a.logits = logits;
     a.xp = nullptr;
-    const RouteLaunch rl = route_plan(T, layout->d_model, layout->n_experts);
+    const RouteLaunch rl = route_plan(T, layout->d_model, layout->n_experts, layout->top_k);
     a.ET = rl.ET;
     a.GC = rl.GC;
+    a.cluster = rl.cluster;
     prof_begin(kStageRoute, static_cast<cudaStream_t>(stream));
     cudaError_t e = launch_route(a, rl, static_cast<cudaStream_t>(stream));
     prof_end(kStageRoute, static_cast<cudaStream_t>(stream));

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mx {
@@ -37,37 +38,69 @@ struct RouteArgs {
     unsigned *tickets;      // [n_token_tiles + 1], zero on entry, zero on exit
     uint16_t *xp;           // FFN operand: [nsplit][T][D] bf16 in operand column order, nullable
     int nsplit;             // 1 (bf16 activations) or 3 (fp32 activations)
+    float *xg;              // FFN operand: [T][D/64] per-group sums of x (with xp)
     int ET, GC;             // experts per CTA, groups per chunk
+    int logits_only;        // 1: stop after the logits
+    int cluster;            // 1: one thread-block cluster; CTA 0 gathers the logits and routes
+    unsigned *err;          // device error word (bounded waits that gave up)
 };
 
 struct FfnArgs {
-    int T, D, I, S, K;
+    int T, D, I, S, E, K;
     const uint8_t *blob;
     uint64_t stride;
     uint64_t off_w[3], off_s[3], off_b[3];  // gate, up, down inside a record
     const uint32_t *sw[3];                  // shared gate, up, down packed words
     const uint16_t *ss[3];
     const uint16_t *sb[3];
-    const uint16_t *xp;                     // [nsplit][T][D]
+    const uint16_t *xp;                     // [nsplit][T][D] x operand (operand column order)
     int nsplit;
-    const int32_t *perm;
-    const int32_t *tiles;
+    const float *xg;                        // [T][D/64] per-group sums of x
+    const float *logits;                    // [T][E] router logits
+    const float *pes;                       // per-expert scale, nullable
+    const int32_t *topk_idx;                // [T][K] routing (written by the router kernel)
+    const float *topk_w;                    // [T][K]
+    const int32_t *perm;                    // [T*K] slots grouped by expert
+    const int32_t *tiles;                   // [3][n] (expert, begin, end)
     const int32_t *n_tiles;
-    const float *topk_w;
     uint16_t *hr[2];                        // routed hidden, hi/lo [T*K][I]
     uint16_t *hs[2];                        // shared hidden, hi/lo [T][S]
     const void *residual;                   // nullable
     void *out;
     int act_dtype;
     float lam;
+    unsigned *err;                          // device error word
 };
+
+// Shapes of the weight-streaming kernels (host-computed; byte offsets into
+// dynamic shared memory).
+struct GuLaunch {
+    int stages, slot_bytes, n_shared, tpt, max_tiles;
+    int off_meta, off_xs, off_xg, off_ring, off_part;
+};
+struct DnLaunch {
+    int stages, slot_bytes, max_tiles;
+    int off_meta, off_ring, off_acc;
+};
+
+// TMA tensor maps of one layer's expert weights (mx_tma.cu): routed gate, up,
+// down over all experts of the blob, and the shared expert's three matrices.
+struct FfnMaps {
+    CUtensorMap gate, up, down, sgate, sup, sdown;
+};
+cudaError_t get_ffn_maps(const FfnArgs &a, FfnMaps *out);
 
 // Launch configuration of the routing kernel for T tokens.
 struct RouteLaunch {
     int TT, ET, GC, n_tt, n_et;
+    int cluster;            // cluster mode (T <= kClusterTokens): n_et CTAs form one cluster
+    size_t off_gather;      // cluster mode: byte offset of the gathered logits [T][E]
+    size_t off_route;       // cluster mode: byte offset of the routing scratch
     size_t smem;
 };
-RouteLaunch route_plan(int T, int D, int E);
+constexpr int kClusterTokens = 8;
+constexpr int kClusterCtas = 8;
+RouteLaunch route_plan(int T, int D, int E, int K);
 cudaError_t launch_route(const RouteArgs &a, const RouteLaunch &L, cudaStream_t s);
 
 // Decode-path FFN: gate/up + GeGLU, then down + combine.  The two launches are

@@ -17,6 +17,7 @@
 // the top-k of those tokens; the last token tile groups all T*K slots by
 // expert.  Tickets return to zero, so the workspace is ready for the next call.
 #include "mx_common.cuh"
+#include "mx_cta_route.cuh"
 #include "mx_internal.h"
 
 #include <climits>
@@ -35,6 +36,35 @@ __device__ __forceinline__ float load_x(const RouteArgs &a, int t, int col)
     if (a.x_dtype == 1)
         return bf2f(__ldg(reinterpret_cast<const uint16_t *>(a.x) + i));
     return __ldg(reinterpret_cast<const float *>(a.x) + i);
+}
+
+// The 64 activations of group g of token t, with 16-byte loads.
+__device__ __forceinline__ void load_group(const RouteArgs &a, int t, int g, float (&v)[kGroup])
+{
+    const size_t i = (size_t)t * a.D + (size_t)g * kGroup;
+    if (a.x_dtype == 1) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(reinterpret_cast<const uint16_t *>(a.x) + i);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint4 w = __ldg(p + j);
+            const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                v[8 * j + 2 * k] = __uint_as_float(u[k] << 16);
+                v[8 * j + 2 * k + 1] = __uint_as_float(u[k] & 0xFFFF0000u);
+            }
+        }
+    } else {
+        const float4 *p = reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(a.x) + i);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float4 w = __ldg(p + j);
+            v[4 * j] = w.x;
+            v[4 * j + 1] = w.y;
+            v[4 * j + 2] = w.z;
+            v[4 * j + 3] = w.w;
+        }
+    }
 }
 
 // Top-k of the logits of tokens [t0, t0+nt): one warp per token.
@@ -111,6 +141,7 @@ __device__ void group_slots(const RouteArgs &a, float *sm)
     int *base = wc + kWarps * E;             // [kWarps][E] per-warp running bases
     int *cnt = base + kWarps * E;            // [E]
     int *off = cnt + E;                      // [E]
+    int *tix = off + E;                      // [E] first tile slot of each expert
     for (int i = threadIdx.x; i < kWarps * E; i += kThreads)
         wc[i] = 0;
     __syncthreads();
@@ -135,14 +166,37 @@ __device__ void group_slots(const RouteArgs &a, float *sm)
         a.counts[e] = run;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        int o = 0;
-        for (int e = 0; e < E; ++e) {
-            off[e] = o;
-            a.offsets[e] = o;
-            o += cnt[e];
+    // exclusive scans over experts (counts -> offsets, tiles per expert -> tile
+    // slots), by warp 0 with a shuffle scan of per-lane partial sums
+    if (warp == 0) {
+        const int per = (E + 31) / 32, e_lo = lane * per, e_hi = min(E, e_lo + per);
+        int sc = 0, st = 0;
+        for (int e = e_lo; e < e_hi; ++e) {
+            sc += cnt[e];
+            st += (cnt[e] + kTileTokens - 1) / kTileTokens;
         }
-        a.offsets[E] = o;
+        int ic = sc, is = st;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int vc = __shfl_up_sync(0xffffffffu, ic, o), vs = __shfl_up_sync(0xffffffffu, is, o);
+            if (lane >= o) {
+                ic += vc;
+                is += vs;
+            }
+        }
+        int oc = ic - sc, os = is - st;
+        for (int e = e_lo; e < e_hi; ++e) {
+            off[e] = oc;
+            a.offsets[e] = oc;
+            tix[e] = os;
+            oc += cnt[e];
+            os += (cnt[e] + kTileTokens - 1) / kTileTokens;
+        }
+        if (lane == 31) {
+            a.offsets[E] = ic;
+            if (a.n_tiles)
+                *a.n_tiles = is;
+        }
     }
     __syncthreads();
     const unsigned lt = (1u << lane) - 1u;
@@ -157,21 +211,24 @@ __device__ void group_slots(const RouteArgs &a, float *sm)
             base[warp * E + e] += __popc(m);
         __syncwarp();
     }
-    if (a.tiles && threadIdx.x == 0) {
-        int nt = 0;
-        for (int e = 0; e < E; ++e)
-            for (int b = 0; b < cnt[e]; b += kTileTokens) {
-                a.tiles[3 * nt + 0] = e;
-                a.tiles[3 * nt + 1] = off[e] + b;
-                a.tiles[3 * nt + 2] = off[e] + min(b + kTileTokens, cnt[e]);
-                ++nt;
+    if (a.tiles) {
+        for (int e = threadIdx.x; e < E; e += kThreads) {
+            int t = tix[e];
+            for (int b = 0; b < cnt[e]; b += kTileTokens, ++t) {
+                a.tiles[3 * t + 0] = e;
+                a.tiles[3 * t + 1] = off[e] + b;
+                a.tiles[3 * t + 2] = off[e] + min(b + kTileTokens, cnt[e]);
             }
-        *a.n_tiles = nt;
+        }
     }
 }
 
+struct RouteSync {
+    __device__ void operator()() const { __syncthreads(); }
+};
+
 template <int TT>
-__global__ void __launch_bounds__(kThreads) route_kernel(const RouteArgs a)
+__global__ void __launch_bounds__(kThreads) route_kernel(const RouteArgs a, const RouteLaunch RL)
 {
     extern __shared__ __align__(16) float sm[];
     __shared__ int s_last;
@@ -187,29 +244,54 @@ __global__ void __launch_bounds__(kThreads) route_kernel(const RouteArgs a)
     float *rn = sB + ET * G;                // [TT]
     const bool prep = (blockIdx.x == 0) && a.xp != nullptr;
 
+    // Let the next kernel (gate/up) launch now: its producer streams the shared
+    // expert's weights while this kernel runs; it waits for our results itself.
+    pdl_trigger();
+    // Router scales, biases and the first chunk's packed bytes do not depend on
+    // the previous kernel: load them before waiting for it.
     for (int i = tid; i < ne * G; i += kThreads) {
         const size_t j = (size_t)e0 * G + i;
         sS[i] = bf2f(__ldg(a.rs + j));
         sB[i] = bf2f(__ldg(a.rb + j));
     }
+    const int my_el = tid % ET, my_gl = tid / ET;
+    const bool my_pair = tid < ET * min(GC, G) && my_el < ne;
+    uint4 qv[4];
+    if (my_pair) {
+        const uint32_t *q = a.rw + (size_t)(e0 + my_el) * (D / 4) + (size_t)my_gl * 16;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            qv[j] = ldg_u4(q + 4 * j);
+    }
+    pdl_wait();
+
     if (a.pre_norm) {
         // rmsnorm_no_scale, canonical order: per group an fma chain of squares,
         // groups summed ascending, r = 1/sqrtf(ss/D + eps).
         float *tmp = Xs;  // [TT][G]; Xs is filled only after this
         for (int i = tid; i < nt * G; i += kThreads) {
             const int t = i / G, g = i % G;
+            float v[kGroup];
+            load_group(a, t0 + t, g, v);
             float p = 0.0f;
-            for (int k = 0; k < kGroup; ++k) {
-                const float v = load_x(a, t0 + t, g * kGroup + k);
-                p = fmaf(v, v, p);
-            }
+#pragma unroll
+            for (int k = 0; k < kGroup; ++k)
+                p = fmaf(v[k], v[k], p);
             tmp[t * G + g] = p;
         }
         __syncthreads();
         if (tid < nt) {
             float ss = 0.0f;
-            for (int g = 0; g < G; ++g)
-                ss = ss + tmp[tid * G + g];
+            for (int gb = 0; gb < G; gb += 8) {
+                float v8[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    v8[j] = tmp[tid * G + min(gb + j, G - 1)];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (gb + j < G)
+                        ss = ss + v8[j];
+            }
             rn[tid] = 1.0f / sqrtf(ss / (float)D + a.eps);
         }
         __syncthreads();
@@ -251,20 +333,32 @@ __global__ void __launch_bounds__(kThreads) route_kernel(const RouteArgs a)
         __syncthreads();
         for (int i = tid; i < nt * gc; i += kThreads) {
             const int t = i / gc, gl = i % gc;
-            const float *xr = xs + (t * GC + gl) * kXPad;
+            const float4 *xr = reinterpret_cast<const float4 *>(xs + (t * GC + gl) * kXPad);
+            float4 v[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                v[j] = xr[j];
             float s = 0.0f;
-            for (int k = 0; k < kGroup; ++k)
-                s = s + xr[k];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                s = s + v[j].x;
+                s = s + v[j].y;
+                s = s + v[j].z;
+                s = s + v[j].w;
+            }
             Xs[t * G + c0 + gl] = s;
+            if (prep)
+                a.xg[(size_t)(t0 + t) * G + c0 + gl] = s;
         }
         if (tid < ET * gc) {
-            const int el = tid % ET, gl = tid / ET;
+            const int el = my_el, gl = my_gl;
             if (el < ne) {
-                const uint32_t *q = a.rw + (size_t)(e0 + el) * (D / 4) + (size_t)(c0 + gl) * 16;
-                uint4 qv[4];
+                if (c0 > 0) {
+                    const uint32_t *q = a.rw + (size_t)(e0 + el) * (D / 4) + (size_t)(c0 + gl) * 16;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    qv[j] = ldg_u4(q + 4 * j);
+                    for (int j = 0; j < 4; ++j)
+                        qv[j] = ldg_u4(q + 4 * j);
+                }
                 float P[TT];
 #pragma unroll
                 for (int t = 0; t < TT; ++t)
@@ -299,10 +393,23 @@ __global__ void __launch_bounds__(kThreads) route_kernel(const RouteArgs a)
             if (p < npairs) {
                 const int t = p / ne, el = p % ne;
                 float v = acc[i];
-                for (int gl = 0; gl < gc; ++gl) {
-                    const int g = c0 + gl;
-                    v = fmaf(sS[el * G + g], Ps[(t * ET + el) * GC + gl], v);
-                    v = fmaf(sB[el * G + g], Xs[t * G + g], v);
+                for (int gb = 0; gb < gc; gb += 8) {
+                    float ps[8], xs8[8], ss8[8], bs8[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const int gl = min(gb + j, gc - 1), g = c0 + gl;
+                        ss8[j] = sS[el * G + g];
+                        bs8[j] = sB[el * G + g];
+                        ps[j] = Ps[(t * ET + el) * GC + gl];
+                        xs8[j] = Xs[t * G + g];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        if (gb + j < gc) {
+                            v = fmaf(ss8[j], ps[j], v);
+                            v = fmaf(bs8[j], xs8[j], v);
+                        }
+                    }
                 }
                 acc[i] = v;
             }
@@ -318,6 +425,48 @@ __global__ void __launch_bounds__(kThreads) route_kernel(const RouteArgs a)
         }
     }
 
+    if (a.cluster) {
+        // Deliver this CTA's logits to CTA 0 of the cluster (distributed shared
+        // memory), then CTA 0 routes all T tokens and publishes the result.
+        float *gather = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(sm) + RL.off_gather);
+#pragma unroll
+        for (int i = 0; i < kAcc; ++i) {
+            const int p = tid + i * kThreads;
+            if (p < npairs) {
+                const int t = p / ne, el = p % ne;
+                uint32_t remote;
+                asm volatile("mapa.shared::cluster.u32 %0, %1, 0;"
+                             : "=r"(remote)
+                             : "r"(smem_u32(gather + t * E + e0 + el)));
+                asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(acc[i]) : "memory");
+            }
+        }
+        asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+        if (blockIdx.x != 0)
+            return;
+        const CtaRoute rt = cta_route_carve(reinterpret_cast<uint8_t *>(sm) + RL.off_route, a.T, E, a.K);
+        cta_route(gather, a.T, E, a.K, a.pes, rt, RouteSync{});
+        const int tk = a.T * a.K;
+        for (int i = tid; i < tk; i += kThreads) {
+            a.topk_idx[i] = rt.topk_idx[i];
+            a.topk_w[i] = rt.topk_w[i];
+            a.perm[i] = rt.perm[i];
+        }
+        for (int e = tid; e < E; e += kThreads) {
+            a.counts[e] = rt.cnt[e];
+            a.offsets[e] = rt.off[e];
+        }
+        const int nt_tiles = *rt.n_tiles;
+        for (int i = tid; i < 3 * nt_tiles; i += kThreads)
+            a.tiles[i] = rt.tiles[i];
+        if (tid == 0) {
+            a.offsets[E] = rt.off[E];
+            *a.n_tiles = nt_tiles;
+        }
+        return;
+    }
+    if (a.logits_only)
+        return;
     // last expert tile of this token tile: top-k
     __threadfence();
     __syncthreads();
@@ -360,13 +509,30 @@ cudaError_t launch_tt(const RouteArgs &a, const RouteLaunch &L, cudaStream_t s)
             return e;
         configured = L.smem;
     }
-    k<<<dim3(L.n_et, L.n_tt), kThreads, L.smem, s>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.n_et, L.n_tt);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int n = 1;
+    if (L.cluster) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = L.n_et;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, k, a, L);
 }
 
 } // namespace
 
-RouteLaunch route_plan(int T, int D, int E)
+RouteLaunch route_plan(int T, int D, int E, int K)
 {
     RouteLaunch L{};
     const int G = D / kGroup;
@@ -378,33 +544,50 @@ RouteLaunch route_plan(int T, int D, int E)
         L.TT = 8;
     else
         L.TT = 32;
-    if (L.TT <= 4) {
-        L.GC = G;
-    } else if (L.TT == 8) {
-        L.GC = G < 32 ? G : 32;
+    L.cluster = T <= kClusterTokens;
+    if (L.cluster) {
+        // one cluster: the experts split over kClusterCtas CTAs
+        int et = (E + kClusterCtas - 1) / kClusterCtas;
+        L.ET = et;
+        int gc = kThreads / et;
+        L.GC = gc < 1 ? 1 : (gc > G ? G : gc);
     } else {
-        L.GC = G < 8 ? G : 8;
+        if (L.TT <= 4)
+            L.GC = G;
+        else if (L.TT == 8)
+            L.GC = G < 32 ? G : 32;
+        else
+            L.GC = G < 8 ? G : 8;
+        int et = kThreads / L.GC;
+        if (et * L.TT > 1024)
+            et = 1024 / L.TT;
+        if (et > E)
+            et = E;
+        if (et < 1)
+            et = 1;
+        L.ET = et;
     }
-    int et = kThreads / L.GC;
-    if (et * L.TT > 1024)
-        et = 1024 / L.TT;
-    if (et > E)
-        et = E;
-    if (et < 1)
-        et = 1;
-    L.ET = et;
     L.n_tt = (T + L.TT - 1) / L.TT;
-    L.n_et = (E + et - 1) / et;
+    L.n_et = (E + L.ET - 1) / L.ET;
     const size_t main_f = (size_t)L.TT * L.GC * kXPad + (size_t)L.TT * L.ET * L.GC + (size_t)L.TT * G +
                           2 * (size_t)L.ET * G + L.TT;
     const size_t topk_f = (size_t)kWarps * E + (size_t)kWarps * ((E + 31) / 32);
-    const size_t group_f = 2 * (size_t)kWarps * E + 2 * (size_t)E;
+    const size_t group_f = 2 * (size_t)kWarps * E + 3 * (size_t)E;
     size_t f = main_f;
-    if (topk_f > f)
-        f = topk_f;
-    if (group_f > f)
-        f = group_f;
-    L.smem = f * sizeof(float);
+    if (!L.cluster) {
+        if (topk_f > f)
+            f = topk_f;
+        if (group_f > f)
+            f = group_f;
+    }
+    size_t bytes = ((f * sizeof(float)) + 127) & ~size_t(127);
+    if (L.cluster) {
+        L.off_gather = bytes;
+        bytes += (((size_t)T * E * sizeof(float)) + 127) & ~size_t(127);
+        L.off_route = bytes;
+        bytes += cta_route_bytes(T, E, K);
+    }
+    L.smem = bytes;
     return L;
 }
 

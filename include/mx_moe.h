@@ -164,6 +164,15 @@ MX_API size_t mx_moe_workspace_bytes(const mx_moe_layout *layout, int T_max);
 MX_API mx_status mx_moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * Device-side error word of a workspace.  Kernels that wait on asynchronous
+ * copies give up after a bounded time, record it in the workspace's first word
+ * and skip their math; this call synchronises on `stream`, reads the word, and
+ * returns MX_ERR_DEVICE_TIMEOUT if it is set (MX_OK otherwise).  The word stays
+ * set until the workspace is re-initialised (mx_moe_workspace_init).
+ */
+MX_API mx_status mx_moe_workspace_check(const void *ws, void *stream);
+
+/*
  * Routing alone (router GEMV + top-k + softmax + grouping), for exact checks.
  *   topk_idx  device int32 [T][K];  topk_w device fp32 [T][K]
  *   counts    device int32 [E]      tokens per expert

@@ -52,6 +52,7 @@ def run_block(dev: mx.DeviceLayer, x: np.ndarray, residual: np.ndarray | None = 
         rd = to_dev(residual) if residual is not None else None
         mx.layer_forward_ex(xd, T, dev, out, idx, w, ws.t, ws.nbytes, stream=torch.cuda.current_stream(),
                             residual=rd, pre_rmsnorm=pre_norm, rms_eps=eps)
+        mx.workspace_check(ws.t, torch.cuda.current_stream())
     else:
         assert residual is None and not pre_norm
         mx.layer_forward(xd, T, dev, out, idx, w)

@@ -169,7 +169,17 @@ def test_prefill_route_exact_and_sampled_outputs(orc, gu, ci):
 
 def test_decode_stack_30_layers(orc, gu):
     """Single-token decode through the 30-layer stack (RMSNorm -> block ->
-    residual), free-running on both sides from the same input."""
+    residual).
+
+    Per layer on identical inputs: layer l of the GPU path is fed the oracle's
+    own output of layer l-1 (inputs flow from the oracle to the GPU, never
+    back); top-k exact, routing weights rel-L2 <= 1e-4, output within the BF16
+    bars.  Free-running through the stack entry point from the same input:
+    top-k exact in every layer, and the stack entry point equal bit for bit to
+    the chain of single-layer calls.  Free-running, the two sides' residual
+    streams may round differently to BF16 in a few elements per layer, and the
+    difference grows with depth; the final output is held to the BF16 bars and
+    the routing weights to 5e-3."""
     import expert_ffn_gb300 as mx
     cfg = synth.CONFIGS[1]
     layers = [synth.make_layer(cfg, l) for l in range(cfg.layers)]
@@ -177,13 +187,30 @@ def test_decode_stack_30_layers(orc, gu):
     devs = [mx.DeviceLayer(l, mx.MX_BF16) for l in layers]
     stack = mx.Stack(devs)
     T, K, n = cfg.T, cfg.K, cfg.layers
+    xs_ref, idx_ref, w_ref = orc.stack_forward(layers, x, 1e-6)
+
+    ws1 = gu.Workspace(mx.workspace_bytes(devs[0].layout, T))
+    for l in range(n):
+        xin = x if l == 0 else xs_ref[l - 1]
+        out, li, lw = gu.run_block(devs[l], xin, residual=xin, pre_norm=True, eps=1e-6, ws=ws1)
+        assert np.array_equal(li, idx_ref[l]), l
+        assert rel_l2(lw, w_ref[l]) <= 1e-4, (l, rel_l2(lw, w_ref[l]))
+        check_out(out, xs_ref[l], "bf16")
+
     xd = gu.to_dev(x)
     idx = torch.full((n, T, K), -1, dtype=torch.int32, device="cuda")
     w = torch.zeros((n, T, K), dtype=torch.float32, device="cuda")
     ws = gu.Workspace(mx.stack_workspace_bytes(devs[0].layout, T))
     mx.stack_forward(xd, T, stack, idx, w, ws.t, ws.nbytes, rms_eps=1e-6, stream=torch.cuda.current_stream())
     torch.cuda.synchronize()
-    xs_ref, idx_ref, w_ref = orc.stack_forward(layers, x, 1e-6)
-    assert np.array_equal(idx.cpu().numpy(), idx_ref)
-    assert rel_l2(w.cpu().numpy(), w_ref) <= 1e-4
-    check_out(gu.to_host(xd, np.uint16), xs_ref[-1], "bf16")
+    idx, w = idx.cpu().numpy(), w.cpu().numpy()
+    x_final = gu.to_host(xd, np.uint16)
+    cur = x
+    for l in range(n):
+        out, li, lw = gu.run_block(devs[l], cur, residual=cur, pre_norm=True, eps=1e-6, ws=ws1)
+        assert np.array_equal(li, idx[l]) and np.array_equal(lw, w[l])
+        cur = out
+    assert np.array_equal(x_final, cur)
+    assert np.array_equal(idx, idx_ref)
+    assert rel_l2(w, w_ref) <= 5e-3
+    check_out(x_final, xs_ref[-1], "bf16")
