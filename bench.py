@@ -38,8 +38,9 @@ import synth  # noqa: E402
 METRIC = "MoE-layer tokens/s; decode HBM GB/s and prefill TFLOP/s as % of GB300 roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
-KERNEL_SOURCES = ("expert_ffn_gb300/csrc/mx_ffn_decode.cu", "expert_ffn_gb300/csrc/mx_common.cuh",
-                  "expert_ffn_gb300/csrc/mx_route.cu")
+KERNEL_SOURCES = ("expert_ffn_gb300/csrc/mx_decode.cu", "expert_ffn_gb300/csrc/mx_ffn_decode.cu",
+                  "expert_ffn_gb300/csrc/mx_common.cuh", "expert_ffn_gb300/csrc/mx_route.cu")
+PD_MAX_T, PD_MAX_LAYERS = 4, 30  # single-launch decode path: tokens per call, layers per launch
 
 
 # ------------------------------------------------------------------ helpers
@@ -302,12 +303,21 @@ def bench_ours(args, cfg, world, rank, local, pg):
     d2h = T * D * es + n_layers * T * K * 8
 
     workload = cfg.name
-    achieved = gu_bytes_per_launch / gu_s / 1e9
-    roof = {"bound": "hbm", "kernel": "gateup_kernel", "achieved": round(achieved, 1),
+    single = T <= PD_MAX_T and os.environ.get("MX_MOE_SINGLE_LAUNCH", "1") != "0"
+    if single:
+        # one persistent launch runs every layer of the step (up to 30 per launch):
+        # its algorithmic bytes are the whole step's
+        launches = -(-n_layers // PD_MAX_LAYERS)
+        kname, bytes_launch = "pd_kernel", step_bytes / launches
+    else:
+        launches = n_layers * 3 * ((T + 63) // 64)
+        kname, bytes_launch = "gateup_kernel", gu_bytes_per_launch
+    achieved = bytes_launch / gu_s / 1e9
+    roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "peak_source": peak_src,
-            "traffic": committed_traffic("gateup_kernel", workload),
-            "bytes_per_launch": int(gu_bytes_per_launch), "launch_us": round(gu_s * 1e6, 2),
+            "traffic": committed_traffic(kname, workload),
+            "bytes_per_launch": int(bytes_launch), "launch_us": round(gu_s * 1e6, 2),
             "launches_timed": gu_n}
     step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     stages_us = {k: round(v[0] * 1e3 / max(v[1], 1), 2) for k, v in prof.items()}
@@ -330,7 +340,7 @@ def bench_ours(args, cfg, world, rank, local, pg):
         "e2e": {"value": round(world * args.steps * T / (e2e_ms / 1e3), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host input copied in, the C-ABI call (no graph), outputs copied out, every step"},
-        "gpu_launches": args.steps * n_layers * 3 * ((T + 63) // 64),
+        "gpu_launches": args.steps * launches,
         "device": dev_name, "gen_s": round(gen_s, 1),
     }
     if rank == 0 and not args.no_cpu_baseline:

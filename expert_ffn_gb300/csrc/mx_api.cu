@@ -11,6 +11,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -113,7 +114,11 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb)
 // Workspace plan.  Offsets are 256-byte aligned; the ticket counters come first
 // so mx_moe_workspace_init only needs to clear the front.
 struct Plan {
-    size_t err, tickets, logits, counts, offsets, perm, tiles, ntiles, xp, xg, hr0, hr1, hs0, hs1, total;
+    size_t err, tickets, logits, counts, offsets, perm, tiles, ntiles, xp, xg, hr0, hr1, hs0, hs1;
+    // single-launch decode path (T <= kPdMaxT)
+    size_t pd_ctr, pd_logits, pd_h, pd_hs, pd_y, pd_x;
+    int pd_T;
+    size_t total;
     int max_tiles_route;
 };
 
@@ -142,6 +147,16 @@ Plan make_plan(const mx_moe_layout *L, int T_route, int T_ffn)
     p.hr1 = take((size_t)T_ffn * K * I * 2);
     p.hs0 = take((size_t)T_ffn * S * 2);
     p.hs1 = take((size_t)T_ffn * S * 2);
+    // single-launch decode path, sized for min(T, kPdMaxT) tokens
+    const size_t Tp = T_ffn < kPdMaxT ? T_ffn : kPdMaxT;
+    const size_t es = L->act_dtype == MX_F32 ? 4 : 2;
+    p.pd_T = (int)Tp;
+    p.pd_ctr = take(pd_ctr_ints((int)E, kPdMaxLayers) * 4);
+    p.pd_logits = take(Tp * E * 4);
+    p.pd_h = take(Tp * K * I * 4);
+    p.pd_hs = take(Tp * S * 4);
+    p.pd_y = take((size_t)kPdMaxLayers * Tp * D * 8);
+    p.pd_x = take(Tp * D * es);
     p.total = o;
     return p;
 }
@@ -164,6 +179,145 @@ int num_sms()
         cache[dev] = n;
     }
     return cache[dev];
+}
+
+// Device limits used by the single-launch path (cached per device).
+struct DevInfo {
+    int sms = 0, smem_optin = 0;
+};
+
+DevInfo dev_info()
+{
+    static std::mutex mu;
+    static DevInfo cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return DevInfo{};
+    std::lock_guard<std::mutex> g(mu);
+    DevInfo &d = cache[dev];
+    if (!d.sms) {
+        int n = 0, m = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&m, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return DevInfo{};
+        d.sms = n;
+        d.smem_optin = m;
+    }
+    return d;
+}
+
+// Whether T tokens of this layout take the single-launch path; fills its plan.
+// MX_MOE_SINGLE_LAUNCH=0 in the environment turns the path off (the block then
+// runs as separate router / gate-up / down launches).
+bool pd_usable(const mx_moe_layout *L, int T, PdSmem *sm, int *n_cta)
+{
+    if (T < 1 || T > kPdMaxT)
+        return false;
+    const char *env = getenv("MX_MOE_SINGLE_LAUNCH");
+    if (env && env[0] == '0')
+        return false;
+    const DevInfo d = dev_info();
+    if (!d.sms)
+        return false;
+    const int act = L->act_dtype == MX_BF16 ? 1 : 0;
+    // leave room for the kernel's static shared memory
+    if (!pd_plan(T, L->d_model, L->d_expert, L->d_shared, L->n_experts, L->top_k, act, d.sms, d.smem_optin - 2048,
+                 sm))
+        return false;
+    *n_cta = d.sms;
+    return true;
+}
+
+// One layer of the single-launch path.
+struct PdIn {
+    const mx_qlinear *router;
+    const mx_ffn *shared;
+    const void *blob;
+    const mx_moe_layout *L;
+    const void *x_in;      // used for the launch's first layer
+    void *x_out;           // nullable
+    const void *residual;  // res_mode 2
+    int res_mode;          // 0 none, 1 the layer input, 2 residual
+    int32_t *topk_idx;
+    float *topk_w;
+};
+
+mx_status run_pd(const PdIn *in, int n, int T, int pre_norm, float eps, const PdSmem &sm, int n_cta, const Plan &p,
+                 uint8_t *ws, cudaStream_t s)
+{
+    const mx_moe_layout *L0 = in[0].L;
+    static thread_local PdParams P;  // ~31 KB: kept off the stack
+    std::memset(&P, 0, sizeof P);
+    P.T = T;
+    P.D = L0->d_model;
+    P.I = L0->d_expert;
+    P.S = L0->d_shared;
+    P.E = L0->n_experts;
+    P.K = L0->top_k;
+    P.n_layers = n;
+    P.act = L0->act_dtype == MX_BF16 ? 1 : 0;
+    P.pre_norm = pre_norm;
+    P.eps = eps;
+    P.n_cta = n_cta;
+    P.err = reinterpret_cast<unsigned *>(ws + p.err);
+    P.ctr = reinterpret_cast<int *>(ws + p.pd_ctr);
+    P.cstride = 3 + P.E;
+    P.logits = reinterpret_cast<float *>(ws + p.pd_logits);
+    P.hbuf = reinterpret_cast<float *>(ws + p.pd_h);
+    P.hsbuf = reinterpret_cast<float *>(ws + p.pd_hs);
+    P.ybuf = reinterpret_cast<long long *>(ws + p.pd_y);
+    P.sm = sm;
+    for (int l = 0; l < n; ++l) {
+        const PdIn &c = in[l];
+        const mx_moe_layout *L = c.L;
+        PdLayer &d = P.L[l];
+        FfnArgs f{};
+        f.D = L->d_model;
+        f.I = L->d_expert;
+        f.S = L->d_shared;
+        f.E = L->n_experts;
+        f.blob = static_cast<const uint8_t *>(c.blob);
+        f.stride = L->record_stride;
+        const mx_sub *subs[3] = {&L->gate, &L->up, &L->down};
+        const mx_qlinear *sq[3] = {&c.shared->gate, &c.shared->up, &c.shared->down};
+        for (int j = 0; j < 3; ++j) {
+            f.off_w[j] = subs[j]->w;
+            d.off_s[j] = subs[j]->s;
+            d.off_b[j] = subs[j]->b;
+            f.sw[j] = static_cast<const uint32_t *>(sq[j]->w);
+            d.ss[j] = static_cast<const uint16_t *>(sq[j]->scales);
+            d.sb[j] = static_cast<const uint16_t *>(sq[j]->biases);
+        }
+        FfnMaps maps;
+        cudaError_t e = get_ffn_maps(f, &maps);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "encoding the weight tensor maps");
+        d.gate = maps.gate;
+        d.up = maps.up;
+        d.down = maps.down;
+        d.sgate = maps.sgate;
+        d.sup = maps.sup;
+        d.sdown = maps.sdownk;
+        d.rw = static_cast<const uint32_t *>(c.router->w);
+        d.rs = static_cast<const uint16_t *>(c.router->scales);
+        d.rb = static_cast<const uint16_t *>(c.router->biases);
+        d.blob = f.blob;
+        d.stride = L->record_stride;
+        d.pes = L->per_expert_scale;
+        d.topk_idx = c.topk_idx;
+        d.topk_w = c.topk_w;
+        d.x_in = c.x_in;
+        d.x_out = c.x_out;
+        d.residual = c.residual;
+        d.res_mode = c.res_mode;
+        d.lam = L->layer_scalar;
+    }
+    prof_begin(kStageGateUp, s);
+    cudaError_t e = launch_pd(P, s);
+    prof_end(kStageGateUp, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "single-launch decode kernel");
+    return MX_OK;
 }
 
 struct Call {
@@ -326,6 +480,14 @@ mx_status forward_impl(const Call &c, cudaStream_t s, void *ws, size_t ws_bytes)
     if (!aligned(ws, 256))
         return fail(MX_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
     uint8_t *w = static_cast<uint8_t *>(ws);
+    PdSmem sm;
+    int n_cta = 0;
+    if (c.T <= p.pd_T && pd_usable(c.L, c.T, &sm, &n_cta)) {
+        const void *res = c.opt ? c.opt->residual : nullptr;
+        const PdIn in{c.router, c.shared, c.blob, c.L, c.x, c.out, res, res ? 2 : 0, c.topk_idx, c.topk_w};
+        const int pre = (c.opt && c.opt->pre_rmsnorm) ? 1 : 0;
+        return run_pd(&in, 1, c.T, pre, c.opt ? c.opt->rms_eps : 0.0f, sm, n_cta, p, w, s);
+    }
     for (int t0 = 0; t0 < c.T; t0 += kDecodeChunk) {
         const int n = c.T - t0 < kDecodeChunk ? c.T - t0 : kDecodeChunk;
         mx_moe_options o{};
@@ -547,6 +709,33 @@ mx_status mx_moe_stack_forward(void *x_io, int T, int n_layers, const mx_qlinear
     if (T == 0)
         return MX_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    {
+        const Plan p = make_plan(L0, ffn_tokens(t1), ffn_tokens(t1));
+        PdSmem sm;
+        int n_cta = 0;
+        if (T <= p.pd_T && pd_usable(L0, T, &sm, &n_cta)) {
+            // all layers in launches of up to kPdMaxLayers: x stays on chip
+            // inside a launch; between launches it passes through the
+            // workspace; the last layer writes x_io
+            uint8_t *w = static_cast<uint8_t *>(ws);
+            static thread_local PdIn in[kPdMaxLayers];
+            for (int l0 = 0; l0 < n_layers; l0 += kPdMaxLayers) {
+                const int n = n_layers - l0 < kPdMaxLayers ? n_layers - l0 : kPdMaxLayers;
+                for (int i = 0; i < n; ++i) {
+                    const int l = l0 + i;
+                    const void *xin = l == 0 ? x_io : static_cast<const void *>(w + p.pd_x);
+                    void *xout = nullptr;
+                    if (i == n - 1)
+                        xout = l == n_layers - 1 ? x_io : static_cast<void *>(w + p.pd_x);
+                    in[i] = PdIn{&routers[l], &shareds[l], expert_blobs[l], &layouts[l], xin, xout, nullptr, 1,
+                                 topk_idx + (size_t)l * T * L0->top_k, topk_w + (size_t)l * T * L0->top_k};
+                }
+                if ((st = run_pd(in, n, T, 1, rms_eps, sm, n_cta, p, w, s)) != MX_OK)
+                    return st;
+            }
+            return MX_OK;
+        }
+    }
     for (int l = 0; l < n_layers; ++l) {
         const void *xin = (l % 2 == 0) ? x_io : xbuf;
         void *xout = (l % 2 == 0) ? static_cast<void *>(xbuf) : x_io;

@@ -1,0 +1,1392 @@
+// mx_decode.cu -- single-launch decode path: the whole block, or a stack of
+// blocks, for T <= 4 tokens in one persistent cooperative kernel.
+//
+// What it computes is the block of the "Mference System design" page
+// (section "Decode": router GEMV, top-8, softmax; the routed gated experts,
+// the unweighted shared expert and the layer scalar; section "Metal
+// execution": affine decode fused into the expert math, GeGLU and the weighted
+// expert reduction fused), for every layer of the call.
+//
+// Why one launch.  At T = 1 a layer streams ~37 MB of packed weights, about
+// 5.5 us of HBM time on this GPU, while the dependency chain of a layer (x ->
+// router -> top-k -> routed gate/up -> routed down -> next x) crosses the whole
+// grid three times.  Separate launches pay a ramp at every edge and leave HBM
+// idle meanwhile.  Here every SM runs one CTA for the whole call; CTAs hand
+// results to each other through global counters (bounded waits), and each CTA's
+// producer warp keeps loading weights whose addresses are already known -- the
+// shared expert's, also those of the next layer -- so the memory system stays
+// busy across the edges.  Every CTA keeps the residual stream x in its own
+// shared memory and rebuilds x_{l+1} from the summed down projections, so
+// layers hand over without another exchange.
+//
+// CTA: 8 consumer warps + 1 producer warp.  The producer streams work items
+// into two rings of shared memory with TMA tensor copies (one copy per block of
+// rows, group-major, see mx_tma.cu) plus bulk copies of the rows' BF16 scales
+// and biases:
+//   ring L  gate/up items: 8 gate + 8 up rows x D (the 16 rows of one MMA tile,
+//           so gelu(g) * u is lane-local); split over the 8 consumer warps;
+//   ring S  down items: 16 rows x one K chunk (shared expert) or x I (routed);
+//           one consumer warp per item.
+// Per layer, each list split over all CTAs in contiguous ranges:
+//   A1  shared gate/up     S/8 items           -> hs = gelu(gate x) * (up x)
+//   SD  shared down        D/16 x K chunks     -> y
+//   B   routed gate/up     n_active * I/8      -> h_slot = w_slot gelu(g) * u
+//   RD  routed down        D/16 x n_active     -> y
+// and the router rows (E rows, round-robin).  Down items add their partial
+// sums into y in 64-bit fixed point, whose integer addition does not depend on
+// the order, so the result is deterministic; every CTA then forms
+// x_{l+1} = residual + lambda * y.
+//
+// Math: legacy warp MMA m16n8k32 with FP8 (e4m3) operands and fp32
+// accumulation.  A raw nibble byte n (0..15) is exactly the e4m3 number
+// n * 2^-9, so A is built from the packed words with one mask (low nibbles) or
+// a shift and a mask (high nibbles) per 4 weights -- the high/low split reorders
+// K, and B follows the same order.  B carries the activation (x, or the hidden
+// vector for the down projections) scaled by a per-vector power of two and
+// split into e4m3 planes whose sum reproduces it (x: 2 planes when it is BF16,
+// exact for every element within 2^10 of the vector's largest; 4 planes for
+// fp32 x and for the fp32 hidden vectors, about 16 significant bits); the
+// planes sit in the columns of the MMA, and each lane adds its plane columns.
+// The per-group affine terms are applied in fp32: y += s_g * P_g + b_g * X_g
+// with P_g = sum q x from the MMA and X_g = sum x.  The e4m3 MMA accumulates in
+// fp32 (checked against exact sums on this GPU).
+//
+// The router is not on the MMA: its logits are computed in the fixed fp32
+// order of the header so the top-k choice matches the oracle bit for bit.
+#include "mx_common.cuh"
+#include "mx_internal.h"
+
+#include <algorithm>
+#include <climits>
+#include <cstring>
+#include <mutex>
+
+namespace mx {
+
+namespace {
+
+constexpr int kCW = 8;                 // consumer warps
+constexpr int kCT = kCW * 32;          // consumer threads
+constexpr int kPT = kCT + 32;          // + the producer warp
+constexpr uint32_t kLo = 0x0F0F0F0Fu;  // low nibble of every byte
+
+// ------------------------------------------------------------------ helpers
+
+__device__ __forceinline__ uint2 lds64(const uint8_t *p) { return *reinterpret_cast<const uint2 *>(p); }
+
+// D += A(16x32 e4m3, row) * B(32x8 e4m3, col), fp32 accumulate.
+__device__ __forceinline__ void mma_fp8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats -> two e4m3 bytes (round to nearest even, saturating): lo in bits 0-7.
+__device__ __forceinline__ uint32_t to_e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two e4m3 bytes (bits 0-15 of v) -> floats, exactly.
+__device__ __forceinline__ float2 from_e4m3x2(uint32_t v)
+{
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)v));
+    return __half22float2(*reinterpret_cast<__half2 *>(&h));
+}
+
+// Power-of-two scale 2^k putting the largest magnitude m in [128, 256), and
+// the factor 2^(9-k) that turns an MMA sum of (n 2^-9)(x 2^k) back into sum n x.
+__device__ __forceinline__ void plane_scale(float m, float &sc, float &back)
+{
+    const int E = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;
+    int k = 7 - E;
+    k = k > 126 ? 126 : (k < -117 ? -117 : k);
+    sc = __uint_as_float((uint32_t)(127 + k) << 23);
+    back = __uint_as_float((uint32_t)(127 + 9 - k) << 23);
+}
+
+// Split 8 scaled values into NP e4m3 planes; plane p -> (even elements, odd
+// elements) as the b0/b1 register pair of one MMA k-step.
+template <int NP>
+__device__ __forceinline__ void make_planes(float (&r)[8], uint2 (&out)[NP])
+{
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+        const uint32_t e0 = to_e4m3x2(r[0], r[2]), e1 = to_e4m3x2(r[4], r[6]);
+        const uint32_t o0 = to_e4m3x2(r[1], r[3]), o1 = to_e4m3x2(r[5], r[7]);
+        out[p] = make_uint2(e0 | (e1 << 16), o0 | (o1 << 16));
+        if (p + 1 < NP) {
+            const float2 a = from_e4m3x2(e0), b = from_e4m3x2(e1), c = from_e4m3x2(o0), d = from_e4m3x2(o1);
+            r[0] -= a.x; r[2] -= a.y; r[4] -= b.x; r[6] -= b.y;
+            r[1] -= c.x; r[3] -= c.y; r[5] -= d.x; r[7] -= d.y;
+        }
+    }
+}
+
+__device__ __forceinline__ int ld_acquire(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                            uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                 "%3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+                 "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Contiguous split of n items over nc CTAs; with n <= nc, CTA c < n takes item c.
+__device__ __forceinline__ void prange(int n, int c, int nc, int &lo, int &hi)
+{
+    if (n <= nc) {
+        lo = c < n ? c : n;
+        hi = c < n ? c + 1 : n;
+    } else {
+        lo = (int)((long long)c * n / nc);
+        hi = (int)((long long)(c + 1) * n / nc);
+    }
+}
+
+// ------------------------------------------------------------ shared memory
+
+struct Rt {  // routing of the current layer (computed by the consumer warps)
+    int *n_act;       // [1]
+    int *act_e;       // [amax] active experts, ascending
+    int *act_n;       // [amax] slots of each
+    int *act_slot;    // [amax][4] slot ids s = t*K + k, ascending
+    int *slot_e;      // [T*K]
+    float *slot_w;    // [T*K] (first the selected logits, then the weights)
+    int *emap;        // [E] expert -> active index
+    uint32_t *emask;  // [16]
+};
+
+struct Smem {
+    uint64_t *fullL, *emptyL, *fullS, *emptyS, *route_bar;
+    uint8_t *ringL, *ringS;
+    uint8_t *xraw;         // layer input x_l (act dtype) [T][D]
+    uint8_t *xq;           // x_l after the optional rmsnorm (act dtype) [T][D]
+    float *xg;             // [T][GD] group sums of xq, canonical order
+    uint8_t *xpl;          // planes of xq (layout A, NB plane pairs)
+    uint8_t *hspl;         // planes of hs (layout A, 2 pairs), Gp = nch*GI groups, zero padded
+    float *hsg;            // [T][Gp]
+    uint8_t *hpl;          // planes of h (layout B, 2 pairs), per slot
+    float *hg;             // [T*K][GI]
+    float *red;            // [NL][kCW][32][2] gate/up cross-warp sums, per ring slot
+    int *icnt;             // [NL] warps done with the item in each gate/up slot
+    float *lg;             // [T][E] logits of the layer
+    float *pr;             // scratch
+    float *fx, *fhs, *fh;  // back factors 2^(9-k): x [T], hs [T], h [T*K]
+    float *rn, *xsc;       // [T] rmsnorm factors, x plane scales
+    int *vmax;             // [max(T, T*K)] plane maxima (float bits)
+    int *flag;             // [4]
+    uint8_t *zero;         // 16 zero bytes
+    Rt rt;
+};
+
+__device__ __forceinline__ Smem carve(uint8_t *sm, const PdParams &p)
+{
+    const PdSmem &o = p.sm;
+    Smem s;
+    s.fullL = reinterpret_cast<uint64_t *>(sm);
+    s.emptyL = s.fullL + o.NL;
+    s.fullS = s.emptyL + o.NL;
+    s.emptyS = s.fullS + o.NS;
+    s.route_bar = s.emptyS + o.NS;
+    s.ringL = sm + o.ringL;
+    s.ringS = sm + o.ringS;
+    s.xraw = sm + o.xraw;
+    s.xq = sm + o.xq;
+    s.xg = reinterpret_cast<float *>(sm + o.xg);
+    s.xpl = sm + o.xpl;
+    s.hspl = sm + o.hspl;
+    s.hsg = reinterpret_cast<float *>(sm + o.hsg);
+    s.hpl = sm + o.hpl;
+    s.hg = reinterpret_cast<float *>(sm + o.hg);
+    s.red = reinterpret_cast<float *>(sm + o.red);
+    s.icnt = reinterpret_cast<int *>(sm + o.red + (size_t)o.NL * kCW * 64 * 4);
+    s.lg = reinterpret_cast<float *>(sm + o.lg);
+    s.pr = reinterpret_cast<float *>(sm + o.pr);
+    float *m = reinterpret_cast<float *>(sm + o.misc);
+    const int TK = p.T * p.K;
+    s.fx = m;
+    s.fhs = m + 4;
+    s.rn = m + 8;
+    s.xsc = m + 12;
+    s.flag = reinterpret_cast<int *>(m + 16);
+    s.fh = m + 20;                                         // [TK]
+    s.vmax = reinterpret_cast<int *>(m + 20 + TK);         // [max(T, TK)]
+    int *r = reinterpret_cast<int *>(sm + o.rt);
+    const int amax = TK < p.E ? TK : p.E;
+    s.rt.n_act = r;
+    s.rt.emask = reinterpret_cast<uint32_t *>(r + 4);
+    s.rt.act_e = r + 20;
+    s.rt.act_n = s.rt.act_e + amax;
+    s.rt.act_slot = s.rt.act_n + amax;
+    s.rt.slot_e = s.rt.act_slot + 4 * amax;
+    s.rt.slot_w = reinterpret_cast<float *>(s.rt.slot_e + TK);
+    s.rt.emap = reinterpret_cast<int *>(s.rt.slot_w + TK);
+    s.zero = sm + o.zero;
+    return s;
+}
+
+// ------------------------------------------------------------- sync helpers
+
+__device__ __forceinline__ int *abort_word(const PdParams &p) { return p.ctr + p.n_layers * p.cstride + 1; }
+
+__device__ __forceinline__ void set_abort(const PdParams &p) { atomicExch(abort_word(p), 1); }
+
+// Spin until *c >= target.  False after kWaitLimitNs (error word set) or when
+// another CTA has given up.
+__device__ bool gwait(const int *c, int target, const PdParams &p)
+{
+    if (ld_acquire(c) >= target)
+        return true;
+    const unsigned long long t0 = global_ns();
+    const int *ab = abort_word(p);
+    for (unsigned it = 0;; ++it) {
+        __nanosleep(32);
+        if (ld_acquire(c) >= target)
+            return true;
+        if ((it & 63u) == 63u) {
+            if (ld_acquire(ab))
+                return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                atomicOr(p.err, kErrTimeout);
+                set_abort(p);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, const PdParams &p)
+{
+    if (mbar_wait(bar, parity, p.err))
+        return true;
+    set_abort(p);
+    return false;
+}
+
+__device__ __forceinline__ void csync() { named_sync(1, kCT); }
+
+// Consumer barrier that also ANDs a per-thread verdict, so every consumer
+// thread leaves with the same answer (a wait may give up on one thread and not
+// on another).
+__device__ __forceinline__ bool csync_and(bool v)
+{
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+                 "barrier.cta.red.and.pred q, 1, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "r"(kCT)
+                 : "memory");
+    return r != 0;
+}
+
+// All consumer threads: thread 0 waits for *c >= target; returns the verdict to all.
+__device__ bool cwait(const int *c, int target, const PdParams &p, const Smem &s)
+{
+    if (threadIdx.x == 0)
+        s.flag[0] = gwait(c, target, p) ? 1 : 0;
+    csync();
+    const bool ok = s.flag[0] != 0;
+    csync();
+    return ok;
+}
+
+__device__ __forceinline__ void red_add(int *c, int v)
+{
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(c), "r"(v) : "memory");
+}
+
+// The down projections' partial sums are added into y in 64-bit fixed point
+// (2^-32 units): integer addition is associative, so y does not depend on the
+// order in which CTAs arrive.
+constexpr float kFix = 4294967296.0f;         // 2^32
+constexpr float kUnfix = 2.3283064365386963e-10f;  // 2^-32
+__device__ __forceinline__ void red_fix(long long *y, float v)
+{
+    const long long q = __float2ll_rn(v * kFix);
+    asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(y), "l"(q) : "memory");
+}
+
+// ---------------------------------------------------------------- the math
+
+// Gate/up item (8 gate rows -> MMA rows 0-7, 8 up rows -> rows 8-15) over the
+// groups g = g0, g0 + gs, ... of K = G groups.  Slot layout: gate tile
+// [G][8][32 B], up tile [G][8][32 B], gate.s, gate.b, up.s, up.b ([8][G] BF16).
+// bp: this lane's B column (plane pair) for group 0; bgs/bms/bnbs: strides of
+// group, k-step, plane pair.  fo, xgo: the lane's output column (slot c).
+template <int NB>
+__device__ __forceinline__ void gu_math(const uint8_t *st, int G, int g0, int gs, const uint8_t *bp, int bgs,
+                                        int bms, int bnbs, float fo, const float *xgo, float &accg, float &accu)
+{
+    const int lane = threadIdx.x & 31, gid = lane >> 2, c = lane & 3;
+    const uint8_t *gt = st + gid * 32 + c * 8, *ut = gt + 256 * G;
+    const uint16_t *sc = reinterpret_cast<const uint16_t *>(st + 512 * G) + gid * G;
+    const uint16_t *sg = sc, *bg = sc + 8 * G, *su = sc + 16 * G, *bu = sc + 24 * G;
+#pragma unroll 2
+    for (int g = g0; g < G; g += gs) {
+        const uint2 qg = lds64(gt + 256 * g), qu = lds64(ut + 256 * g);
+        float Rg = 0.f, Ru = 0.f;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint2 b0 = lds64(bp + g * bgs + nb * bnbs), b1 = lds64(bp + g * bgs + bms + nb * bnbs);
+            mma_fp8(d, qg.x & kLo, qu.x & kLo, (qg.x >> 4) & kLo, (qu.x >> 4) & kLo, b0.x, b0.y);
+            mma_fp8(d, qg.y & kLo, qu.y & kLo, (qg.y >> 4) & kLo, (qu.y >> 4) & kLo, b1.x, b1.y);
+            Rg += d[0] + d[1];
+            Ru += d[2] + d[3];
+        }
+        const float X = xgo[g];
+        accg = fmaf(bf2f(sg[g]), Rg * fo, accg);
+        accg = fmaf(bf2f(bg[g]), X, accg);
+        accu = fmaf(bf2f(su[g]), Ru * fo, accu);
+        accu = fmaf(bf2f(bu[g]), X, accu);
+    }
+}
+
+// Down item: 16 rows x G groups, one warp.  tile [G][16][32 B]; s, b: the
+// rows' BF16 scales and biases with row pitch `pitch` (already offset to the
+// item's first group).  Lane output: rows gid (a0) and gid + 8 (a8), column
+// slot c.  B: 2 plane pairs; bgs/bms/bnbs: strides of group, k-step, pair.
+__device__ __forceinline__ void dn_math(const uint8_t *tile, const uint16_t *s, const uint16_t *b, int pitch, int G,
+                                        const uint8_t *bp, int bgs, int bms, int bnbs, float fo, const float *xgo,
+                                        float &a0, float &a8)
+{
+    const int lane = threadIdx.x & 31, gid = lane >> 2, c = lane & 3;
+    const uint8_t *t0 = tile + gid * 32 + c * 8;
+    const uint16_t *s0 = s + gid * pitch, *s8 = s + (gid + 8) * pitch, *b0 = b + gid * pitch,
+                   *b8 = b + (gid + 8) * pitch;
+#pragma unroll 2
+    for (int g = 0; g < G; ++g) {
+        const uint2 q0 = lds64(t0 + 512 * g), q8 = lds64(t0 + 512 * g + 256);
+        const uint32_t l0 = q0.x & kLo, l8 = q8.x & kLo, h0 = (q0.x >> 4) & kLo, h8 = (q8.x >> 4) & kLo;
+        const uint32_t m0 = q0.y & kLo, m8 = q8.y & kLo, k0 = (q0.y >> 4) & kLo, k8 = (q8.y >> 4) & kLo;
+        const uint8_t *bg = bp + g * bgs;
+        float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint2 v0 = lds64(bg), v1 = lds64(bg + bms), w0 = lds64(bg + bnbs), w1 = lds64(bg + bms + bnbs);
+        mma_fp8(d, l0, l8, h0, h8, v0.x, v0.y);
+        mma_fp8(e, l0, l8, h0, h8, w0.x, w0.y);
+        mma_fp8(d, m0, m8, k0, k8, v1.x, v1.y);
+        mma_fp8(e, m0, m8, k0, k8, w1.x, w1.y);
+        const float R0 = (d[0] + d[1]) + (e[0] + e[1]), R8 = (d[2] + d[3]) + (e[2] + e[3]);
+        const float X = xgo[g];
+        a0 = fmaf(bf2f(s0[g]), R0 * fo, a0);
+        a0 = fmaf(bf2f(b0[g]), X, a0);
+        a8 = fmaf(bf2f(s8[g]), R8 * fo, a8);
+        a8 = fmaf(bf2f(b8[g]), X, a8);
+    }
+}
+
+// ----------------------------------------------------------- plane builders
+
+// e4m3 planes (2 pairs) of nvec fp32 vectors of G*64 values, row stride ld,
+// written by other CTAs (read from L2), zero padded to Gp >= G groups.
+//   layout A (per_slot false): g*(256*nvec) + m*(128*nvec) + nb*(64*nvec) + (2v+pp)*32 + c*8
+//   layout B (per_slot true):  v*(Gp*256) + g*256 + m*128 + nb*64 + pp*32 + c*8
+// Also gsum[v][g] (group sums, 0 on padding) and back[v] = 2^(9-k).
+__device__ __forceinline__ size_t plane_off(bool per_slot, int nvec, int Gp, int v, int g, int m, int nb, int pp, int c)
+{
+    return per_slot ? (size_t)v * Gp * 256 + (size_t)g * 256 + m * 128 + nb * 64 + pp * 32 + c * 8
+                    : (size_t)g * 256 * nvec + (size_t)m * 128 * nvec + (size_t)nb * 64 * nvec + (2 * v + pp) * 32 + c * 8;
+}
+
+__device__ __forceinline__ void load8(const float *src, size_t ld, int v, int g, int w, int G, float (&x)[8])
+{
+    if (g < G) {
+        const float4 *q = reinterpret_cast<const float4 *>(src + (size_t)v * ld + (size_t)g * 64 + 8 * w);
+        const float4 a = __ldcg(q), b = __ldcg(q + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            x[j] = 0.f;
+    }
+}
+
+__device__ __forceinline__ void store_planes(uint8_t *dst, bool per_slot, int nvec, int Gp, int v, int g, int w,
+                                             float sc, float (&x)[8])
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        x[j] *= sc;
+    uint2 pl[4];
+    make_planes<4>(x, pl);
+    const int m = w & 1, c = w >> 1;
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+        *reinterpret_cast<uint2 *>(dst + plane_off(per_slot, nvec, Gp, v, g, m, p >> 1, p & 1, c)) = pl[p];
+}
+
+__device__ void planes_f32(const float *src, size_t ld, int nvec, int G, int Gp, bool per_slot, uint8_t *dst,
+                           float *gsum, float *back, int *vmax)
+{
+    const int tid = threadIdx.x;
+    const int nw = nvec * Gp * 8;  // 8-value words, padding included
+    constexpr int R = 4;           // words per thread kept in registers
+    for (int v = tid; v < nvec; v += kCT)
+        vmax[v] = 0;
+    csync();
+    const bool in_regs = nw <= R * kCT;
+    float x[R][8];
+    for (int w0 = 0; w0 < nw; w0 += R * kCT) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int wi = w0 + tid + r * kCT, v = wi / (Gp * 8), rem = wi - v * Gp * 8;
+            if (wi < nw)
+                load8(src, ld, v, rem >> 3, rem & 7, G, x[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int wi = w0 + tid + r * kCT, v = wi / (Gp * 8);
+            float sm = 0.f, mx = 0.f;
+            if (wi < nw) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    sm += x[r][j];
+                    mx = fmaxf(mx, fabsf(x[r][j]));
+                }
+            }
+            // the 8 words of a group sit in 8 consecutive lanes
+            sm += __shfl_xor_sync(0xffffffffu, sm, 1);
+            sm += __shfl_xor_sync(0xffffffffu, sm, 2);
+            sm += __shfl_xor_sync(0xffffffffu, sm, 4);
+            if (wi < nw) {
+                if ((wi & 7) == 0)
+                    gsum[wi >> 3] = sm;
+                if (mx > 0.f)
+                    atomicMax(&vmax[v], __float_as_int(mx));
+            }
+        }
+    }
+    csync();
+    for (int v = tid; v < nvec; v += kCT) {
+        float sc, bk;
+        plane_scale(__int_as_float(vmax[v]), sc, bk);
+        back[v] = bk;
+    }
+    for (int w0 = 0; w0 < nw; w0 += R * kCT) {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int wi = w0 + tid + r * kCT, v = wi / (Gp * 8), rem = wi - v * Gp * 8;
+            if (wi < nw && !in_regs)
+                load8(src, ld, v, rem >> 3, rem & 7, G, x[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const int wi = w0 + tid + r * kCT, v = wi / (Gp * 8), rem = wi - v * Gp * 8;
+            if (wi < nw) {
+                float sc, bk;
+                plane_scale(__int_as_float(vmax[v]), sc, bk);
+                store_planes(dst, per_slot, nvec, Gp, v, rem >> 3, rem & 7, sc, x[r]);
+            }
+        }
+    }
+    csync();
+}
+
+// x_l (xraw) -> xq (optionally rmsnorm'd, rounded to the act dtype), its group
+// sums in the canonical order (the router's X), and its e4m3 planes.
+template <int NB>
+__device__ void prologue(const PdParams &p, const Smem &s)
+{
+    constexpr int es = NB == 1 ? 2 : 4;
+    const int tid = threadIdx.x, lane = tid & 31, T = p.T, D = p.D, GD = D / 64;
+    auto ld64 = [&](const uint8_t *base, int t, int g, float (&v)[64]) {
+        const uint8_t *r = base + ((size_t)t * D + g * 64) * es;
+#pragma unroll
+        for (int ch = 0; ch < 4 * es; ++ch) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(r + 16 * ch);
+            if constexpr (es == 2) {
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    v[8 * ch + 2 * q] = __uint_as_float(u[q] << 16);
+                    v[8 * ch + 2 * q + 1] = __uint_as_float(u[q] & 0xFFFF0000u);
+                }
+            } else {
+                v[4 * ch] = __uint_as_float(w.x);
+                v[4 * ch + 1] = __uint_as_float(w.y);
+                v[4 * ch + 2] = __uint_as_float(w.z);
+                v[4 * ch + 3] = __uint_as_float(w.w);
+            }
+        }
+    };
+    if (tid < T)
+        s.vmax[tid] = 0;
+    if (p.pre_norm) {
+        // sum of squares: per group an fma chain, then the groups in order
+        for (int i = tid; i < T * GD; i += kCT) {
+            const int t = i / GD, g = i - t * GD;
+            float v[64];
+            ld64(s.xraw, t, g, v);
+            float q = 0.f;
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+                q = fmaf(v[k], v[k], q);
+            s.pr[i] = q;
+        }
+        csync();
+        if (tid < T) {
+            float ss = 0.f;
+            for (int g0 = 0; g0 < GD; g0 += 8) {
+                float q[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    q[j] = g0 + j < GD ? s.pr[tid * GD + g0 + j] : 0.f;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (g0 + j < GD)
+                        ss = ss + q[j];
+            }
+            s.rn[tid] = 1.0f / sqrtf(ss / (float)D + p.eps);
+        }
+    }
+    csync();
+    // elementwise: xq = round(x * r), the magnitude maximum per token
+    {
+        const int n8 = T * D / 8;  // 8-value words
+        for (int i = tid; i < n8; i += kCT) {
+            const int t = (8 * i) / D;
+            float v[8];
+            if constexpr (es == 2) {
+                const uint4 w = reinterpret_cast<const uint4 *>(s.xraw)[i];
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    v[2 * q] = __uint_as_float(u[q] << 16);
+                    v[2 * q + 1] = __uint_as_float(u[q] & 0xFFFF0000u);
+                }
+            } else {
+                const float4 a = reinterpret_cast<const float4 *>(s.xraw)[2 * i];
+                const float4 b = reinterpret_cast<const float4 *>(s.xraw)[2 * i + 1];
+                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+                v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            }
+            float mx = 0.f;
+            if (p.pre_norm) {
+                const float r = s.rn[t];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    v[k] = es == 2 ? bf2f(f2bf(v[k] * r)) : v[k] * r;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                mx = fmaxf(mx, fabsf(v[k]));
+            if constexpr (es == 2) {
+                uint4 w;
+                w.x = (__float_as_uint(v[0]) >> 16) | (__float_as_uint(v[1]) & 0xFFFF0000u);
+                w.y = (__float_as_uint(v[2]) >> 16) | (__float_as_uint(v[3]) & 0xFFFF0000u);
+                w.z = (__float_as_uint(v[4]) >> 16) | (__float_as_uint(v[5]) & 0xFFFF0000u);
+                w.w = (__float_as_uint(v[6]) >> 16) | (__float_as_uint(v[7]) & 0xFFFF0000u);
+                reinterpret_cast<uint4 *>(s.xq)[i] = w;
+            } else {
+                reinterpret_cast<float4 *>(s.xq)[2 * i] = make_float4(v[0], v[1], v[2], v[3]);
+                reinterpret_cast<float4 *>(s.xq)[2 * i + 1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
+            // one token per warp-aligned run when D is a multiple of 256 values;
+            // otherwise lanes of a warp may hold two tokens: reduce per lane
+            if (mx > 0.f)
+                atomicMax(&s.vmax[t], __float_as_int(mx));
+        }
+        (void)lane;
+    }
+    csync();
+    if (tid < T) {
+        float sc, bk;
+        plane_scale(__int_as_float(s.vmax[tid]), sc, bk);
+        s.xsc[tid] = sc;
+        s.fx[tid] = bk;
+    }
+    csync();
+    // group sums in the canonical order (the router's X), and the planes
+    for (int i = tid; i < T * GD; i += kCT) {
+        const int t = i / GD, g = i - t * GD;
+        float v[64];
+        ld64(s.xq, t, g, v);
+        float X = 0.f;
+#pragma unroll
+        for (int k = 0; k < 64; ++k)
+            X = X + v[k];
+        s.xg[i] = X;
+    }
+    for (int i = tid; i < T * GD * 8; i += kCT) {
+        const int t = i / (GD * 8), rem = i - t * GD * 8, g = rem >> 3, w = rem & 7;
+        const uint8_t *src = s.xq + ((size_t)t * D + g * 64 + 8 * w) * es;
+        float x[8];
+        if constexpr (es == 2) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(src);
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                x[2 * j] = __uint_as_float(u[j] << 16);
+                x[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+            }
+        } else {
+            const float4 a = *reinterpret_cast<const float4 *>(src), b = *reinterpret_cast<const float4 *>(src + 16);
+            x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+            x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        }
+        const float sc = s.xsc[t];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            x[j] *= sc;
+        uint2 pl[2 * NB];
+        make_planes<2 * NB>(x, pl);
+        const int m = w & 1, c = w >> 1;
+#pragma unroll
+        for (int q = 0; q < 2 * NB; ++q) {
+            const size_t off = (size_t)g * (2 * NB * 64 * T) + (size_t)m * (NB * 64 * T) + (size_t)(q >> 1) * (64 * T) +
+                               (2 * t + (q & 1)) * 32 + c * 8;
+            *reinterpret_cast<uint2 *>(s.xpl + off) = pl[q];
+        }
+    }
+    csync();
+}
+
+// Router rows r = blockIdx.x, + gridDim.x, ...: logits in the fixed order of
+// the header.  rq/rsv/rbv: the first row's bytes and affine terms, prefetched.
+template <int NB>
+__device__ void router_rows(const PdParams &p, const PdLayer &L, const Smem &s, uint4 (&rq)[4], float rsv,
+                            float rbv)
+{
+    constexpr int es = NB == 1 ? 2 : 4;
+    const int tid = threadIdx.x, T = p.T, D = p.D, GD = D / 64, C = blockIdx.x, NC = gridDim.x;
+    float *P = s.pr;            // [GD][T]
+    float *sv = s.pr + GD * T;  // [GD]
+    float *bv = sv + GD;        // [GD]
+    for (int r = C; r < p.E; r += NC) {
+        if (r != C && tid < GD) {
+            const uint4 *q = reinterpret_cast<const uint4 *>(L.rw + (size_t)r * (D / 4) + (size_t)tid * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                rq[j] = __ldg(q + j);
+            rsv = bf2f(__ldg(L.rs + (size_t)r * GD + tid));
+            rbv = bf2f(__ldg(L.rb + (size_t)r * GD + tid));
+        }
+        if (tid < GD) {
+            const int g = tid;
+            sv[g] = rsv;
+            bv[g] = rbv;
+            for (int t = 0; t < T; ++t) {
+                float xv[64];
+                const uint8_t *xr = s.xq + ((size_t)t * D + g * 64) * es;
+#pragma unroll
+                for (int ch = 0; ch < 4 * es; ++ch) {
+                    const uint4 w = *reinterpret_cast<const uint4 *>(xr + 16 * ch);
+                    if constexpr (es == 2) {
+                        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            xv[8 * ch + 2 * q] = __uint_as_float(u[q] << 16);
+                            xv[8 * ch + 2 * q + 1] = __uint_as_float(u[q] & 0xFFFF0000u);
+                        }
+                    } else {
+                        xv[4 * ch] = __uint_as_float(w.x);
+                        xv[4 * ch + 1] = __uint_as_float(w.y);
+                        xv[4 * ch + 2] = __uint_as_float(w.z);
+                        xv[4 * ch + 3] = __uint_as_float(w.w);
+                    }
+                }
+                float acc = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const uint32_t w = j % 4 == 0 ? rq[j / 4].x : j % 4 == 1 ? rq[j / 4].y
+                                     : j % 4 == 2 ? rq[j / 4].z : rq[j / 4].w;
+                    acc = fmaf(byte_f<0>(w), xv[4 * j], acc);
+                    acc = fmaf(byte_f<1>(w), xv[4 * j + 1], acc);
+                    acc = fmaf(byte_f<2>(w), xv[4 * j + 2], acc);
+                    acc = fmaf(byte_f<3>(w), xv[4 * j + 3], acc);
+                }
+                P[g * T + t] = acc;
+            }
+        }
+        csync();
+        if (tid < T) {
+            float acc = 0.f;
+            for (int g0 = 0; g0 < GD; g0 += 8) {
+                float a[8], b[8], c[8], d[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int g = g0 + j < GD ? g0 + j : GD - 1;
+                    a[j] = sv[g];
+                    b[j] = P[g * T + tid];
+                    c[j] = bv[g];
+                    d[j] = s.xg[tid * GD + g];
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    if (g0 + j < GD) {
+                        acc = fmaf(a[j], b[j], acc);
+                        acc = fmaf(c[j], d[j], acc);
+                    }
+                }
+            }
+            p.logits[(size_t)tid * p.E + r] = acc;
+        }
+        csync();
+    }
+}
+
+// Top-k (descending, ties to the lower expert, NaN as -inf), softmax of the
+// selected logits times the per-expert scale, and the grouping of slots by
+// expert (ascending expert, ascending slot).  All consumer threads.
+__device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = p.T, E = p.E, K = p.K;
+    const Rt &rt = s.rt;
+    for (int i = tid; i < T * E; i += kCT) {
+        const float v = __ldcg(p.logits + i);
+        s.lg[i] = isnan(v) ? -INFINITY : v;
+    }
+    csync();
+    for (int i = tid; i < T * E; i += kCT) {
+        const int t = i / E, e = i - t * E;
+        const float *row = s.lg + t * E;
+        const float v = row[e];
+        int rank = 0;
+#pragma unroll 8
+        for (int j = 0; j < E; ++j) {
+            const float u = row[j];
+            rank += (u > v) || (u == v && j < e);
+        }
+        if (rank < K) {
+            rt.slot_e[t * K + rank] = e;
+            rt.slot_w[t * K + rank] = v;
+        }
+    }
+    csync();
+    if (tid < T) {
+        float *w = rt.slot_w + tid * K;
+        const float m = w[0];
+        float sum = 0.f;
+        for (int k = 0; k < K; ++k) {
+            w[k] = expf(w[k] - m);
+            sum += w[k];
+        }
+        for (int k = 0; k < K; ++k) {
+            float x = w[k] / sum;
+            if (L.pes)
+                x = x * __ldg(L.pes + rt.slot_e[tid * K + k]);
+            w[k] = x;
+            if (blockIdx.x == 0) {
+                L.topk_idx[tid * K + k] = rt.slot_e[tid * K + k];
+                L.topk_w[tid * K + k] = x;
+            }
+        }
+    }
+    if (warp == 0) {
+        if (lane < 16)
+            rt.emask[lane] = 0u;
+        __syncwarp();
+    }
+    csync();
+    if (warp == 0) {
+        const int nw = (E + 31) >> 5;
+        for (int i = lane; i < T * K; i += 32) {
+            const int e = rt.slot_e[i];
+            atomicOr(&rt.emask[e >> 5], 1u << (e & 31));
+        }
+        __syncwarp();
+        const uint32_t bits = lane < nw ? rt.emask[lane] : 0u;
+        const int cnt = __popc(bits);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        int j = incl - cnt;
+        for (uint32_t b = bits; b; b &= b - 1u, ++j) {
+            const int e = 32 * lane + __ffs(b) - 1;
+            rt.act_e[j] = e;
+            rt.act_n[j] = 0;
+            rt.emap[e] = j;
+        }
+        if (lane == 31)
+            *rt.n_act = incl;
+        __syncwarp();
+        for (int t = 0; t < T; ++t) {
+            if (lane < K) {
+                const int sl = t * K + lane, a = rt.emap[rt.slot_e[sl]];
+                rt.act_slot[4 * a + rt.act_n[a]] = sl;
+                rt.act_n[a] += 1;
+            }
+            __syncwarp();
+        }
+    }
+    csync();
+}
+
+// ------------------------------------------------------------------ producer
+
+template <int NB>
+__device__ void producer(const PdParams &p, const Smem &s)
+{
+    const int lane = threadIdx.x & 31, C = blockIdx.x, NC = gridDim.x;
+    const int GD = p.D / 64, GI = p.I / 64, GS = p.S / 64;
+    const int GC = GI < GS ? GI : GS, nch = (GS + GC - 1) / GC;  // shared-down K chunks of GC groups
+    const PdSmem &o = p.sm;
+    int kL = 0, kS = 0;
+    bool ok = true;
+    // reserve the next slot of a ring (lane 0 waits; the verdict is the warp's)
+    auto take = [&](bool ringL, uint32_t bytes, uint8_t *&dst, uint64_t *&bar) -> bool {
+        int &k = ringL ? kL : kS;
+        const int n = ringL ? o.NL : o.NS, sl = k % n;
+        uint64_t *empty = ringL ? s.emptyL : s.emptyS;
+        int good = 1;
+        if (k >= n && lane == 0)
+            good = pwait(&empty[sl], ((k / n) - 1) & 1, p) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, good, 0))
+            return false;
+        dst = (ringL ? s.ringL + (size_t)sl * o.slotL : s.ringS + (size_t)sl * o.slotS);
+        bar = (ringL ? s.fullL : s.fullS) + sl;
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar, bytes);
+        __syncwarp();
+        ++k;
+        return true;
+    };
+    for (int l = 0; l < p.n_layers && ok; ++l) {
+        const PdLayer &L = p.L[l];
+        int lo, hi;
+        // A1: shared gate/up -> ring L
+        prange(p.S / 8, C, NC, lo, hi);
+        for (int it = lo; it < hi && ok; ++it) {
+            uint8_t *dst;
+            uint64_t *bar;
+            if (!(ok = take(true, 576u * GD, dst, bar)))
+                break;
+            if (lane == 0) {
+                tma_load_4d(dst, &L.sgate, 0, 8 * it, 0, 0, bar);
+                tma_load_4d(dst + 256 * GD, &L.sup, 0, 8 * it, 0, 0, bar);
+            } else if (lane <= 4) {
+                const int j = lane - 1;
+                const uint16_t *src = (j & 1 ? L.sb[j >> 1] : L.ss[j >> 1]) + (size_t)8 * it * GD;
+                bulk_g2s(dst + 512 * GD + j * 16 * GD, src, 16u * GD, bar);
+            }
+        }
+        // SD: shared down, 16 rows x (GC groups of one K chunk) -> ring S
+        prange((p.D / 16) * nch, C, NC, lo, hi);
+        for (int it = lo; it < hi && ok; ++it) {
+            const int rb = it / nch, ch = it - rb * nch;
+            uint8_t *dst;
+            uint64_t *bar;
+            if (!(ok = take(false, 512u * GC + 64u * GS, dst, bar)))
+                break;
+            if (lane == 0) {
+                tma_load_4d(dst, &L.sdown, 0, 16 * rb, ch * GC, 0, bar);
+            } else if (lane <= 2) {
+                const uint16_t *src = (lane == 2 ? L.sb[2] : L.ss[2]) + (size_t)16 * rb * GS;
+                bulk_g2s(dst + 512 * GC + (lane - 1) * 32 * GS, src, 32u * GS, bar);
+            }
+        }
+        if (!ok)
+            break;
+        // routing of this layer (from the consumers)
+        int good = 1;
+        if (lane == 0)
+            good = pwait(s.route_bar, l & 1, p) ? 1 : 0;
+        if (!(ok = __shfl_sync(0xffffffffu, good, 0) != 0))
+            break;
+        const int na = *s.rt.n_act;
+        // B: routed gate/up -> ring L
+        prange(na * (p.I / 8), C, NC, lo, hi);
+        for (int it = lo; it < hi && ok; ++it) {
+            const int j = it / (p.I / 8), rbi = it - j * (p.I / 8), e = s.rt.act_e[j];
+            uint8_t *dst;
+            uint64_t *bar;
+            if (!(ok = take(true, 576u * GD, dst, bar)))
+                break;
+            if (lane == 0) {
+                tma_load_4d(dst, &L.gate, 0, 8 * rbi, 0, e, bar);
+                tma_load_4d(dst + 256 * GD, &L.up, 0, 8 * rbi, 0, e, bar);
+            } else if (lane <= 4) {
+                const int jj = lane - 1;
+                const uint8_t *rec = L.blob + (uint64_t)e * L.stride;
+                const uint16_t *src =
+                    reinterpret_cast<const uint16_t *>(rec + (jj & 1 ? L.off_b[jj >> 1] : L.off_s[jj >> 1])) +
+                    (size_t)8 * rbi * GD;
+                bulk_g2s(dst + 512 * GD + jj * 16 * GD, src, 16u * GD, bar);
+            }
+        }
+        // RD: routed down, row-block major -> ring S
+        prange((p.D / 16) * na, C, NC, lo, hi);
+        for (int it = lo; it < hi && ok; ++it) {
+            const int rb = it / na, j = it - rb * na, e = s.rt.act_e[j];
+            uint8_t *dst;
+            uint64_t *bar;
+            if (!(ok = take(false, 576u * GI, dst, bar)))
+                break;
+            if (lane == 0) {
+                tma_load_4d(dst, &L.down, 0, 16 * rb, 0, e, bar);
+            } else if (lane <= 2) {
+                const uint8_t *rec = L.blob + (uint64_t)e * L.stride;
+                const uint16_t *src =
+                    reinterpret_cast<const uint16_t *>(rec + (lane == 2 ? L.off_b[2] : L.off_s[2])) +
+                    (size_t)16 * rb * GI;
+                bulk_g2s(dst + 512 * GI + (lane - 1) * 32 * GI, src, 32u * GI, bar);
+            }
+        }
+    }
+    // Leave no copy in flight: wait (bounded) for the last item of every slot.
+    __syncwarp();
+    if (lane == 0) {
+        for (int k = (kL > o.NL ? kL - o.NL : 0); k < kL; ++k)
+            mbar_wait(&s.fullL[k % o.NL], (k / o.NL) & 1, p.err);
+        for (int k = (kS > o.NS ? kS - o.NS : 0); k < kS; ++k)
+            mbar_wait(&s.fullS[k % o.NS], (k / o.NS) & 1, p.err);
+    }
+    __syncwarp();
+}
+
+// ----------------------------------------------------------------- consumers
+
+template <int NB>
+__device__ void consumers(const PdParams &p, const Smem &s)
+{
+    constexpr int es = NB == 1 ? 2 : 4;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, c = lane & 3;
+    const int C = blockIdx.x, NC = gridDim.x, T = p.T, K = p.K, TK = T * K;
+    const int D = p.D, I = p.I, S = p.S, GD = D / 64, GI = I / 64, GS = S / 64;
+    const int GC = GI < GS ? GI : GS, nch = (GS + GC - 1) / GC;  // shared-down K chunks of GC groups
+    const PdSmem &o = p.sm;
+    int kL = 0, kS = 0;
+    bool ok = true;
+    const int xgs = 2 * NB * 64 * T, xms = NB * 64 * T, xnbs = 64 * T;  // x planes (layout A)
+    const int hgs = 256 * T;                                             // hs planes (layout A, 2 pairs)
+    for (int l = 0; l < p.n_layers && ok; ++l) {
+        const PdLayer &L = p.L[l];
+        int *ctr = p.ctr + l * p.cstride;
+        long long *y = p.ybuf + (size_t)l * T * D;
+        // this CTA's router row: bytes and affine terms do not depend on x
+        uint4 rq[4] = {};
+        float rsv = 0.f, rbv = 0.f;
+        if (C < p.E && tid < GD) {
+            const uint4 *q = reinterpret_cast<const uint4 *>(L.rw + (size_t)C * (D / 4) + (size_t)tid * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                rq[j] = __ldg(q + j);
+            rsv = bf2f(__ldg(L.rs + (size_t)C * GD + tid));
+            rbv = bf2f(__ldg(L.rb + (size_t)C * GD + tid));
+        }
+        if (l == 0) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(L.x_in);
+            uint4 *dst = reinterpret_cast<uint4 *>(s.xraw);
+            for (int i = tid; i < T * D * es / 16; i += kCT)
+                dst[i] = __ldg(src + i);
+            csync();
+        }
+        prologue<NB>(p, s);
+        router_rows<NB>(p, L, s, rq, rsv, rbv);  // ends with a consumer barrier
+        if (tid == 0) {
+            __threadfence();
+            red_add(ctr + 0, 1);
+        }
+
+        // ---- gate/up items, all warps on each item, the last warp to finish
+        // an item reduces it (no CTA barrier per item): first the shared
+        // expert's (their weights are already on chip), then -- after the
+        // routing, done once every CTA's logits are in -- the routed ones.
+        int lo, hi, lo1, hi1, na = 0;
+        prange(S / 8, C, NC, lo1, hi1);
+        const int nA1 = hi1 - lo1;
+        lo = hi = 0;
+        for (int q = 0;; ++q) {
+            if (q == nA1) {
+                // shared gate/up of this CTA done: publish hs; then the routing
+                if (!(ok = csync_and(ok)))
+                    break;
+                if (tid == 0 && nA1 > 0) {
+                    __threadfence();
+                    red_add(ctr + 1, nA1);
+                }
+                if (!(ok = cwait(ctr + 0, NC, p, s)))
+                    break;
+                route_tables(p, L, s);
+                if (tid == 0)
+                    mbar_arrive(s.route_bar);
+                na = *s.rt.n_act;
+                prange(na * (I / 8), C, NC, lo, hi);
+            }
+            if (q >= nA1 && q - nA1 >= hi - lo)
+                break;
+            const bool routed = q >= nA1;
+            const int sl = kL % o.NL;
+            const bool bvalid_s = (gid >> 1) < T;
+            int it, ne, e = 0, rbi = 0, oslot = 0, ot, bt;
+            bool bvalid;
+            if (!routed) {
+                it = lo1 + q;
+                ne = T;
+                bvalid = bvalid_s;
+                bt = gid >> 1;
+                ot = c < T ? c : 0;
+            } else {
+                it = lo + q - nA1;
+                const int j = it / (I / 8);
+                rbi = it - j * (I / 8);
+                e = s.rt.act_e[j];
+                ne = s.rt.act_n[j];
+                bvalid = (gid >> 1) < ne;
+                bt = bvalid ? s.rt.act_slot[4 * j + (gid >> 1)] / K : 0;
+                oslot = c < ne ? s.rt.act_slot[4 * j + c] : 0;
+                ot = oslot / K;
+            }
+            const uint8_t *bp = bvalid ? s.xpl + (2 * bt + (gid & 1)) * 32 + c * 8 : s.zero;
+            const int bgs = bvalid ? xgs : 0, bms = bvalid ? xms : 0, bnbs = bvalid ? xnbs : 0;
+            // a warp whose wait gave up skips the remaining items but keeps to
+            // the loop, so that it reaches the same barriers as the others
+            if (ok && !__all_sync(0xffffffffu, pwait(&s.fullL[sl], (kL / o.NL) & 1, p)))
+                ok = false;
+            if (!ok) {
+                ++kL;
+                continue;
+            }
+            float ag = 0.f, au = 0.f;
+            gu_math<NB>(s.ringL + (size_t)sl * o.slotL, GD, warp, kCW, bp, bgs, bms, bnbs, s.fx[ot], s.xg + ot * GD,
+                        ag, au);
+            float *red = s.red + (size_t)sl * kCW * 64;
+            red[(warp * 32 + lane) * 2] = ag;
+            red[(warp * 32 + lane) * 2 + 1] = au;
+            __syncwarp();
+            int last = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                last = atomicAdd(&s.icnt[sl], 1) == kCW - 1;
+            }
+            if (__shfl_sync(0xffffffffu, last, 0)) {
+                __threadfence_block();
+                if (c < ne) {
+                    float g = 0.f, u = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kCW; ++w) {
+                        g += red[(w * 32 + lane) * 2];
+                        u += red[(w * 32 + lane) * 2 + 1];
+                    }
+                    const float h = gelu_tanh(g) * u;
+                    if (routed)
+                        p.hbuf[(size_t)oslot * I + 8 * rbi + gid] = s.rt.slot_w[oslot] * h;
+                    else
+                        p.hsbuf[(size_t)c * S + 8 * it + gid] = h;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    s.icnt[sl] = 0;
+                    mbar_arrive(&s.emptyL[sl]);
+                }
+            }
+            (void)e;
+            ++kL;
+        }
+        if (!(ok = csync_and(ok)))
+            break;
+        // publish h: one fence, then one count per expert this CTA worked on
+        if (tid == 0) {
+            __threadfence();
+            for (int it = lo; it < hi;) {
+                const int j = it / (I / 8), end = min(hi, (j + 1) * (I / 8));
+                red_add(ctr + 3 + s.rt.act_e[j], end - it);
+                it = end;
+            }
+        }
+
+        // ---- down projections, one warp per item: the shared expert's K
+        // chunks (hs planes), then -- once h of every active expert is in --
+        // the routed ones (h planes)
+        if (!(ok = cwait(ctr + 1, S / 8, p, s)))
+            break;
+        const int Gp = nch * GC;
+        planes_f32(p.hsbuf, S, T, GS, Gp, false, s.hspl, s.hsg, s.fhs, s.vmax);
+        int slo, shi, rlo, rhi;
+        prange((D / 16) * nch, C, NC, slo, shi);
+        prange((D / 16) * na, C, NC, rlo, rhi);
+        const int nsd = shi - slo, ndn = nsd + (rhi - rlo);
+        bool hstep = false;
+        for (int q = warp;; q += kCW) {
+            if (!hstep && q >= nsd) {
+                // every warp joins this once, after its shared items
+                hstep = true;
+                bool good = ok;
+                if (tid < na)
+                    good = good && gwait(ctr + 3 + s.rt.act_e[tid], I / 8, p);
+                if (!(ok = csync_and(good)))
+                    break;
+                planes_f32(p.hbuf, I, TK, GI, GI, true, s.hpl, s.hg, s.fh, s.vmax);
+            }
+            if (q >= ndn)
+                break;
+            if (!ok)
+                continue;  // skip the work, still join the h step above
+            const int k = kS + q, sl = k % o.NS;
+            const uint8_t *st = s.ringS + (size_t)sl * o.slotS;
+            const uint16_t *sv = reinterpret_cast<const uint16_t *>(st + 512 * (q < nsd ? GC : GI));
+            const uint16_t *bv;
+            const uint8_t *bp;
+            const float *xgo;
+            int rb, ne, pitch, G, bgs, bms, bnbs, ot;
+            float fo;
+            if (q < nsd) {  // shared down, K chunk ch: B = hs planes of every token
+                const int it = slo + q, ch = it % nch;
+                rb = it / nch;
+                ne = T;
+                pitch = GS;
+                G = min(GC, GS - ch * GC);
+                bv = sv + 16 * GS + ch * GC;
+                sv += ch * GC;
+                const bool bvalid = (gid >> 1) < T;
+                bp = bvalid ? s.hspl + (size_t)ch * GC * hgs + gid * 32 + c * 8 : s.zero;
+                bgs = bvalid ? hgs : 0;
+                bms = bvalid ? 128 * T : 0;
+                bnbs = bvalid ? 64 * T : 0;
+                ot = c < T ? c : 0;
+                fo = s.fhs[ot];
+                xgo = s.hsg + ot * Gp + ch * GC;
+            } else {  // routed down of active expert j: B = h planes of its slots
+                const int it = rlo + q - nsd, j = it % na;
+                rb = it / na;
+                ne = s.rt.act_n[j];
+                pitch = GI;
+                G = GI;
+                bv = sv + 16 * GI;
+                const bool bvalid = (gid >> 1) < ne;
+                const int bs = bvalid ? s.rt.act_slot[4 * j + (gid >> 1)] : 0;
+                bp = bvalid ? s.hpl + (size_t)bs * GI * 256 + (gid & 1) * 32 + c * 8 : s.zero;
+                bgs = bvalid ? 256 : 0;
+                bms = bvalid ? 128 : 0;
+                bnbs = bvalid ? 64 : 0;
+                const int oslot = c < ne ? s.rt.act_slot[4 * j + c] : 0;
+                ot = oslot / K;
+                fo = s.fh[oslot];
+                xgo = s.hg + oslot * GI;
+            }
+            if (!__all_sync(0xffffffffu, pwait(&s.fullS[sl], (k / o.NS) & 1, p))) {
+                ok = false;
+                continue;
+            }
+            float a0 = 0.f, a8 = 0.f;
+            dn_math(st, sv, bv, pitch, G, bp, bgs, bms, bnbs, fo, xgo, a0, a8);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&s.emptyS[sl]);
+            if (c < ne) {
+                red_fix(y + (size_t)ot * D + 16 * rb + gid, a0);
+                red_fix(y + (size_t)ot * D + 16 * rb + gid + 8, a8);
+            }
+        }
+        kS += ndn;
+        if (!(ok = csync_and(ok)))
+            break;
+        if (tid == 0) {
+            __threadfence();
+            red_add(ctr + 2, 1);
+        }
+
+        // ---- y is complete when every CTA has added its part: out = residual + lambda y
+        if (!(ok = cwait(ctr + 2, NC, p, s)))
+            break;
+        for (int i0 = 0; i0 < T * D; i0 += 4 * kCT) {
+            long long yq[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = i0 + tid + j * kCT;
+                yq[j] = i < T * D ? __ldcg(y + i) : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+            const int i = i0 + tid + j * kCT;
+            if (i >= T * D)
+                break;
+            const float yv = __ll2float_rn(yq[j]) * kUnfix;
+            float res = 0.f;
+            if (L.res_mode == 1)
+                res = es == 2 ? bf2f(reinterpret_cast<const uint16_t *>(s.xraw)[i])
+                              : reinterpret_cast<const float *>(s.xraw)[i];
+            else if (L.res_mode == 2)
+                res = es == 2 ? bf2f(__ldg(reinterpret_cast<const uint16_t *>(L.residual) + i))
+                              : __ldg(reinterpret_cast<const float *>(L.residual) + i);
+            const float v = res + L.lam * yv;
+            if constexpr (es == 2) {
+                const uint16_t h = f2bf(v);
+                reinterpret_cast<uint16_t *>(s.xraw)[i] = h;
+                if (L.x_out && (i % NC) == C)
+                    reinterpret_cast<uint16_t *>(L.x_out)[i] = h;
+            } else {
+                reinterpret_cast<float *>(s.xraw)[i] = v;
+                if (L.x_out && (i % NC) == C)
+                    reinterpret_cast<float *>(L.x_out)[i] = v;
+            }
+            }
+        }
+        csync();
+    }
+    (void)lane;
+}
+
+template <int NB>
+__global__ void __launch_bounds__(kPT, 1) pd_kernel(const __grid_constant__ PdParams p)
+{
+    extern __shared__ __align__(1024) uint8_t sm[];
+    const Smem s = carve(sm, p);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.sm.NL; ++i) {
+            mbar_init(&s.fullL[i], 1);
+            mbar_init(&s.emptyL[i], 1);
+        }
+        for (int i = 0; i < p.sm.NS; ++i) {
+            mbar_init(&s.fullS[i], 1);
+            mbar_init(&s.emptyS[i], 1);
+        }
+        mbar_init(s.route_bar, 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 4)
+        reinterpret_cast<uint32_t *>(s.zero)[threadIdx.x] = 0u;
+    if (threadIdx.x < p.sm.NL)
+        s.icnt[threadIdx.x] = 0;
+    // Clear this CTA's share of the fixed-point sums of every layer; the first
+    // layer's logit exchange orders it before any CTA adds into them.
+    {
+        const size_t n = (size_t)p.n_layers * p.T * p.D;
+        const size_t per = (n + gridDim.x - 1) / gridDim.x, b = per * blockIdx.x;
+        for (size_t i = b + threadIdx.x; i < b + per && i < n; i += kPT)
+            p.ybuf[i] = 0;
+        __threadfence();
+    }
+    __syncthreads();
+    if (threadIdx.x >= kCT)
+        producer<NB>(p, s);
+    else
+        consumers<NB>(p, s);
+    __syncthreads();
+    // The last CTA to finish clears the counters for the next call (unless a
+    // wait gave up: then the workspace must be re-initialised).
+    __shared__ int s_last;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        int *done = p.ctr + p.n_layers * p.cstride;
+        const int old = atomicAdd(done, 1);
+        s_last = (old == (int)gridDim.x - 1) && !ld_acquire(abort_word(p));
+    }
+    __syncthreads();
+    if (s_last) {
+        __threadfence();
+        const int n = p.n_layers * p.cstride + 1;  // counters + done
+        for (int i = threadIdx.x; i < n; i += kPT)
+            p.ctr[i] = 0;
+    }
+}
+
+// ------------------------------------------------------------------- host
+
+size_t al(size_t n, size_t a) { return (n + a - 1) / a * a; }
+
+} // namespace
+
+// Shared-memory plan; returns false if no ring depth fits.
+bool pd_plan(int T, int D, int I, int S, int E, int K, int act, int n_cta, int smem_max, PdSmem *out)
+{
+    if (T < 1 || T > kPdMaxT || n_cta < 1)
+        return false;
+    const int NB = act == 0 ? 2 : 1;
+    const int GD = D / 64, GI = I / 64, GS = S / 64, TK = T * K, amax = TK < E ? TK : E;
+    const int GC = GI < GS ? GI : GS, Gp = (GS + GC - 1) / GC * GC;
+    const int es = act == 1 ? 2 : 4;
+    const size_t scratch = (size_t)4 * std::max((size_t)T * GD, (size_t)GD * (T + 2));
+    const int depths[][2] = {{4, 8}, {3, 12}, {3, 8}, {2, 8}, {2, 4}};
+    for (const auto &dp : depths) {
+        PdSmem o{};
+        o.NL = dp[0];
+        o.NS = dp[1];
+        o.slotL = (int)al((size_t)576 * GD, 128);
+        o.slotS = (int)al((size_t)512 * GI + 64 * (size_t)std::max(GI, GS), 128);
+        size_t off = al((size_t)8 * (2 * o.NL + 2 * o.NS + 1), 128);
+        auto take = [&](size_t bytes) {
+            const size_t at = off;
+            off = al(off + bytes, 128);
+            return (int)at;
+        };
+        o.ringL = take((size_t)o.NL * o.slotL);
+        o.ringS = take((size_t)o.NS * o.slotS);
+        o.xraw = take((size_t)T * D * es);
+        o.xq = take((size_t)T * D * es);
+        o.xg = take((size_t)T * GD * 4);
+        o.xpl = take((size_t)GD * 128 * NB * T);
+        o.hspl = take((size_t)Gp * 256 * T);
+        o.hsg = take((size_t)T * Gp * 4);
+        o.hpl = take((size_t)TK * GI * 256);
+        o.hg = take((size_t)TK * GI * 4);
+        o.red = take((size_t)o.NL * (kCW * 64 * 4 + 4));
+        o.lg = take((size_t)T * E * 4);
+        o.rt = take((size_t)4 * (20 + 6 * amax + 2 * TK + E));
+        o.pr = take(scratch);
+        o.misc = take((size_t)4 * (20 + TK + std::max(T, TK)));
+        o.zero = take(16);
+        o.total = (int)off;
+        if ((long long)off <= smem_max) {
+            *out = o;
+            return true;
+        }
+    }
+    return false;
+}
+
+size_t pd_ctr_ints(int E, int n_layers) { return (size_t)n_layers * (3 + E) + 2; }
+
+namespace {
+
+template <int NB>
+cudaError_t launch_nb(const PdParams &p, cudaStream_t st)
+{
+    auto k = pd_kernel<NB>;
+    static std::mutex mu;
+    static int configured = 0;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (p.sm.total > configured) {
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, p.sm.total);
+            if (e != cudaSuccess)
+                return e;
+            configured = p.sm.total;
+        }
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kPT, p.sm.total);
+    if (e != cudaSuccess)
+        return e;
+    if (per_sm < 1)
+        return cudaErrorCooperativeLaunchTooLarge;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_cta);
+    cfg.blockDim = dim3(kPT);
+    cfg.dynamicSmemBytes = p.sm.total;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k, p);
+}
+
+} // namespace
+
+cudaError_t launch_pd(const PdParams &p, cudaStream_t st)
+{
+    return p.act == 0 ? launch_nb<2>(p, st) : launch_nb<1>(p, st);
+}
+
+} // namespace mx

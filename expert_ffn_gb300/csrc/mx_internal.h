@@ -87,6 +87,7 @@ struct DnLaunch {
 // down over all experts of the blob, and the shared expert's three matrices.
 struct FfnMaps {
     CUtensorMap gate, up, down, sgate, sup, sdown;
+    CUtensorMap sdownk;  // shared down in K chunks of min(I, S)/64 groups (single-launch path)
 };
 cudaError_t get_ffn_maps(const FfnArgs &a, FfnMaps *out);
 
@@ -106,6 +107,59 @@ cudaError_t launch_route(const RouteArgs &a, const RouteLaunch &L, cudaStream_t 
 // Decode-path FFN: gate/up + GeGLU, then down + combine.  The two launches are
 // bracketed by prof_begin/prof_end (no-ops unless stage profiling is on).
 cudaError_t launch_ffn_decode(const FfnArgs &a, int max_tiles, int num_sms, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Single-launch decode path (mx_decode.cu): the block, or a stack of blocks,
+// for T <= kPdMaxT tokens in one persistent cooperative kernel.
+constexpr int kPdMaxT = 4;
+constexpr int kPdMaxLayers = 30;  // layers per launch (the layer table is a kernel parameter)
+
+// Byte offsets into the kernel's dynamic shared memory.
+struct PdSmem {
+    int NL, NS, slotL, slotS;  // ring depths and slot bytes (gate/up ring, down ring)
+    int ringL, ringS, xraw, xq, xg, xpl, hspl, hsg, hpl, hg, red, lg, rt, pr, misc, zero;
+    int total;
+};
+
+// One layer: TMA maps of its routed (over all experts of the blob) and shared
+// matrices (the shared down map in K chunks of min(I, S)/64 groups), its
+// router, the s/b offsets of the expert records, its outputs.
+struct PdLayer {
+    CUtensorMap gate, up, down, sgate, sup, sdown;
+    const uint32_t *rw;
+    const uint16_t *rs, *rb;
+    const uint8_t *blob;
+    uint64_t stride;
+    uint64_t off_s[3], off_b[3];
+    const uint16_t *ss[3], *sb[3];
+    const float *pes;
+    int32_t *topk_idx;
+    float *topk_w;
+    const void *x_in;      // the launch's first layer: its input x
+    void *x_out;           // nullable: where this layer's output goes (else it stays on chip)
+    const void *residual;  // res_mode 2
+    float lam;
+    int res_mode;          // 0 none, 1 the layer's input x, 2 `residual`
+};
+
+struct PdParams {
+    int T, D, I, S, E, K, n_layers, act, pre_norm, n_cta;
+    float eps;
+    unsigned *err;         // workspace error word
+    int *ctr;              // [n_layers][cstride] counters, then done, abort (zero on entry)
+    int cstride;           // 3 + E
+    float *logits;         // [T][E]
+    float *hbuf;           // [T*K][I] routed hidden (weighted)
+    float *hsbuf;          // [T][S] shared hidden
+    long long *ybuf;       // [n_layers][T][D] fixed-point sums of the down projections
+    PdSmem sm;
+    PdLayer L[kPdMaxLayers];
+};
+static_assert(sizeof(PdParams) <= 32764, "the layer table must fit the kernel parameter space");
+
+bool pd_plan(int T, int D, int I, int S, int E, int K, int act, int n_cta, int smem_max, PdSmem *out);
+size_t pd_ctr_ints(int E, int n_layers);
+cudaError_t launch_pd(const PdParams &p, cudaStream_t s);
 
 // Stage profiler (mx_moe_profile_*): event pair around one launch.
 enum Stage { kStageRoute = 0, kStageGateUp = 1, kStageDown = 2 };

@@ -41,9 +41,9 @@ EncodeTiledFn encode_fn()
 }
 
 // Map of `experts` matrices [rows][cols] (4-bit) at base + e*record_stride,
-// box = (8 words, box_rows rows, all groups, 1 expert).
+// box = (8 words, box_rows rows, box_groups groups (0: all), 1 expert).
 cudaError_t encode_qmat(CUtensorMap *m, const void *base, int rows, int cols, int experts, uint64_t record_stride,
-                        int box_rows)
+                        int box_rows, int box_groups = 0)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -52,7 +52,7 @@ cudaError_t encode_qmat(CUtensorMap *m, const void *base, int rows, int cols, in
     const cuuint64_t pitch = (cuuint64_t)cols / 2;
     cuuint64_t dims[4] = {8, (cuuint64_t)rows, (cuuint64_t)G, (cuuint64_t)experts};
     cuuint64_t strides[3] = {pitch, 32, experts > 1 ? (cuuint64_t)record_stride : pitch * rows};
-    cuuint32_t box[4] = {8, (cuuint32_t)box_rows, (cuuint32_t)G, 1};
+    cuuint32_t box[4] = {8, (cuuint32_t)box_rows, (cuuint32_t)(box_groups > 0 ? box_groups : G), 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void *>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -105,7 +105,8 @@ cudaError_t get_ffn_maps(const FfnArgs &a, FfnMaps *out)
         (e = encode_qmat(&m.down, a.blob + a.off_w[2], a.D, a.I, a.E, a.stride, 16)) != cudaSuccess ||
         (e = encode_qmat(&m.sgate, a.sw[0], a.S, a.D, 1, 0, 8)) != cudaSuccess ||
         (e = encode_qmat(&m.sup, a.sw[1], a.S, a.D, 1, 0, 8)) != cudaSuccess ||
-        (e = encode_qmat(&m.sdown, a.sw[2], a.D, a.S, 1, 0, 16)) != cudaSuccess)
+        (e = encode_qmat(&m.sdown, a.sw[2], a.D, a.S, 1, 0, 16)) != cudaSuccess ||
+        (e = encode_qmat(&m.sdownk, a.sw[2], a.D, a.S, 1, 0, 16, a.I < a.S ? a.I / 64 : a.S / 64)) != cudaSuccess)
         return e;
     std::lock_guard<std::mutex> g(g_mu);
     g_keys[g_next] = k;
