@@ -302,7 +302,7 @@ def bench_ours(args, cfg, world, rank, local, pg):
     h2d = T * D * es
     d2h = T * D * es + n_layers * T * K * 8
 
-    workload = cfg.name
+    workload = cfg.name if n_layers == synth.CONFIGS[args.config].layers else f"{cfg.name}[{n_layers} layers]"
     single = T <= PD_MAX_T and os.environ.get("MX_MOE_SINGLE_LAUNCH", "1") != "0"
     if single:
         # one persistent launch runs every layer of the step (up to 30 per launch):
@@ -441,10 +441,15 @@ def main():
     ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run only the first N layers of the workload (profiling captures; 0 = all)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     cfg = synth.CONFIGS[args.config]
+    if args.layers > 0:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, layers=min(args.layers, cfg.layers))
     world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
         res = bench_reference(args, cfg, world, rank, pg)
