@@ -39,7 +39,8 @@ METRIC = "MoE-layer tokens/s; decode HBM GB/s and prefill TFLOP/s as % of GB300 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = ("expert_ffn_gb300/csrc/mx_decode.cu", "expert_ffn_gb300/csrc/mx_ffn_decode.cu",
-                  "expert_ffn_gb300/csrc/mx_common.cuh", "expert_ffn_gb300/csrc/mx_route.cu")
+                  "expert_ffn_gb300/csrc/mx_common.cuh", "expert_ffn_gb300/csrc/mx_route.cu",
+                  "expert_ffn_gb300/csrc/mx_prefill.cu")
 PD_MAX_T, PD_MAX_LAYERS = 4, 30  # single-launch decode path: tokens per call, layers per launch
 
 
@@ -304,21 +305,40 @@ def bench_ours(args, cfg, world, rank, local, pg):
 
     workload = cfg.name if n_layers == synth.CONFIGS[args.config].layers else f"{cfg.name}[{n_layers} layers]"
     single = T <= PD_MAX_T and os.environ.get("MX_MOE_SINGLE_LAUNCH", "1") != "0"
-    if single:
-        # one persistent launch runs every layer of the step (up to 30 per launch):
-        # its algorithmic bytes are the whole step's
-        launches = -(-n_layers // PD_MAX_LAYERS)
-        kname, bytes_launch = "pd_kernel", step_bytes / launches
+    prefill = T > 64 and cfg.act == "bf16" and os.environ.get("MX_MOE_PREFILL_GEMM", "1") != "0"
+    if prefill:
+        # the gate/up grouped GEMM (tcgen05, FP16 operands, fp32 accumulation)
+        # is the dominant kernel: its algorithmic FLOPs per launch
+        launches = n_layers * 6  # route, index, gather, gate/up GEMM, down GEMM, combine
+        kname = "pf_gemm<0>"
+        gu_flops = 2 * 2 * T * (K * cfg.I + cfg.S) * D
+        achieved = gu_flops / gu_s / 1e12
+        # FP16 and BF16 run at the same tensor rate: the BF16 cuBLAS peak applies
+        roof = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_source": peak_src + " (bf16 burst; fp16 is the same tensor rate)",
+                "traffic": committed_traffic(kname, workload),
+                "flops_per_launch": int(gu_flops), "launch_us": round(gu_s * 1e6, 2), "launches_timed": gu_n}
+        dn_ms, dn_n = prof["down"]
+        if dn_n:
+            dn_flops = 2 * T * (K * cfg.I + cfg.S) * D
+            roof["down_gemm_tflops"] = round(dn_flops / (dn_ms / 1e3 / dn_n) / 1e12, 1)
     else:
-        launches = n_layers * 3 * ((T + 63) // 64)
-        kname, bytes_launch = "gateup_kernel", gu_bytes_per_launch
-    achieved = bytes_launch / gu_s / 1e9
-    roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
-            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "peak_source": peak_src,
-            "traffic": committed_traffic(kname, workload),
-            "bytes_per_launch": int(bytes_launch), "launch_us": round(gu_s * 1e6, 2),
-            "launches_timed": gu_n}
+        if single:
+            # one persistent launch runs every layer of the step (up to 30 per
+            # launch): its algorithmic bytes are the whole step's
+            launches = -(-n_layers // PD_MAX_LAYERS)
+            kname, bytes_launch = "pd_kernel", step_bytes / launches
+        else:
+            launches = n_layers * 3 * ((T + 63) // 64)
+            kname, bytes_launch = "gateup_kernel", gu_bytes_per_launch
+        achieved = bytes_launch / gu_s / 1e9
+        roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_source": peak_src,
+                "traffic": committed_traffic(kname, workload),
+                "bytes_per_launch": int(bytes_launch), "launch_us": round(gu_s * 1e6, 2),
+                "launches_timed": gu_n}
     step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
     stages_us = {k: round(v[0] * 1e3 / max(v[1], 1), 2) for k, v in prof.items()}
     res = {

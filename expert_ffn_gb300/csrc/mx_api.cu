@@ -118,6 +118,8 @@ struct Plan {
     // single-launch decode path (T <= kPdMaxT)
     size_t pd_ctr, pd_logits, pd_h, pd_hs, pd_y, pd_x;
     int pd_T;
+    // prefill path (T > kDecodeChunk, BF16)
+    size_t pf;
     size_t total;
     int max_tiles_route;
 };
@@ -157,6 +159,9 @@ Plan make_plan(const mx_moe_layout *L, int T_route, int T_ffn)
     p.pd_hs = take(Tp * S * 4);
     p.pd_y = take((size_t)kPdMaxLayers * Tp * D * 8);
     p.pd_x = take(Tp * D * es);
+    p.pf = (T_route > kDecodeChunk && L->act_dtype == MX_BF16)
+               ? take(pf_workspace_bytes(T_route, (int)D, (int)I, (int)S, (int)E, (int)K))
+               : o;
     p.total = o;
     return p;
 }
@@ -470,10 +475,74 @@ mx_status run_pass(const void *x, int T, const mx_qlinear *router, const mx_ffn 
     return MX_OK;
 }
 
+// Prefill: prepare the activations, route all T tokens at once from them, then
+// the grouped tensor-core GEMMs.
+mx_status run_prefill(const Call &c, const Plan &p, uint8_t *ws, cudaStream_t s)
+{
+    const mx_moe_layout *L = c.L;
+    RouteArgs ra = route_args(c.x, c.T, c.router, L, c.opt, p, ws);
+    ra.topk_idx = c.topk_idx;
+    ra.topk_w = c.topk_w;
+    ra.xp = nullptr;
+    PfCall f{};
+    f.x = c.x;
+    f.T = c.T;
+    f.D = L->d_model;
+    f.I = L->d_expert;
+    f.S = L->d_shared;
+    f.E = L->n_experts;
+    f.K = L->top_k;
+    f.pre_norm = (c.opt && c.opt->pre_rmsnorm) ? 1 : 0;
+    f.eps = c.opt ? c.opt->rms_eps : 0.0f;
+    f.perm = ra.perm;
+    f.counts = ra.counts;
+    f.offsets = ra.offsets;
+    f.topk_w = c.topk_w;
+    f.blob = static_cast<const uint8_t *>(c.blob);
+    f.stride = L->record_stride;
+    const mx_sub *subs[3] = {&L->gate, &L->up, &L->down};
+    const mx_qlinear *sq[3] = {&c.shared->gate, &c.shared->up, &c.shared->down};
+    for (int j = 0; j < 3; ++j) {
+        f.off_w[j] = subs[j]->w;
+        f.off_s[j] = subs[j]->s;
+        f.off_b[j] = subs[j]->b;
+        f.sw[j] = static_cast<const uint32_t *>(sq[j]->w);
+        f.ss[j] = static_cast<const uint16_t *>(sq[j]->scales);
+        f.sb[j] = static_cast<const uint16_t *>(sq[j]->biases);
+    }
+    f.lam = L->layer_scalar;
+    f.residual = c.opt ? c.opt->residual : nullptr;
+    f.out = c.out;
+    f.err = ra.err;
+    f.ws = ws + p.pf;
+    f.n_cta = num_sms();
+    PfPrepared pp;
+    prof_begin(kStageRoute, s);
+    cudaError_t e = launch_prefill_prepare(f, &pp, s);
+    if (e == cudaSuccess)
+        e = launch_route_large(ra, pp.X16, pp.xsc, pp.XG, s);
+    prof_end(kStageRoute, s);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "prefill routing");
+    e = launch_prefill(f, s);  // times its gate/up GEMM and its down GEMM + combine as stages 1 and 2
+    if (e != cudaSuccess)
+        return cuda_fail(e, "prefill kernels");
+    return MX_OK;
+}
+
 mx_status forward_impl(const Call &c, cudaStream_t s, void *ws, size_t ws_bytes)
 {
     const int D = c.L->d_model, K = c.L->top_k;
     const size_t es = c.L->act_dtype == MX_F32 ? 4 : 2;
+    const char *pf_env = getenv("MX_MOE_PREFILL_GEMM");
+    if (c.T > kDecodeChunk && c.L->act_dtype == MX_BF16 && !(pf_env && pf_env[0] == '0')) {
+        const Plan p = make_plan(c.L, c.T, ffn_tokens(c.T));
+        if (!ws || ws_bytes < p.total)
+            return fail(MX_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes, p.total);
+        if (!aligned(ws, 256))
+            return fail(MX_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
+        return run_prefill(c, p, static_cast<uint8_t *>(ws), s);
+    }
     const Plan p = make_plan(c.L, ffn_tokens(c.T), ffn_tokens(c.T));
     if (!ws || ws_bytes < p.total)
         return fail(MX_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes, p.total);
@@ -548,7 +617,7 @@ size_t mx_moe_stack_workspace_bytes(const mx_moe_layout *layout, int T)
         return 0;
     const int t = T < 1 ? 1 : T;
     // the per-layer plan, then the ping-pong activation buffer
-    return make_plan(layout, ffn_tokens(t), ffn_tokens(t)).total + up256((size_t)t * layout->d_model * 4);
+    return make_plan(layout, t, ffn_tokens(t)).total + up256((size_t)t * layout->d_model * 4);
 }
 
 mx_status mx_moe_workspace_init(void *ws, size_t ws_bytes, void *stream)
@@ -688,7 +757,7 @@ mx_status mx_moe_stack_forward(void *x_io, int T, int n_layers, const mx_qlinear
     if (!aligned(ws, 256))
         return fail(MX_ERR_ALIGNMENT, "workspace must be 256-byte aligned");
     const int t1 = T < 1 ? 1 : T;
-    const size_t layer_ws = make_plan(L0, ffn_tokens(t1), ffn_tokens(t1)).total;
+    const size_t layer_ws = make_plan(L0, t1, ffn_tokens(t1)).total;
     uint8_t *xbuf = static_cast<uint8_t *>(ws) + layer_ws;
     for (int l = 0; l < n_layers; ++l) {
         const mx_moe_layout *L = &layouts[l];

@@ -161,6 +161,70 @@ bool pd_plan(int T, int D, int I, int S, int E, int K, int act, int n_cta, int s
 size_t pd_ctr_ints(int E, int n_layers);
 cudaError_t launch_pd(const PdParams &p, cudaStream_t s);
 
+// ---------------------------------------------------------------------------
+// Prefill path (mx_prefill.cu): T > kDecodeChunk tokens with BF16 activations;
+// grouped GEMMs on tcgen05 tensor cores.
+
+// Arguments of the grouped-GEMM kernel (one per launch: gate/up or down).
+struct PfArgs {
+    int mode;               // 0 gate/up, 1 down
+    int T, D, I, S, E, K;
+    int FT, FTs;            // weight-row tiles: routed, shared
+    int KT, KTs;            // K tiles of 64 columns: routed, shared
+    int GK, GK_s;           // scale groups per weight row: routed, shared
+    int rows, rows_s;       // weight rows: routed, shared
+    const int32_t *tt_off;  // [E+1] per-expert token-tile offsets
+    const int32_t *counts, *offsets, *perm;
+    const float *xsc;       // [T] 2^-k of each token's FP16 scale
+    const uint8_t *blob;
+    uint64_t stride;
+    uint64_t off_s[3], off_b[3];
+    const uint16_t *ss[3], *sb[3];
+    void *H, *Hs;           // FP16 [T*K][I], [T][S] (operand column order)
+    float *Y, *Ys;          // fp32 [T*K][D], [T][D]
+    unsigned *err;
+    CUtensorMap wa, wb;     // routed packed weights (gate, up) or (down, -)
+    CUtensorMap swa, swb;   // shared packed weights
+    CUtensorMap xr, xs;     // FP16 operand rows: routed slots, shared tokens
+};
+
+// One prefill call, after the router has written counts/offsets/perm/topk.
+struct PfCall {
+    const void *x;          // BF16 [T][D]
+    int T, D, I, S, E, K;
+    int pre_norm;
+    float eps;
+    const int32_t *perm, *counts, *offsets;
+    const float *topk_w;
+    const uint8_t *blob;
+    uint64_t stride;
+    uint64_t off_w[3], off_s[3], off_b[3];
+    const uint32_t *sw[3];
+    const uint16_t *ss[3], *sb[3];
+    float lam;
+    const void *residual;   // BF16, nullable
+    void *out;              // BF16 [T][D]
+    unsigned *err;
+    uint8_t *ws;            // pf_workspace_bytes(...)
+    int n_cta;
+};
+
+// Buffers the router reads on the prefill path: FP16 activations in operand
+// order (scaled per token by xsc^-1), per-group sums of the BF16 values.
+struct PfPrepared {
+    const void *X16;
+    const float *xsc, *XG;
+};
+
+size_t pf_workspace_bytes(int T, int D, int I, int S, int E, int K);
+// Before routing: (optional rmsnorm) -> FP16 rows, scales, group sums.
+cudaError_t launch_prefill_prepare(const PfCall &c, PfPrepared *out, cudaStream_t s);
+// After routing: scatter, gate/up GEMM, down GEMM, combine.
+cudaError_t launch_prefill(const PfCall &c, cudaStream_t s);
+// Routing of many tokens from the prepared activations (same logits, bit for bit).
+cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float *xsc, const float *XG,
+                               cudaStream_t s);
+
 // Stage profiler (mx_moe_profile_*): event pair around one launch.
 enum Stage { kStageRoute = 0, kStageGateUp = 1, kStageDown = 2 };
 void prof_begin(int stage, cudaStream_t s);

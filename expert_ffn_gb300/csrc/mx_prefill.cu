@@ -1,0 +1,855 @@
+// mx_prefill.cu -- prefill path (T > 64 tokens, BF16 activations): grouped
+// GEMMs on the 5th-generation tensor cores (tcgen05, accumulators in TMEM).
+//
+// What it computes is the block of the "Mference System design" page: section
+// "Prefill" (token/expert pairs grouped into per-expert work, each expert's
+// weights streamed once for all its tokens), section "Metal execution" (affine
+// decode of the packed weights fused into the expert kernels, GeGLU, the
+// weighted expert reduction), section "Why the runtime has this shape" (shared
+// expert without a routing weight, layer scalar).
+//
+// Sequence (one stream):
+//   route    router GEMV + top-k + softmax + grouping of slots by expert
+//            (mx_route.cu; exact, the canonical logit order)
+//   index    inverse permutation; per-expert token-tile offsets
+//   gather   x -> FP16 rows (scaled per token by a power of two, operand column
+//            order), once in token order (shared expert) and once per slot in
+//            expert order (routed experts)
+//   gate/up  grouped GEMM, tiles of 128 weight rows x 128 tokens:
+//            h = gelu(W_gate x) * (W_up x), FP16 [slot][I] and [T][S]
+//   down     grouped GEMM: y = W_down h, fp32 [slot][D] and [T][D]
+//   combine  out = residual + lambda * (shared + sum_k w_k y_k), k ascending
+//
+// The GEMM kernel is persistent (one CTA per SM) and warp-specialised:
+//   warp 0      TMA producer: packed 4-bit weight rows (one group of 64
+//               columns per stage) and the 128-token operand tile
+//               (SWIZZLE_128B) into a ring of stages;
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma (M = 128,
+//               N = the tile's tokens rounded up to 16, K = 16, FP16 in, fp32
+//               accumulate) and commits to mbarriers;
+//   warps 2-9   dequantize: w = s*q + b in FP16 (one fused multiply-add on a
+//               half2 of exact integers), written in the 128-byte swizzled
+//               K-major layout the MMA reads (two threads per weight row);
+//   warps 10-13 epilogue: tcgen05.ld of the accumulators (two TMEM buffers,
+//               so the next tile's MMAs overlap this tile's epilogue).
+// Why FP16 and not BF16: BF16 rounding of the dequantized weights (8-bit
+// significand) alone gives ~1.6e-3 relative error per GEMM, above the 1e-3
+// rel-L2 bar on BF16 outputs; FP16 (11-bit significand) gives ~2e-4.  BF16
+// activations are exact in FP16 after a per-token power-of-two scale.
+#include "mx_common.cuh"
+#include "mx_internal.h"
+
+#include <cuda_fp16.h>
+#include <mutex>
+
+namespace mx {
+
+namespace {
+
+constexpr int kMT = 128;  // weight rows per tile (MMA M)
+constexpr int kNT = 128;  // tokens per tile (MMA N, at most)
+constexpr int kDqWarps = 8;  // dequantizing warps (2..9)
+constexpr int kWarps = 2 + kDqWarps + 4, kThreads = kWarps * 32;
+constexpr int kEpiWarp0 = 2 + kDqWarps;  // first epilogue warp
+// Ring depths per kernel (gate/up holds two weight matrices per stage):
+// packed weights + operand tile, and dequantized FP16 weight tiles.  The FP16
+// ring is what lets the dequantizing warps run ahead of the MMAs.
+template <int MODE> struct Depth;
+template <> struct Depth<0> { static constexpr int NP = 5, NF = 3; };
+template <> struct Depth<1> { static constexpr int NP = 6, NF = 4; };
+constexpr int kBTile = kNT * 128;  // bytes of one operand tile (128 tokens x 64 FP16)
+constexpr int kFTile = kMT * 128;  // bytes of one FP16 weight tile (128 rows x 64)
+
+// ------------------------------------------------------------- tcgen05 glue
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (the layout TMA writes with SWIZZLE_128B).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    return (uint64_t)((saddr & 0x3FFFF) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor: FP16 A and B (K-major), fp32 D, M = 128, N.
+__device__ __forceinline__ uint32_t idesc_f16(int n) { return (1u << 4) | ((uint32_t)(n >> 3) << 17) | (8u << 24); }
+
+__device__ __forceinline__ void umma(uint32_t dtm, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtm),
+                 "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                   "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+                   "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+                   "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(ta));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                 "%3}], [%4];" ::"r"(smem_u32(dst)),
+                 "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                       uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+                 "%3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+                 "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// ------------------------------------------------------------------- units
+
+struct Unit {
+    int shared;  // 1: the shared expert
+    int e;       // routed expert
+    int row0;    // first weight row of the tile
+    int slot0;   // first token row of the tile (slot position or token)
+    int n;       // tokens in the tile
+    int kt_n;    // K tiles
+};
+
+__device__ __forceinline__ Unit unit_of(const PfArgs &a, int u, int nR)
+{
+    Unit U;
+    if (u < nR * a.FT) {
+        const int tile = u / a.FT, f = u - tile * a.FT;
+        int lo = 0, hi = a.E;
+        while (lo + 1 < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(a.tt_off + mid) <= tile)
+                lo = mid;
+            else
+                hi = mid;
+        }
+        const int tt = tile - __ldg(a.tt_off + lo);
+        U.shared = 0;
+        U.e = lo;
+        U.row0 = kMT * f;
+        U.slot0 = __ldg(a.offsets + lo) + kNT * tt;
+        U.n = min(kNT, __ldg(a.offsets + lo) + __ldg(a.counts + lo) - U.slot0);
+        U.kt_n = a.KT;
+    } else {
+        const int v = u - nR * a.FT, tt = v / a.FTs, f = v - tt * a.FTs;
+        U.shared = 1;
+        U.e = 0;
+        U.row0 = kMT * f;
+        U.slot0 = kNT * tt;
+        U.n = min(kNT, a.T - U.slot0);
+        U.kt_n = a.KTs;
+    }
+    return U;
+}
+
+// Bounded mbarrier wait of the GEMM: false once this CTA has given up (a
+// wait ran past kWaitLimitNs anywhere in the CTA), so one stuck stage costs one
+// time limit, not one per remaining stage.
+__device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, unsigned *err, volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort)
+            return false;
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            *abort = 1;
+            return false;
+        }
+    }
+    return true;
+}
+
+// Nibbles j and j+4 of w as exact FP16 integers (1024 + q) - 1024.
+template <int J>
+__device__ __forceinline__ __half2 nib_h2(uint32_t w)
+{
+    const uint32_t v = ((w >> (4 * J)) & 0x000F000Fu) | 0x64006400u;
+    return __hsub2(*reinterpret_cast<const __half2 *>(&v), __float2half2_rn(1024.0f));
+}
+
+// One packed word (8 weights of a row) -> 8 FP16 weights in operand order
+// [0,4,1,5,2,6,3,7], w = s*q + b with one rounding.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 s2, __half2 b2)
+{
+    const __half2 p0 = __hfma2(nib_h2<0>(w), s2, b2), p1 = __hfma2(nib_h2<1>(w), s2, b2);
+    const __half2 p2 = __hfma2(nib_h2<2>(w), s2, b2), p3 = __hfma2(nib_h2<3>(w), s2, b2);
+    return make_uint4(*reinterpret_cast<const uint32_t *>(&p0), *reinterpret_cast<const uint32_t *>(&p1),
+                      *reinterpret_cast<const uint32_t *>(&p2), *reinterpret_cast<const uint32_t *>(&p3));
+}
+
+// Position of column c in the operand order [0,4,1,5,2,6,3,7] of its 8-block.
+__device__ __forceinline__ int opos(int c)
+{
+    const int a = c & 7;
+    return (c & ~7) | (a < 4 ? 2 * a : 2 * (a - 4) + 1);
+}
+
+// ------------------------------------------------------------ GEMM kernel
+
+// MODE 0: gate/up (two weight matrices, h = gelu(g) * u).  MODE 1: down.
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ PfArgs a)
+{
+    constexpr int NMAT = MODE == 0 ? 2 : 1;
+    constexpr int kNP = Depth<MODE>::NP, kNF = Depth<MODE>::NF;
+    constexpr uint32_t kPacked = 128 * 32;  // packed bytes of one matrix tile (128 rows x 64 columns)
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *fring = sm;                                   // kNF x NMAT x kFTile
+    uint8_t *bring = fring + kNF * NMAT * kFTile;          // kNP x kBTile
+    uint8_t *pring = bring + kNP * kBTile;                 // kNP x NMAT x kPacked
+    uint64_t *bars = reinterpret_cast<uint64_t *>(pring + kNP * NMAT * kPacked);
+    uint64_t *p_full = bars, *p_empty = bars + kNP, *f_full = bars + 2 * kNP, *f_empty = f_full + kNF;
+    uint64_t *acc_full = f_empty + kNF, *acc_empty = acc_full + 2;
+    uint64_t *mma_done = acc_empty + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int kCols = MODE == 0 ? 512 : 256;  // two accumulator buffers
+
+    if (tid == 0) {
+        for (int i = 0; i < kNP; ++i) {
+            mbar_init(&p_full[i], 1);
+            mbar_init(&p_empty[i], kDqWarps + 1);  // the dequantizing warps + the MMA commit
+        }
+        for (int i = 0; i < kNF; ++i) {
+            mbar_init(&f_full[i], kDqWarps);
+            mbar_init(&f_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        mbar_init(mma_done, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
+                     "r"(kCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int nR = __ldg(a.tt_off + a.E);
+    const int n_units = nR * a.FT + ((a.T + kNT - 1) / kNT) * a.FTs;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        int kp = 0;
+        if (lane == 0) {
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const Unit U = unit_of(a, u, nR);
+                for (int kt = 0; kt < U.kt_n; ++kt, ++kp) {
+                    const int sp = kp % kNP;
+                    if (kp >= kNP && !(ok = bwait(&p_empty[sp], ((kp / kNP) - 1) & 1, a.err, abort)))
+                        break;
+                    mbar_arrive_expect_tx(&p_full[sp], kBTile + NMAT * kPacked);
+                    tma_2d(bring + sp * kBTile, U.shared ? &a.xs : &a.xr, 64 * kt, U.slot0, &p_full[sp]);
+                    uint8_t *pk = pring + sp * NMAT * kPacked;
+                    if (U.shared) {
+                        tma_4d(pk, &a.swa, 0, U.row0, kt, 0, &p_full[sp]);
+                        if (NMAT == 2)
+                            tma_4d(pk + kPacked, &a.swb, 0, U.row0, kt, 0, &p_full[sp]);
+                    } else {
+                        tma_4d(pk, &a.wa, 0, U.row0, kt, U.e, &p_full[sp]);
+                        if (NMAT == 2)
+                            tma_4d(pk + kPacked, &a.wb, 0, U.row0, kt, U.e, &p_full[sp]);
+                    }
+                }
+            }
+            // leave no copy in flight (plain bounded waits: copies complete on their own)
+            for (int k = (kp > kNP ? kp - kNP : 0); k < kp; ++k)
+                mbar_wait(&p_full[k % kNP], (k / kNP) & 1, a.err);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA
+        if (lane == 0) {
+            int kp = 0, kf = 0, ai = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ai) {
+                const Unit U = unit_of(a, u, nR);
+                const int b = ai & 1;
+                if (ai >= 2 && !(ok = bwait(&acc_empty[b], ((ai / 2) - 1) & 1, a.err, abort)))
+                    break;
+                tc_fence_after();
+                const int nm = max(16, (U.n + 15) & ~15);
+                const uint32_t idesc = idesc_f16(nm);
+                const uint32_t d0 = tmem + (uint32_t)(b * (kCols / 2));
+                for (int kt = 0; kt < U.kt_n; ++kt, ++kp, ++kf) {
+                    const int sp = kp % kNP, sf = kf % kNF;
+                    if (!(ok = bwait(&f_full[sf], (kf / kNF) & 1, a.err, abort) &&
+                               bwait(&p_full[sp], (kp / kNP) & 1, a.err, abort)))
+                        break;
+                    tc_fence_after();
+                    const uint32_t bb = smem_u32(bring + sp * kBTile);
+                    const uint32_t fa = smem_u32(fring + sf * NMAT * kFTile);
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        const uint64_t bd = sw128_desc(bb + 32 * ks);
+                        const uint32_t acc = (kt | ks) ? 1u : 0u;
+                        umma(d0, sw128_desc(fa + 32 * ks), bd, idesc, acc);
+                        if (NMAT == 2)
+                            umma(d0 + 128, sw128_desc(fa + kFTile + 32 * ks), bd, idesc, acc);
+                    }
+                    umma_commit(&f_empty[sf]);
+                    umma_commit(&p_empty[sp]);
+                }
+                if (ok)
+                    umma_commit(&acc_full[b]);
+            }
+            // every MMA this thread issued has completed before TMEM is freed
+            umma_commit(mma_done);
+            mbar_wait(mma_done, 0, a.err);
+        }
+        __syncwarp();
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------ dequantize
+        // 256 threads, two per weight row: gate/up -> one matrix each; down ->
+        // four of the row's eight words each
+        const int r2 = tid - 64, r = r2 & (kMT - 1), half = r2 >> 7;
+        const int m = MODE == 0 ? half : 0;                 // matrix of this thread
+        const int w0 = MODE == 0 ? 0 : 4 * half, nw = MODE == 0 ? 8 : 4;
+        int kp = 0, kf = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const Unit U = unit_of(a, u, nR);
+            const int rows = U.shared ? a.rows_s : a.rows;
+            const int row = U.row0 + r;
+            const bool valid = row < rows;
+            const int G = U.shared ? a.GK_s : a.GK;  // groups per weight row
+            const int j = MODE == 0 ? m : 2;         // gate, up, or down
+            const uint16_t *sv, *bv;
+            if (U.shared) {
+                sv = a.ss[j] + (size_t)row * G;
+                bv = a.sb[j] + (size_t)row * G;
+            } else {
+                const uint8_t *rec = a.blob + (uint64_t)U.e * a.stride;
+                sv = reinterpret_cast<const uint16_t *>(rec + a.off_s[j]) + (size_t)row * G;
+                bv = reinterpret_cast<const uint16_t *>(rec + a.off_b[j]) + (size_t)row * G;
+            }
+            // the row's scale and bias of group kt, loaded kLook K tiles ahead
+            // into a register ring (the shared-memory carve-out leaves L1 too
+            // small to keep them)
+            constexpr int kLook = 4;
+            uint16_t s_r[kLook], b_r[kLook];
+#pragma unroll
+            for (int j = 0; j < kLook; ++j) {
+                s_r[j] = (valid && j < U.kt_n) ? __ldg(sv + j) : (uint16_t)0;
+                b_r[j] = (valid && j < U.kt_n) ? __ldg(bv + j) : (uint16_t)0;
+            }
+            for (int kt4 = 0; kt4 < U.kt_n && ok; kt4 += kLook)
+#pragma unroll
+            for (int jj = 0; jj < kLook; ++jj) {
+                const int kt = kt4 + jj;
+                if (kt >= U.kt_n)
+                    break;
+                const int sp = kp % kNP, sf = kf % kNF;
+                const __half2 s2 = __float2half2_rn(bf2f(s_r[jj])), b2 = __float2half2_rn(bf2f(b_r[jj]));
+                if (valid && kt + kLook < U.kt_n) {
+                    s_r[jj] = __ldg(sv + kt + kLook);
+                    b_r[jj] = __ldg(bv + kt + kLook);
+                }
+                ok = bwait(&p_full[sp], (kp / kNP) & 1, a.err, abort) &&
+                     (kf < kNF || bwait(&f_empty[sf], ((kf / kNF) - 1) & 1, a.err, abort));
+                if (!__all_sync(0xffffffffu, ok)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t *src = reinterpret_cast<const uint32_t *>(pring + (sp * NMAT + m) * kPacked + r * 32);
+                uint8_t *dst = fring + (sf * NMAT + m) * kFTile + r * 128;
+                if (MODE == 0) {
+                    const uint4 q0 = reinterpret_cast<const uint4 *>(src)[0], q1 = reinterpret_cast<const uint4 *>(src)[1];
+                    const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        *reinterpret_cast<uint4 *>(dst + ((w ^ (r & 7)) << 4)) = dequant_word(wv[w], s2, b2);
+                } else {
+                    const uint4 q = reinterpret_cast<const uint4 *>(src)[half];
+                    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                        *reinterpret_cast<uint4 *>(dst + (((w0 + w) ^ (r & 7)) << 4)) = dequant_word(wv[w], s2, b2);
+                }
+                (void)nw;
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&f_full[sf]);
+                    mbar_arrive(&p_empty[sp]);
+                }
+                ++kp;
+                ++kf;
+            }
+        }
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int q = warp & 3;  // TMEM lane quadrant of this warp
+        int ai = 0;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++ai) {
+            const Unit U = unit_of(a, u, nR);
+            const int b = ai & 1;
+            if (!__all_sync(0xffffffffu, bwait(&acc_full[b], (ai / 2) & 1, a.err, abort)))
+                break;
+            tc_fence_after();
+            const int rows = U.shared ? a.rows_s : a.rows;
+            const int row = U.row0 + 32 * q + lane;
+            const bool valid = row < rows;
+            const uint32_t d0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * (kCols / 2));
+            for (int c0 = 0; c0 < U.n; c0 += 32) {
+                uint32_t g[32];
+                tmem_ld32(d0 + c0, g);
+                if (MODE == 0) {
+                    uint32_t v[32];
+                    tmem_ld32(d0 + 128 + c0, v);
+                    __half *H = static_cast<__half *>(U.shared ? a.Hs : a.H);
+                    const int ld = U.shared ? a.S : a.I;
+                    // lane j fetches the token scale of column c0 + j once
+                    float my_sc = 0.f;
+                    if (c0 + lane < U.n) {
+                        const int p = U.slot0 + c0 + lane;
+                        my_sc = __ldg(a.xsc + (U.shared ? p : __ldg(a.perm + p) / a.K));
+                    }
+#pragma unroll 4
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = c0 + j;
+                        const float sc = __shfl_sync(0xffffffffu, my_sc, j);
+                        if (col < U.n && valid) {
+                            const int p = U.slot0 + col;
+                            const float gg = __uint_as_float(g[j]) * sc, uu = __uint_as_float(v[j]) * sc;
+                            float h = gelu_tanh(gg) * uu;
+                            h = fminf(fmaxf(h, -65504.f), 65504.f);
+                            H[(size_t)p * ld + opos(row)] = __float2half_rn(h);
+                        }
+                    }
+                } else {
+                    float *Y = U.shared ? a.Ys : a.Y;
+#pragma unroll 4
+                    for (int j = 0; j < 32; ++j) {
+                        const int col = c0 + j;
+                        if (col < U.n && valid)
+                            Y[(size_t)(U.slot0 + col) * a.D + row] = __uint_as_float(g[j]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&acc_empty[b]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+}
+
+// -------------------------------------------------------------- small kernels
+
+// inv[perm[i]] = i; block 0 also writes the per-expert token-tile offsets.
+__global__ void pf_index(const int32_t *perm, int n, const int32_t *counts, int E, int32_t *inv, int32_t *tt_off)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n)
+        inv[__ldg(perm + i)] = i;
+    if (blockIdx.x == 0 && threadIdx.x < 32) {
+        const int lane = threadIdx.x, per = (E + 31) / 32, e0 = lane * per, e1 = min(E, e0 + per);
+        int sum = 0;
+        for (int e = e0; e < e1; ++e)
+            sum += (__ldg(counts + e) + kNT - 1) / kNT;
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl += y;
+        }
+        int run = incl - sum;
+        for (int e = e0; e < e1; ++e) {
+            tt_off[e] = run;
+            run += (__ldg(counts + e) + kNT - 1) / kNT;
+        }
+        if (lane == 31)
+            tt_off[E] = incl;
+    }
+}
+
+// One CTA per token: optional rmsnorm (canonical order, rounded to BF16), the
+// token's power-of-two scale, its FP16 row in operand order, and its per-group
+// sums in the fixed add order (the router's X).
+__global__ void __launch_bounds__(256) pf_norm(const uint16_t *x, int D, int pre_norm, float eps, __half *X16,
+                                               float *xsc, float *XG)
+{
+    extern __shared__ float gs[];  // D floats, then 64 + D/64 scratch
+    float *xv = gs, *scr = gs + D;
+    const int t = blockIdx.x, tid = threadIdx.x, G = D / 64;
+    const uint16_t *xr = x + (size_t)t * D;
+    for (int i = tid; i < D; i += 256)
+        xv[i] = bf2f(__ldg(xr + i));
+    __syncthreads();
+    if (pre_norm) {
+        for (int g = tid; g < G; g += 256) {
+            float q = 0.f;
+            for (int k = 0; k < 64; ++k)
+                q = fmaf(xv[64 * g + k], xv[64 * g + k], q);
+            scr[64 + g] = q;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float ss = 0.f;
+            for (int g = 0; g < G; ++g)
+                ss = ss + scr[64 + g];
+            scr[0] = 1.0f / sqrtf(ss / (float)D + eps);
+        }
+        __syncthreads();
+        const float r = scr[0];
+        for (int i = tid; i < D; i += 256)
+            xv[i] = bf2f(f2bf(xv[i] * r));
+        __syncthreads();
+    }
+    for (int g = tid; g < G; g += 256) {
+        float X = 0.f;
+        for (int k = 0; k < 64; ++k)
+            X = X + xv[64 * g + k];
+        XG[(size_t)t * G + g] = X;
+    }
+    float mx = 0.f;
+    for (int i = tid; i < D; i += 256)
+        mx = fmaxf(mx, fabsf(xv[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    __syncthreads();
+    if ((tid & 31) == 0)
+        scr[1 + (tid >> 5)] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        float m = 0.f;
+        for (int w = 0; w < 8; ++w)
+            m = fmaxf(m, scr[1 + w]);
+        // 2^k with m * 2^k in [2^14, 2^15)
+        const int E2 = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;
+        int k = m > 0.f ? 14 - E2 : 0;
+        k = k > 100 ? 100 : (k < -100 ? -100 : k);
+        scr[0] = ldexpf(1.0f, k);
+        xsc[t] = ldexpf(1.0f, -k);
+    }
+    __syncthreads();
+    const float sc = scr[0];
+    __half *row = X16 + (size_t)t * D;
+    for (int i = tid; i < D; i += 256)
+        row[opos(i)] = __float2half_rn(xv[i] * sc);
+}
+
+// Copies of each token's FP16 row at the positions of its K slots (expert order).
+__global__ void __launch_bounds__(256) pf_scatter(const __half *X16, int D, int K, const int32_t *inv, __half *Xr)
+{
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const uint4 *src = reinterpret_cast<const uint4 *>(X16 + (size_t)t * D);
+    for (int k = 0; k < K; ++k) {
+        uint4 *dst = reinterpret_cast<uint4 *>(Xr + (size_t)__ldg(inv + (size_t)t * K + k) * D);
+        for (int i = tid; i < D / 8; i += 256)
+            dst[i] = __ldg(src + i);
+    }
+}
+
+// out[t] = residual[t] + lambda * (shared[t] + sum_k w[t,k] * y[slot(t,k)]), k ascending.
+__global__ void __launch_bounds__(256) pf_combine(const float *Y, const float *Ys, const int32_t *inv,
+                                                  const float *topk_w, int T, int D, int K, float lam,
+                                                  const uint16_t *residual, uint16_t *out)
+{
+    const int t = blockIdx.y, d = 4 * (blockIdx.x * 256 + threadIdx.x);
+    if (t >= T || d >= D)
+        return;
+    float4 acc = *reinterpret_cast<const float4 *>(Ys + (size_t)t * D + d);
+    for (int k = 0; k < K; ++k) {
+        const float w = __ldg(topk_w + (size_t)t * K + k);
+        const float4 y = *reinterpret_cast<const float4 *>(Y + (size_t)__ldg(inv + (size_t)t * K + k) * D + d);
+        acc.x = acc.x + w * y.x;
+        acc.y = acc.y + w * y.y;
+        acc.z = acc.z + w * y.z;
+        acc.w = acc.w + w * y.w;
+    }
+    float r[4] = {0.f, 0.f, 0.f, 0.f};
+    if (residual) {
+        const uint2 rv = *reinterpret_cast<const uint2 *>(residual + (size_t)t * D + d);
+        r[0] = __uint_as_float(rv.x << 16);
+        r[1] = __uint_as_float(rv.x & 0xFFFF0000u);
+        r[2] = __uint_as_float(rv.y << 16);
+        r[3] = __uint_as_float(rv.y & 0xFFFF0000u);
+    }
+    const float o[4] = {r[0] + lam * acc.x, r[1] + lam * acc.y, r[2] + lam * acc.z, r[3] + lam * acc.w};
+    uint2 ov;
+    ov.x = (uint32_t)f2bf(o[0]) | ((uint32_t)f2bf(o[1]) << 16);
+    ov.y = (uint32_t)f2bf(o[2]) | ((uint32_t)f2bf(o[3]) << 16);
+    *reinterpret_cast<uint2 *>(out + (size_t)t * D + d) = ov;
+}
+
+// ------------------------------------------------------------------- host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// FP16 rows [rows][cols] as a 2-D tensor, box (64 columns, 128 rows), 128-byte swizzle.
+cudaError_t encode_rows(CUtensorMap *m, const void *base, int rows, int cols)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)kNT};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// Packed 4-bit weights as (8 words, rows, groups, experts), box (8, 128, 1, 1).
+cudaError_t encode_packed(CUtensorMap *m, const void *base, int rows, int cols, int experts, uint64_t record_stride)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    const int G = cols / 64;
+    const cuuint64_t pitch = (cuuint64_t)cols / 2;
+    cuuint64_t dims[4] = {8, (cuuint64_t)rows, (cuuint64_t)G, (cuuint64_t)experts};
+    cuuint64_t strides[3] = {pitch, 32, experts > 1 ? (cuuint64_t)record_stride : pitch * rows};
+    cuuint32_t box[4] = {8, (cuuint32_t)kMT, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, const_cast<void *>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int MODE>
+size_t gemm_smem()
+{
+    const int nmat = MODE == 0 ? 2 : 1, np = Depth<MODE>::NP, nf = Depth<MODE>::NF;
+    return 1024 + (size_t)nf * nmat * kFTile + (size_t)np * kBTile + (size_t)np * nmat * 128 * 32 + 256;
+}
+
+template <int MODE>
+cudaError_t launch_gemm(const PfArgs &a, int n_cta, cudaStream_t s)
+{
+    auto k = pf_gemm<MODE>;
+    const size_t smem = gemm_smem<MODE>();
+    static std::mutex mu;
+    static bool configured = false;
+    {
+        std::lock_guard<std::mutex> g(mu);
+        if (!configured) {
+            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess)
+                return e;
+            configured = true;
+        }
+    }
+    k<<<n_cta, kThreads, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+namespace {
+
+struct PfBufs {
+    int32_t *inv, *tt_off;
+    float *xsc, *XG;
+    __half *X16, *Xr, *H, *Hs;
+    float *Y, *Ys;
+    size_t total;
+};
+
+PfBufs pf_carve(uint8_t *w, int T, int D, int I, int S, int E, int K)
+{
+    auto up = [](size_t n) { return (n + 255) & ~size_t(255); };
+    const size_t TK = (size_t)T * K;
+    PfBufs b;
+    uint8_t *p = w;
+    auto take = [&](size_t bytes) {
+        uint8_t *at = p;
+        p += up(bytes);
+        return at;
+    };
+    b.inv = reinterpret_cast<int32_t *>(take(TK * 4));
+    b.tt_off = reinterpret_cast<int32_t *>(take((size_t)(E + 1) * 4));
+    b.xsc = reinterpret_cast<float *>(take((size_t)T * 4));
+    b.XG = reinterpret_cast<float *>(take((size_t)T * (D / 64) * 4));
+    b.X16 = reinterpret_cast<__half *>(take((size_t)T * D * 2));
+    b.Xr = reinterpret_cast<__half *>(take(TK * D * 2));
+    b.H = reinterpret_cast<__half *>(take(TK * I * 2));
+    b.Hs = reinterpret_cast<__half *>(take((size_t)T * S * 2));
+    b.Y = reinterpret_cast<float *>(take(TK * D * 4));
+    b.Ys = reinterpret_cast<float *>(take((size_t)T * D * 4));
+    b.total = (size_t)(p - w);
+    return b;
+}
+
+} // namespace
+
+size_t pf_workspace_bytes(int T, int D, int I, int S, int E, int K)
+{
+    return pf_carve(nullptr, T, D, I, S, E, K).total;
+}
+
+cudaError_t launch_prefill_prepare(const PfCall &c, PfPrepared *out, cudaStream_t s)
+{
+    const PfBufs b = pf_carve(c.ws, c.T, c.D, c.I, c.S, c.E, c.K);
+    const size_t gsm = (size_t)(c.D + 64 + c.D / 64) * 4;
+    cudaError_t e;
+    if (gsm > 48 * 1024) {
+        static std::mutex mu;
+        static size_t configured = 0;
+        std::lock_guard<std::mutex> g(mu);
+        if (gsm > configured) {
+            if ((e = cudaFuncSetAttribute(pf_norm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm)) !=
+                cudaSuccess)
+                return e;
+            configured = gsm;
+        }
+    }
+    pf_norm<<<c.T, 256, gsm, s>>>(static_cast<const uint16_t *>(c.x), c.D, c.pre_norm, c.eps, b.X16, b.xsc, b.XG);
+    out->X16 = b.X16;
+    out->xsc = b.xsc;
+    out->XG = b.XG;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const PfCall &c, cudaStream_t s)
+{
+    const int T = c.T, D = c.D, I = c.I, S = c.S, E = c.E, K = c.K, TK = T * K;
+    const PfBufs bf = pf_carve(c.ws, T, D, I, S, E, K);
+    int32_t *inv = bf.inv, *tt_off = bf.tt_off;
+    float *xsc = bf.xsc, *Y = bf.Y, *Ys = bf.Ys;
+    __half *X16 = bf.X16, *Xr = bf.Xr, *H = bf.H, *Hs = bf.Hs;
+
+    cudaError_t e;
+    pf_index<<<(TK + 255) / 256, 256, 0, s>>>(c.perm, TK, c.counts, E, inv, tt_off);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    pf_scatter<<<T, 256, 0, s>>>(X16, D, K, inv, Xr);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+
+    PfArgs a{};
+    a.T = T;
+    a.D = D;
+    a.I = I;
+    a.S = S;
+    a.E = E;
+    a.K = K;
+    a.tt_off = tt_off;
+    a.counts = c.counts;
+    a.offsets = c.offsets;
+    a.perm = c.perm;
+    a.xsc = xsc;
+    a.blob = c.blob;
+    a.stride = c.stride;
+    for (int j = 0; j < 3; ++j) {
+        a.off_s[j] = c.off_s[j];
+        a.off_b[j] = c.off_b[j];
+        a.ss[j] = c.ss[j];
+        a.sb[j] = c.sb[j];
+    }
+    a.H = H;
+    a.Hs = Hs;
+    a.Y = Y;
+    a.Ys = Ys;
+    a.err = c.err;
+    // gate/up: rows I (routed) / S (shared), K = D
+    a.mode = 0;
+    a.FT = (I + kMT - 1) / kMT;
+    a.FTs = (S + kMT - 1) / kMT;
+    a.KT = D / 64;
+    a.KTs = D / 64;
+    a.GK = D / 64;
+    a.GK_s = D / 64;
+    a.rows = I;
+    a.rows_s = S;
+    if ((e = encode_packed(&a.wa, c.blob + c.off_w[0], I, D, E, c.stride)) != cudaSuccess ||
+        (e = encode_packed(&a.wb, c.blob + c.off_w[1], I, D, E, c.stride)) != cudaSuccess ||
+        (e = encode_packed(&a.swa, c.sw[0], S, D, 1, 0)) != cudaSuccess ||
+        (e = encode_packed(&a.swb, c.sw[1], S, D, 1, 0)) != cudaSuccess ||
+        (e = encode_rows(&a.xr, Xr, TK, D)) != cudaSuccess || (e = encode_rows(&a.xs, X16, T, D)) != cudaSuccess)
+        return e;
+    prof_begin(kStageGateUp, s);
+    e = launch_gemm<0>(a, c.n_cta, s);
+    prof_end(kStageGateUp, s);
+    if (e != cudaSuccess)
+        return e;
+    // down: rows D, K = I (routed) / S (shared)
+    a.mode = 1;
+    a.FT = (D + kMT - 1) / kMT;
+    a.FTs = a.FT;
+    a.KT = I / 64;
+    a.KTs = S / 64;
+    a.GK = I / 64;
+    a.GK_s = S / 64;
+    a.rows = D;
+    a.rows_s = D;
+    if ((e = encode_packed(&a.wa, c.blob + c.off_w[2], D, I, E, c.stride)) != cudaSuccess ||
+        (e = encode_packed(&a.swa, c.sw[2], D, S, 1, 0)) != cudaSuccess ||
+        (e = encode_rows(&a.xr, H, TK, I)) != cudaSuccess || (e = encode_rows(&a.xs, Hs, T, S)) != cudaSuccess)
+        return e;
+    prof_begin(kStageDown, s);
+    e = launch_gemm<1>(a, c.n_cta, s);
+    if (e == cudaSuccess) {
+        pf_combine<<<dim3((D / 4 + 255) / 256, T), 256, 0, s>>>(Y, Ys, inv, c.topk_w, T, D, K, c.lam,
+                                                               static_cast<const uint16_t *>(c.residual),
+                                                               static_cast<uint16_t *>(c.out));
+        e = cudaGetLastError();
+    }
+    prof_end(kStageDown, s);
+    return e;
+}
+
+} // namespace mx

@@ -20,7 +20,10 @@
 #include "mx_cta_route.cuh"
 #include "mx_internal.h"
 
+#include <cuda_fp16.h>
+
 #include <climits>
+#include <mutex>
 
 namespace mx {
 
@@ -132,20 +135,21 @@ __device__ void topk_tokens(const RouteArgs &a, int t0, int nt, float *sm)
     }
 }
 
-// Group all T*K slots by expert, ascending slot id inside an expert.
-__device__ void group_slots(const RouteArgs &a, float *sm)
+// Group all T*K slots by expert, ascending slot id inside an expert; NW warps.
+template <int NW>
+__device__ void group_slots_nw(const RouteArgs &a, float *sm)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = a.E, n = a.T * a.K;
-    int *wc = reinterpret_cast<int *>(sm);   // [kWarps][E] per-warp counts
-    int *base = wc + kWarps * E;             // [kWarps][E] per-warp running bases
-    int *cnt = base + kWarps * E;            // [E]
+    int *wc = reinterpret_cast<int *>(sm);   // [NW][E] per-warp counts
+    int *base = wc + NW * E;             // [NW][E] per-warp running bases
+    int *cnt = base + NW * E;            // [E]
     int *off = cnt + E;                      // [E]
     int *tix = off + E;                      // [E] first tile slot of each expert
-    for (int i = threadIdx.x; i < kWarps * E; i += kThreads)
+    for (int i = threadIdx.x; i < NW * E; i += (32 * NW))
         wc[i] = 0;
     __syncthreads();
-    const int chunk = (n + kWarps - 1) / kWarps;
+    const int chunk = (n + NW - 1) / NW;
     const int lo = min(n, warp * chunk), hi = min(n, lo + chunk);
     for (int s0 = lo; s0 < hi; s0 += 32) {
         const int s = s0 + lane;
@@ -156,9 +160,9 @@ __device__ void group_slots(const RouteArgs &a, float *sm)
         __syncwarp();
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kThreads) {
+    for (int e = threadIdx.x; e < E; e += (32 * NW)) {
         int run = 0;
-        for (int w = 0; w < kWarps; ++w) {
+        for (int w = 0; w < NW; ++w) {
             base[w * E + e] = run;
             run += wc[w * E + e];
         }
@@ -212,7 +216,7 @@ __device__ void group_slots(const RouteArgs &a, float *sm)
         __syncwarp();
     }
     if (a.tiles) {
-        for (int e = threadIdx.x; e < E; e += kThreads) {
+        for (int e = threadIdx.x; e < E; e += (32 * NW)) {
             int t = tix[e];
             for (int b = 0; b < cnt[e]; b += kTileTokens, ++t) {
                 a.tiles[3 * t + 0] = e;
@@ -222,6 +226,8 @@ __device__ void group_slots(const RouteArgs &a, float *sm)
         }
     }
 }
+
+__device__ void group_slots(const RouteArgs &a, float *sm) { group_slots_nw<kWarps>(a, sm); }
 
 struct RouteSync {
     __device__ void operator()() const { __syncthreads(); }
@@ -530,6 +536,159 @@ cudaError_t launch_tt(const RouteArgs &a, const RouteLaunch &L, cudaStream_t s)
     return cudaLaunchKernelEx(&cfg, k, a, L);
 }
 
+// ---------------------------------------------------------------- large T
+//
+// For many tokens the logits are a batched product: a register-tiled kernel
+// computes a 64-token x 64-expert block, one group of 64 columns at a time.
+// Every (token, expert) accumulator still follows the fixed order of the
+// header -- within a group an fma chain over the 64 columns in ascending
+// order, then acc = fma(s, P, acc), acc = fma(b, X, acc), groups ascending --
+// so the logits equal the small-T kernel's bit for bit.  The activations come
+// from the prefill gather: FP16 rows scaled by a power of two per token (exact
+// for the BF16 values), in operand column order, and their per-group sums in
+// the fixed add order.
+
+constexpr int kLE = 64;  // experts per block
+
+// Block of TT tokens x 64 experts; TT/4 x 16 threads, 4 x 4 accumulators each.
+// The next group's activations and router bytes are loaded into registers
+// while the current group is multiplied.
+template <int TT>
+__global__ void __launch_bounds__(TT * 4) logits_gemm(const __half *__restrict__ X16, const float *__restrict__ xsc,
+                                                       const float *__restrict__ XG, const uint32_t *__restrict__ rw,
+                                                       const uint16_t *__restrict__ rs, const uint16_t *__restrict__ rb,
+                                                       int T, int D, int E, float *__restrict__ logits)
+{
+    constexpr int NT = TT * 4;               // threads
+    constexpr int XV = TT * 8 / NT;          // 16-byte activation vectors per thread per group (= 2)
+    constexpr int QV = kLE * 4 / NT;         // 16-byte router vectors per thread per group
+    static_assert(XV * NT == TT * 8 && QV * NT == kLE * 4, "tile shape");
+    __shared__ __align__(16) float xs[64][TT];   // [column][token]
+    __shared__ __align__(16) float qs[64][kLE];  // [column][expert]
+    __shared__ float sS[kLE], sB[kLE], sX[TT];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int t0 = blockIdx.y * TT, e0 = blockIdx.x * kLE, G = D / 64;
+    uint4 xr[XV], qr[QV];
+    float xscale[XV];
+    auto fetch = [&](int g) {
+#pragma unroll
+        for (int v = 0; v < XV; ++v) {
+            const int i = tid + v * NT, t = i >> 3, ch = i & 7, tt = t0 + t;
+            xr[v] = tt < T ? __ldg(reinterpret_cast<const uint4 *>(X16 + (size_t)tt * D + 64 * g) + ch)
+                           : make_uint4(0, 0, 0, 0);
+            xscale[v] = tt < T ? __ldg(xsc + tt) : 0.f;
+        }
+#pragma unroll
+        for (int v = 0; v < QV; ++v) {
+            const int i = tid + v * NT, e = i >> 2, w4 = i & 3, ee = e0 + e;
+            qr[v] = ee < E ? __ldg(reinterpret_cast<const uint4 *>(rw + (size_t)ee * (D / 4) + 16 * g) + w4)
+                           : make_uint4(0, 0, 0, 0);
+        }
+    };
+    float acc[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            acc[i][j] = 0.f;
+    fetch(0);
+    for (int g = 0; g < G; ++g) {
+        // registers -> shared: activations back in column order (operand
+        // position p of an 8-block holds column [0,4,1,5,2,6,3,7][p]), router
+        // bytes as floats
+#pragma unroll
+        for (int v = 0; v < XV; ++v) {
+            const int i = tid + v * NT, t = i >> 3, ch = i & 7;
+            const uint32_t u[4] = {xr[v].x, xr[v].y, xr[v].z, xr[v].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const __half2 h = *reinterpret_cast<const __half2 *>(&u[j]);
+                const float2 f = __half22float2(h);
+                xs[8 * ch + j][t] = f.x * xscale[v];      // operand position 2j   -> column j
+                xs[8 * ch + j + 4][t] = f.y * xscale[v];  // operand position 2j+1 -> column j+4
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < QV; ++v) {
+            const int i = tid + v * NT, e = i >> 2, w4 = i & 3;
+            const uint32_t u[4] = {qr[v].x, qr[v].y, qr[v].z, qr[v].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = 16 * w4 + 4 * j;
+                qs[c][e] = (float)(u[j] & 0xFFu);
+                qs[c + 1][e] = (float)((u[j] >> 8) & 0xFFu);
+                qs[c + 2][e] = (float)((u[j] >> 16) & 0xFFu);
+                qs[c + 3][e] = (float)(u[j] >> 24);
+            }
+        }
+        if (tid < kLE) {
+            const int ee = e0 + tid;
+            sS[tid] = ee < E ? bf2f(__ldg(rs + (size_t)ee * G + g)) : 0.f;
+            sB[tid] = ee < E ? bf2f(__ldg(rb + (size_t)ee * G + g)) : 0.f;
+        }
+        if (tid < TT) {
+            const int tt = t0 + tid;
+            sX[tid] = tt < T ? __ldg(XG + (size_t)tt * G + g) : 0.f;
+        }
+        __syncthreads();
+        if (g + 1 < G)
+            fetch(g + 1);
+        float P[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                P[i][j] = 0.f;
+#pragma unroll 8
+        for (int c = 0; c < 64; ++c) {
+            const float4 xv = *reinterpret_cast<const float4 *>(&xs[c][4 * ty]);
+            const float4 qv = *reinterpret_cast<const float4 *>(&qs[c][4 * tx]);
+            const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, qa[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    P[i][j] = fmaf(qa[j], xa[i], P[i][j]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                acc[i][j] = fmaf(sS[4 * tx + j], P[i][j], acc[i][j]);
+                acc[i][j] = fmaf(sB[4 * tx + j], sX[4 * ty + i], acc[i][j]);
+            }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int tt = t0 + 4 * ty + i;
+        if (tt >= T)
+            continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int ee = e0 + 4 * tx + j;
+            if (ee < E)
+                logits[(size_t)tt * E + ee] = acc[i][j];
+        }
+    }
+}
+
+// Top-k + softmax of 8 tokens per block (one warp per token), from the logits.
+__global__ void __launch_bounds__(kThreads) topk_kernel(const RouteArgs a)
+{
+    extern __shared__ __align__(16) float sm[];
+    const int t0 = blockIdx.x * kWarps;
+    topk_tokens(a, t0, min(kWarps, a.T - t0), sm);
+}
+
+// Grouping of all slots by expert, one block of 32 warps.
+constexpr int kGroupWarps = 32;
+__global__ void __launch_bounds__(32 * kGroupWarps) group_kernel(const RouteArgs a)
+{
+    extern __shared__ __align__(16) float sm[];
+    group_slots_nw<kGroupWarps>(a, sm);
+}
+
 } // namespace
 
 RouteLaunch route_plan(int T, int D, int E, int K)
@@ -599,6 +758,40 @@ cudaError_t launch_route(const RouteArgs &a, const RouteLaunch &L, cudaStream_t 
     case 8: return launch_tt<8>(a, L, s);
     default: return launch_tt<32>(a, L, s);
     }
+}
+
+cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float *xsc, const float *XG, cudaStream_t s)
+{
+    // 64-token blocks when they fill the GPU twice over, else 32-token blocks
+    const int ne = (a.E + kLE - 1) / kLE;
+    if ((long long)ne * ((a.T + 63) / 64) >= 2 * 152) {
+        logits_gemm<64><<<dim3(ne, (a.T + 63) / 64), 256, 0, s>>>(static_cast<const __half *>(X16), xsc, XG, a.rw,
+                                                                    a.rs, a.rb, a.T, a.D, a.E, a.logits);
+    } else {
+        logits_gemm<32><<<dim3(ne, (a.T + 31) / 32), 128, 0, s>>>(static_cast<const __half *>(X16), xsc, XG, a.rw,
+                                                                    a.rs, a.rb, a.T, a.D, a.E, a.logits);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const size_t topk_smem = ((size_t)kWarps * a.E + (size_t)kWarps * ((a.E + 31) / 32)) * sizeof(float);
+    topk_kernel<<<(a.T + kWarps - 1) / kWarps, kThreads, topk_smem, s>>>(a);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    const size_t group_smem = (2 * (size_t)kGroupWarps * a.E + 3 * (size_t)a.E) * sizeof(float);
+    {
+        static std::mutex mu;
+        static size_t configured = 0;
+        std::lock_guard<std::mutex> g(mu);
+        if (group_smem > 48 * 1024 && group_smem > configured) {
+            if ((e = cudaFuncSetAttribute(group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)group_smem)) != cudaSuccess)
+                return e;
+            configured = group_smem;
+        }
+    }
+    group_kernel<<<1, 32 * kGroupWarps, group_smem, s>>>(a);
+    return cudaGetLastError();
 }
 
 } // namespace mx

@@ -284,3 +284,51 @@ def test_decode_stack_paths_agree(orc, gu, monkeypatch):
         assert np.array_equal(idx.cpu().numpy(), idx_ref), single
         assert rel_l2(w.cpu().numpy(), w_ref) <= 5e-3
         check_out(gu.to_host(xd, np.uint16), xs_ref[-1], "bf16")
+
+
+# --------------------------------------------- prefill: tensor-core GEMMs
+
+PREFILL_SHAPES = [
+    # T, D, E, K, I, S
+    (65, 256, 16, 4, 128, 64),       # one past the decode range
+    (200, 320, 8, 3, 192, 320),      # D, I, S not multiples of 128; T ragged; experts with >128 slots
+    (300, 512, 4, 2, 704, 128),      # few experts: several token tiles each
+    (129, 1024, 64, 8, 256, 384),
+]
+
+
+@pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=[f"T{s[0]}_D{s[1]}_E{s[2]}_K{s[3]}_I{s[4]}_S{s[5]}"
+                                                       for s in PREFILL_SHAPES])
+def test_prefill_gemm_shapes(orc, gu, shape, monkeypatch):
+    """BF16 inputs with T > 64 run the grouped tensor-core GEMMs (stage
+    profiler: one routing launch, the GEMM sequence under gate/up); against
+    the oracle, and against the decode kernels on the same inputs."""
+    import expert_ffn_gb300 as mx
+    T, D, E, K, I, S = shape
+    cfg = synth.small_config(T=T, D=D, E=E, K=K, I=I, S=S, act="bf16", seed=T + 7 * D)
+    layer = synth.make_layer(cfg)
+    x = synth.make_x(cfg)
+    mx.profile_enable(True)
+    try:
+        mx.profile_read(reset=True)
+        dev, out, idx, w = check_block(orc, gu, cfg, layer, x)
+        prof = mx.profile_read(reset=True)
+    finally:
+        mx.profile_enable(False)
+    assert prof["route"][1] == 1 and prof["gate_up"][1] == 1 and prof["down"][1] == 1, prof
+    monkeypatch.setenv("MX_MOE_PREFILL_GEMM", "0")
+    out2, idx2, w2 = gu.run_block(dev, x)
+    assert np.array_equal(idx, idx2)
+    check_out(out, out2, "bf16")
+
+
+def test_prefill_residual_and_prenorm(orc, gu):
+    cfg = synth.small_config(T=96, D=512, E=16, K=4, I=256, S=128, act="bf16", seed=31)
+    layer = synth.make_layer(cfg)
+    x = synth.make_x(cfg)
+    dev = __import__("expert_ffn_gb300").DeviceLayer(layer, gu.act_code(cfg))
+    out, idx, w = gu.run_block(dev, x, residual=x, pre_norm=True, eps=1e-6)
+    xn = orc.rmsnorm_bf16(x, 1e-6)
+    ref, ridx, rw = orc.block_forward(layer, xn, residual=x)
+    assert np.array_equal(idx, ridx)
+    check_out(out, ref, "bf16")
