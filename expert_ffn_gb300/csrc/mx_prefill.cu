@@ -48,9 +48,15 @@ namespace {
 
 constexpr int kMT = 128;  // weight rows per tile (MMA M)
 constexpr int kNT = 128;  // tokens per tile (MMA N, at most)
-constexpr int kDqWarps = 8;  // dequantizing warps (2..9)
-constexpr int kWarps = 2 + kDqWarps + 4, kThreads = kWarps * 32;
-constexpr int kEpiWarp0 = 2 + kDqWarps;  // first epilogue warp
+// Warp roles.  A warp runs on scheduler (warp % 4); the MMA warp (1) shares
+// its scheduler only with an epilogue warp, so the dequantizing warps' ALU
+// stream does not stretch its issue chain.  Warps 9 and 13 have no role.
+constexpr int kDqWarps = 8;
+constexpr int kWarps = 16, kThreads = kWarps * 32;
+constexpr uint32_t kDqMask = (1u << 2) | (1u << 3) | (1u << 8) | (1u << 10) | (1u << 11) | (1u << 12) | (1u << 14) |
+                             (1u << 15);
+constexpr int kEpiWarp0 = 4;  // epilogue warps 4..7: TMEM lane quadrant = warp % 4
+static_assert(__builtin_popcount(kDqMask) == kDqWarps, "dequantizing warps");
 // Ring depths per kernel (gate/up holds two weight matrices per stage):
 // packed weights + operand tile, and dequantized FP16 weight tiles.  The FP16
 // ring is what lets the dequantizing warps run ahead of the MMAs.
@@ -85,6 +91,14 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+
+// One lane of the (converged) warp: true in exactly one lane.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(pred));
+    return pred != 0;
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -264,15 +278,19 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        int kp = 0;
-        if (lane == 0) {
-            bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-                const Unit U = unit_of(a, u, nR);
-                for (int kt = 0; kt < U.kt_n; ++kt, ++kp) {
-                    const int sp = kp % kNP;
-                    if (kp >= kNP && !(ok = bwait(&p_empty[sp], ((kp / kNP) - 1) & 1, a.err, abort)))
+        // the whole warp walks the loop; one elected lane issues the copies
+        int kp = 0, sp = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const Unit U = unit_of(a, u, nR);
+            for (int kt = 0; kt < U.kt_n; ++kt) {
+                if (kp >= kNP) {
+                    ok = __all_sync(0xffffffffu, bwait(&p_empty[sp], ph ^ 1u, a.err, abort));
+                    if (!ok)
                         break;
+                }
+                if (elect_one()) {
                     mbar_arrive_expect_tx(&p_full[sp], kBTile + NMAT * kPacked);
                     tma_2d(bring + sp * kBTile, U.shared ? &a.xs : &a.xr, 64 * kt, U.slot0, &p_full[sp]);
                     uint8_t *pk = pring + sp * NMAT * kPacked;
@@ -286,61 +304,87 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                             tma_4d(pk + kPacked, &a.wb, 0, U.row0, kt, U.e, &p_full[sp]);
                     }
                 }
+                __syncwarp();
+                ++kp;
+                if (++sp == kNP) {
+                    sp = 0;
+                    ph ^= 1u;
+                }
             }
-            // leave no copy in flight (plain bounded waits: copies complete on their own)
+        }
+        // leave no copy in flight (plain bounded waits: copies complete on their own)
+        if (elect_one())
             for (int k = (kp > kNP ? kp - kNP : 0); k < kp; ++k)
                 mbar_wait(&p_full[k % kNP], (k / kNP) & 1, a.err);
-        }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA
-        if (lane == 0) {
-            int kp = 0, kf = 0, ai = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ai) {
-                const Unit U = unit_of(a, u, nR);
-                const int b = ai & 1;
-                if (ai >= 2 && !(ok = bwait(&acc_empty[b], ((ai / 2) - 1) & 1, a.err, abort)))
+        // The whole warp walks the loop (its control and the descriptors stay
+        // warp-uniform); one elected lane issues the MMAs and commits.
+        int sp = 0, sf = 0, ai = 0;
+        uint32_t php = 0, phf = 0;
+        bool ok = true;
+        const uint32_t bring_s = smem_u32(bring), fring_s = smem_u32(fring);
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ai) {
+            const Unit U = unit_of(a, u, nR);
+            const int b = ai & 1;
+            if (ai >= 2) {
+                ok = __all_sync(0xffffffffu, bwait(&acc_empty[b], ((ai >> 1) - 1) & 1, a.err, abort));
+                if (!ok)
+                    break;
+            }
+            tc_fence_after();
+            const uint32_t idesc = idesc_f16(max(16, (U.n + 15) & ~15));
+            const uint32_t d0 = tmem + (uint32_t)(b * (kCols / 2));
+            for (int kt = 0; kt < U.kt_n; ++kt) {
+                ok = __all_sync(0xffffffffu, bwait(&f_full[sf], phf, a.err, abort) &&
+                                                 bwait(&p_full[sp], php, a.err, abort));
+                if (!ok)
                     break;
                 tc_fence_after();
-                const int nm = max(16, (U.n + 15) & ~15);
-                const uint32_t idesc = idesc_f16(nm);
-                const uint32_t d0 = tmem + (uint32_t)(b * (kCols / 2));
-                for (int kt = 0; kt < U.kt_n; ++kt, ++kp, ++kf) {
-                    const int sp = kp % kNP, sf = kf % kNF;
-                    if (!(ok = bwait(&f_full[sf], (kf / kNF) & 1, a.err, abort) &&
-                               bwait(&p_full[sp], (kp / kNP) & 1, a.err, abort)))
-                        break;
-                    tc_fence_after();
-                    const uint32_t bb = smem_u32(bring + sp * kBTile);
-                    const uint32_t fa = smem_u32(fring + sf * NMAT * kFTile);
+                if (elect_one()) {
+                    // descriptors of the stage; +2 per 16-element K step (32 bytes)
+                    const uint64_t bd = sw128_desc(bring_s + (uint32_t)(sp * kBTile));
+                    const uint64_t ad = sw128_desc(fring_s + (uint32_t)(sf * NMAT * kFTile));
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
-                        const uint64_t bd = sw128_desc(bb + 32 * ks);
                         const uint32_t acc = (kt | ks) ? 1u : 0u;
-                        umma(d0, sw128_desc(fa + 32 * ks), bd, idesc, acc);
+                        umma(d0, ad + 2 * ks, bd + 2 * ks, idesc, acc);
                         if (NMAT == 2)
-                            umma(d0 + 128, sw128_desc(fa + kFTile + 32 * ks), bd, idesc, acc);
+                            umma(d0 + 128, ad + (kFTile >> 4) + 2 * ks, bd + 2 * ks, idesc, acc);
                     }
                     umma_commit(&f_empty[sf]);
                     umma_commit(&p_empty[sp]);
                 }
-                if (ok)
-                    umma_commit(&acc_full[b]);
+                __syncwarp();
+                if (++sf == kNF) {
+                    sf = 0;
+                    phf ^= 1u;
+                }
+                if (++sp == kNP) {
+                    sp = 0;
+                    php ^= 1u;
+                }
             }
-            // every MMA this thread issued has completed before TMEM is freed
+            if (ok && elect_one())
+                umma_commit(&acc_full[b]);
+            __syncwarp();
+        }
+        // every MMA this warp issued has completed before TMEM is freed
+        if (elect_one()) {
             umma_commit(mma_done);
             mbar_wait(mma_done, 0, a.err);
         }
         __syncwarp();
-    } else if (warp < kEpiWarp0) {
+    } else if ((kDqMask >> warp) & 1u) {
         // ------------------------------------------------------ dequantize
         // 256 threads, two per weight row: gate/up -> one matrix each; down ->
         // four of the row's eight words each
-        const int r2 = tid - 64, r = r2 & (kMT - 1), half = r2 >> 7;
+        const int r2 = __popc(kDqMask & ((1u << warp) - 1u)) * 32 + lane, r = r2 & (kMT - 1), half = r2 >> 7;
         const int m = MODE == 0 ? half : 0;                 // matrix of this thread
         const int w0 = MODE == 0 ? 0 : 4 * half, nw = MODE == 0 ? 8 : 4;
-        int kp = 0, kf = 0;
+        int sp = 0, sf = 0, kf = 0;
+        uint32_t php = 0, phf = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit U = unit_of(a, u, nR);
@@ -374,14 +418,12 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 const int kt = kt4 + jj;
                 if (kt >= U.kt_n)
                     break;
-                const int sp = kp % kNP, sf = kf % kNF;
                 const __half2 s2 = __float2half2_rn(bf2f(s_r[jj])), b2 = __float2half2_rn(bf2f(b_r[jj]));
                 if (valid && kt + kLook < U.kt_n) {
                     s_r[jj] = __ldg(sv + kt + kLook);
                     b_r[jj] = __ldg(bv + kt + kLook);
                 }
-                ok = bwait(&p_full[sp], (kp / kNP) & 1, a.err, abort) &&
-                     (kf < kNF || bwait(&f_empty[sf], ((kf / kNF) - 1) & 1, a.err, abort));
+                ok = bwait(&p_full[sp], php, a.err, abort) && (kf < kNF || bwait(&f_empty[sf], phf ^ 1u, a.err, abort));
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
@@ -408,11 +450,18 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                     mbar_arrive(&f_full[sf]);
                     mbar_arrive(&p_empty[sp]);
                 }
-                ++kp;
                 ++kf;
+                if (++sf == kNF) {
+                    sf = 0;
+                    phf ^= 1u;
+                }
+                if (++sp == kNP) {
+                    sp = 0;
+                    php ^= 1u;
+                }
             }
         }
-    } else {
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // -------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quadrant of this warp
         int ai = 0;
@@ -440,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                         const int p = U.slot0 + c0 + lane;
                         my_sc = __ldg(a.xsc + (U.shared ? p : __ldg(a.perm + p) / a.K));
                     }
-#pragma unroll 4
+#pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int col = c0 + j;
                         const float sc = __shfl_sync(0xffffffffu, my_sc, j);
@@ -454,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                     }
                 } else {
                     float *Y = U.shared ? a.Ys : a.Y;
-#pragma unroll 4
+#pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int col = c0 + j;
                         if (col < U.n && valid)
