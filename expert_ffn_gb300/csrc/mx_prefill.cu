@@ -48,21 +48,22 @@ namespace {
 
 constexpr int kMT = 128;  // weight rows per tile (MMA M)
 constexpr int kNT = 128;  // tokens per tile (MMA N, at most)
-// Warp roles.  A warp runs on scheduler (warp % 4); the MMA warp (1) shares
-// its scheduler only with an epilogue warp, so the dequantizing warps' ALU
-// stream does not stretch its issue chain.  Warps 9 and 13 have no role.
+// Warp roles.  A warp runs on scheduler (warp % 4): each scheduler gets two
+// dequantizing warps (8..15), one epilogue warp (4..7, TMEM lane quadrant =
+// warp % 4) and one of: the weight producer (0), the MMA warp (1), the
+// activation producer (2), nothing (3).
 constexpr int kDqWarps = 8;
 constexpr int kWarps = 16, kThreads = kWarps * 32;
-constexpr uint32_t kDqMask = (1u << 2) | (1u << 3) | (1u << 8) | (1u << 10) | (1u << 11) | (1u << 12) | (1u << 14) |
-                             (1u << 15);
-constexpr int kEpiWarp0 = 4;  // epilogue warps 4..7: TMEM lane quadrant = warp % 4
+constexpr uint32_t kDqMask = 0xFF00u;
+constexpr int kEpiWarp0 = 4;
+constexpr int kBWarp = 2;
 static_assert(__builtin_popcount(kDqMask) == kDqWarps, "dequantizing warps");
 // Ring depths per kernel (gate/up holds two weight matrices per stage):
 // packed weights + operand tile, and dequantized FP16 weight tiles.  The FP16
 // ring is what lets the dequantizing warps run ahead of the MMAs.
 template <int MODE> struct Depth;
-template <> struct Depth<0> { static constexpr int NP = 5, NF = 3; };
-template <> struct Depth<1> { static constexpr int NP = 6, NF = 4; };
+template <> struct Depth<0> { static constexpr int NP = 9, NF = 3; };
+template <> struct Depth<1> { static constexpr int NP = 16, NF = 5; };
 constexpr int kBTile = kNT * 128;  // bytes of one operand tile (128 tokens x 64 FP16)
 constexpr int kFTile = kMT * 128;  // bytes of one FP16 weight tile (128 rows x 64)
 
@@ -198,20 +199,24 @@ __device__ __forceinline__ bool bwait(uint64_t *bar, uint32_t parity, unsigned *
     return true;
 }
 
-// Nibbles j and j+4 of w as exact FP16 integers (1024 + q) - 1024.
-template <int J>
-__device__ __forceinline__ __half2 nib_h2(uint32_t w)
+// The nibbles at bit offsets O and O+16 of v as exact FP16 integers.  A
+// nibble in mantissa bits 0-3 under exponent 2^10 reads 1024 + q; one in
+// mantissa bits 4-7 under exponent 2^6 reads 64 + q (no shift needed).
+template <int O>
+__device__ __forceinline__ __half2 nib_h2(uint32_t v)
 {
-    const uint32_t v = ((w >> (4 * J)) & 0x000F000Fu) | 0x64006400u;
-    return __hsub2(*reinterpret_cast<const __half2 *>(&v), __float2half2_rn(1024.0f));
+    constexpr uint32_t mask = 0x000F000Fu << (O & 4), magic = (O & 4) ? 0x54005400u : 0x64006400u;
+    const uint32_t t = (v & mask) | magic;
+    return __hsub2(*reinterpret_cast<const __half2 *>(&t), __float2half2_rn((O & 4) ? 64.0f : 1024.0f));
 }
 
 // One packed word (8 weights of a row) -> 8 FP16 weights in operand order
 // [0,4,1,5,2,6,3,7], w = s*q + b with one rounding.
 __device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 s2, __half2 b2)
 {
-    const __half2 p0 = __hfma2(nib_h2<0>(w), s2, b2), p1 = __hfma2(nib_h2<1>(w), s2, b2);
-    const __half2 p2 = __hfma2(nib_h2<2>(w), s2, b2), p3 = __hfma2(nib_h2<3>(w), s2, b2);
+    const uint32_t w8 = w >> 8;
+    const __half2 p0 = __hfma2(nib_h2<0>(w), s2, b2), p1 = __hfma2(nib_h2<4>(w), s2, b2);
+    const __half2 p2 = __hfma2(nib_h2<0>(w8), s2, b2), p3 = __hfma2(nib_h2<4>(w8), s2, b2);
     return make_uint4(*reinterpret_cast<const uint32_t *>(&p0), *reinterpret_cast<const uint32_t *>(&p1),
                       *reinterpret_cast<const uint32_t *>(&p2), *reinterpret_cast<const uint32_t *>(&p3));
 }
@@ -232,11 +237,11 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
     constexpr int NMAT = MODE == 0 ? 2 : 1;
     constexpr int kNP = Depth<MODE>::NP, kNF = Depth<MODE>::NF;
     constexpr uint32_t kPacked = 128 * 32;  // packed bytes of one matrix tile (128 rows x 64 columns)
+    constexpr uint32_t kStage = NMAT * kFTile + kBTile;  // FP16 weight tiles, then the activation tile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *fring = sm;                                   // kNF x NMAT x kFTile
-    uint8_t *bring = fring + kNF * NMAT * kFTile;          // kNP x kBTile
-    uint8_t *pring = bring + kNP * kBTile;                 // kNP x NMAT x kPacked
+    uint8_t *fring = sm;                                   // kNF x kStage
+    uint8_t *pring = fring + kNF * kStage;                 // kNP x NMAT x kPacked
     uint64_t *bars = reinterpret_cast<uint64_t *>(pring + kNP * NMAT * kPacked);
     uint64_t *p_full = bars, *p_empty = bars + kNP, *f_full = bars + 2 * kNP, *f_empty = f_full + kNF;
     uint64_t *acc_full = f_empty + kNF, *acc_empty = acc_full + 2;
@@ -249,10 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
     if (tid == 0) {
         for (int i = 0; i < kNP; ++i) {
             mbar_init(&p_full[i], 1);
-            mbar_init(&p_empty[i], kDqWarps + 1);  // the dequantizing warps + the MMA commit
+            mbar_init(&p_empty[i], kDqWarps);
         }
         for (int i = 0; i < kNF; ++i) {
-            mbar_init(&f_full[i], kDqWarps);
+            mbar_init(&f_full[i], kDqWarps + 1);  // the dequantizing warps + the activation copy
             mbar_init(&f_empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -276,55 +281,73 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
     const int nR = __ldg(a.tt_off + a.E);
     const int n_units = nR * a.FT + ((a.T + kNT - 1) / kNT) * a.FTs;
 
-    if (warp == 0) {
-        // ---------------------------------------------------------- producer
-        // the whole warp walks the loop; one elected lane issues the copies
+    if (warp == 0 || warp == kBWarp) {
+        // ---------------------------------------------------------- producers
+        // warp 0: packed weight tiles into the packed ring (deep: released by
+        // the dequantizing warps); warp kBWarp: activation tiles into the
+        // stage the MMA reads (released by the MMA).  The whole warp walks the
+        // loop; one elected lane issues the copies.
+        const bool wts = warp == 0;
+        const int depth = wts ? kNP : kNF;
+        uint64_t *full = wts ? p_full : f_full, *empty = wts ? p_empty : f_empty;
         int kp = 0, sp = 0;
         uint32_t ph = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit U = unit_of(a, u, nR);
             for (int kt = 0; kt < U.kt_n; ++kt) {
-                if (kp >= kNP) {
-                    ok = __all_sync(0xffffffffu, bwait(&p_empty[sp], ph ^ 1u, a.err, abort));
+                if (kp >= depth) {
+                    ok = __all_sync(0xffffffffu, bwait(&empty[sp], ph ^ 1u, a.err, abort));
                     if (!ok)
                         break;
                 }
                 if (elect_one()) {
-                    mbar_arrive_expect_tx(&p_full[sp], kBTile + NMAT * kPacked);
-                    tma_2d(bring + sp * kBTile, U.shared ? &a.xs : &a.xr, 64 * kt, U.slot0, &p_full[sp]);
-                    uint8_t *pk = pring + sp * NMAT * kPacked;
-                    if (U.shared) {
-                        tma_4d(pk, &a.swa, 0, U.row0, kt, 0, &p_full[sp]);
-                        if (NMAT == 2)
-                            tma_4d(pk + kPacked, &a.swb, 0, U.row0, kt, 0, &p_full[sp]);
+                    if (wts) {
+                        mbar_arrive_expect_tx(&full[sp], NMAT * kPacked);
+                        uint8_t *pk = pring + sp * NMAT * kPacked;
+                        if (U.shared) {
+                            tma_4d(pk, &a.swa, 0, U.row0, kt, 0, &full[sp]);
+                            if (NMAT == 2)
+                                tma_4d(pk + kPacked, &a.swb, 0, U.row0, kt, 0, &full[sp]);
+                        } else {
+                            tma_4d(pk, &a.wa, 0, U.row0, kt, U.e, &full[sp]);
+                            if (NMAT == 2)
+                                tma_4d(pk + kPacked, &a.wb, 0, U.row0, kt, U.e, &full[sp]);
+                        }
                     } else {
-                        tma_4d(pk, &a.wa, 0, U.row0, kt, U.e, &p_full[sp]);
-                        if (NMAT == 2)
-                            tma_4d(pk + kPacked, &a.wb, 0, U.row0, kt, U.e, &p_full[sp]);
+                        mbar_arrive_expect_tx(&full[sp], kBTile);
+                        tma_2d(fring + sp * kStage + NMAT * kFTile, U.shared ? &a.xs : &a.xr, 64 * kt, U.slot0,
+                               &full[sp]);
                     }
                 }
                 __syncwarp();
                 ++kp;
-                if (++sp == kNP) {
+                if (++sp == depth) {
                     sp = 0;
                     ph ^= 1u;
                 }
             }
         }
-        // leave no copy in flight (plain bounded waits: copies complete on their own)
-        if (elect_one())
-            for (int k = (kp > kNP ? kp - kNP : 0); k < kp; ++k)
-                mbar_wait(&p_full[k % kNP], (k / kNP) & 1, a.err);
+        // Leave no copy in flight.  The packed ring's phases complete with the
+        // copies; a stage's phase completes once its copy and the dequantizing
+        // warps are done, so after a failure this gives up at one time limit
+        // in all.
+        if (elect_one()) {
+            const unsigned long long t0 = global_ns();
+            for (int k = (kp > depth ? kp - depth : 0); k < kp; ++k)
+                while (!mbar_try_wait(&full[k % depth], (k / depth) & 1))
+                    if (global_ns() - t0 > kWaitLimitNs)
+                        break;
+        }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA
         // The whole warp walks the loop (its control and the descriptors stay
         // warp-uniform); one elected lane issues the MMAs and commits.
-        int sp = 0, sf = 0, ai = 0;
-        uint32_t php = 0, phf = 0;
+        int sf = 0, ai = 0;
+        uint32_t phf = 0;
         bool ok = true;
-        const uint32_t bring_s = smem_u32(bring), fring_s = smem_u32(fring);
+        const uint32_t fring_s = smem_u32(fring);
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ai) {
             const Unit U = unit_of(a, u, nR);
             const int b = ai & 1;
@@ -337,15 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
             const uint32_t idesc = idesc_f16(max(16, (U.n + 15) & ~15));
             const uint32_t d0 = tmem + (uint32_t)(b * (kCols / 2));
             for (int kt = 0; kt < U.kt_n; ++kt) {
-                ok = __all_sync(0xffffffffu, bwait(&f_full[sf], phf, a.err, abort) &&
-                                                 bwait(&p_full[sp], php, a.err, abort));
+                ok = __all_sync(0xffffffffu, bwait(&f_full[sf], phf, a.err, abort));
                 if (!ok)
                     break;
                 tc_fence_after();
                 if (elect_one()) {
                     // descriptors of the stage; +2 per 16-element K step (32 bytes)
-                    const uint64_t bd = sw128_desc(bring_s + (uint32_t)(sp * kBTile));
-                    const uint64_t ad = sw128_desc(fring_s + (uint32_t)(sf * NMAT * kFTile));
+                    const uint32_t st = fring_s + (uint32_t)(sf * kStage);
+                    const uint64_t ad = sw128_desc(st), bd = sw128_desc(st + NMAT * kFTile);
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t acc = (kt | ks) ? 1u : 0u;
@@ -354,16 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                             umma(d0 + 128, ad + (kFTile >> 4) + 2 * ks, bd + 2 * ks, idesc, acc);
                     }
                     umma_commit(&f_empty[sf]);
-                    umma_commit(&p_empty[sp]);
                 }
                 __syncwarp();
                 if (++sf == kNF) {
                     sf = 0;
                     phf ^= 1u;
-                }
-                if (++sp == kNP) {
-                    sp = 0;
-                    php ^= 1u;
                 }
             }
             if (ok && elect_one())
@@ -382,8 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
         // four of the row's eight words each
         const int r2 = __popc(kDqMask & ((1u << warp) - 1u)) * 32 + lane, r = r2 & (kMT - 1), half = r2 >> 7;
         const int m = MODE == 0 ? half : 0;                 // matrix of this thread
-        const int w0 = MODE == 0 ? 0 : 4 * half, nw = MODE == 0 ? 8 : 4;
+        const int w0 = MODE == 0 ? 0 : 4 * half;
+        constexpr int nw = MODE == 0 ? 8 : 4;  // packed words of this thread per K tile
         int sp = 0, sf = 0, kf = 0;
+        int pend = -1;  // stage whose stores are not yet fenced and published
         uint32_t php = 0, phf = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -429,27 +448,37 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                     break;
                 }
                 const uint32_t *src = reinterpret_cast<const uint32_t *>(pring + (sp * NMAT + m) * kPacked + r * 32);
-                uint8_t *dst = fring + (sf * NMAT + m) * kFTile + r * 128;
+                uint8_t *dst = fring + sf * kStage + m * kFTile + r * 128;
+                // dequantize into registers, release the packed stage, then store
+                uint4 o[nw];
                 if (MODE == 0) {
                     const uint4 q0 = reinterpret_cast<const uint4 *>(src)[0], q1 = reinterpret_cast<const uint4 *>(src)[1];
                     const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        *reinterpret_cast<uint4 *>(dst + ((w ^ (r & 7)) << 4)) = dequant_word(wv[w], s2, b2);
+                    for (int w = 0; w < nw; ++w)
+                        o[w] = dequant_word(wv[w], s2, b2);
                 } else {
                     const uint4 q = reinterpret_cast<const uint4 *>(src)[half];
                     const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                    for (int w = 0; w < 4; ++w)
-                        *reinterpret_cast<uint4 *>(dst + (((w0 + w) ^ (r & 7)) << 4)) = dequant_word(wv[w], s2, b2);
+                    for (int w = 0; w < nw; ++w)
+                        o[w] = dequant_word(wv[w], s2, b2);
                 }
-                (void)nw;
-                fence_async_smem();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&f_full[sf]);
+                if (lane == 0)
                     mbar_arrive(&p_empty[sp]);
+                // publish the previous tile now: its stores drained behind
+                // this tile's waits, loads and arithmetic
+                if (pend >= 0) {
+                    fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&f_full[pend]);
                 }
+#pragma unroll
+                for (int w = 0; w < nw; ++w)
+                    *reinterpret_cast<uint4 *>(dst + (((w0 + w) ^ (r & 7)) << 4)) = o[w];
+                pend = sf;
                 ++kf;
                 if (++sf == kNF) {
                     sf = 0;
@@ -460,6 +489,12 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                     php ^= 1u;
                 }
             }
+        }
+        if (ok && pend >= 0) {
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&f_full[pend]);
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // -------------------------------------------------------- epilogue
@@ -723,7 +758,7 @@ template <int MODE>
 size_t gemm_smem()
 {
     const int nmat = MODE == 0 ? 2 : 1, np = Depth<MODE>::NP, nf = Depth<MODE>::NF;
-    return 1024 + (size_t)nf * nmat * kFTile + (size_t)np * kBTile + (size_t)np * nmat * 128 * 32 + 256;
+    return 1024 + (size_t)nf * (nmat * kFTile + kBTile) + (size_t)np * nmat * 128 * 32 + 512;
 }
 
 template <int MODE>
