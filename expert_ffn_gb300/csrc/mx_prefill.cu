@@ -58,14 +58,17 @@ constexpr uint32_t kDqMask = 0xFF00u;
 constexpr int kEpiWarp0 = 4;
 constexpr int kBWarp = 2;
 static_assert(__builtin_popcount(kDqMask) == kDqWarps, "dequantizing warps");
-// Ring depths per kernel (gate/up holds two weight matrices per stage):
-// packed weights + operand tile, and dequantized FP16 weight tiles.  The FP16
-// ring is what lets the dequantizing warps run ahead of the MMAs.
-template <int MODE> struct Depth;
-template <> struct Depth<0> { static constexpr int NP = 9, NF = 3; };
-template <> struct Depth<1> { static constexpr int NP = 16, NF = 5; };
+// TMEM (512 columns): accumulators in columns [0, kACols), the FP16 weight
+// slots of the stages above.  Gate/up needs 256 columns per accumulator (gate
+// and up side by side), so it keeps one accumulator and four 64-K weight
+// slots; down double-buffers its 128-column accumulator and has eight slots.
+// A stage = one TMEM weight slot + one activation tile in shared memory; the
+// packed ring (shared memory) runs ahead of the stages.
+constexpr uint32_t kTmemCols = 512, kACols = 256;
+template <int MODE> struct Cfg;
+template <> struct Cfg<0> { static constexpr int NMAT = 2, NACC = 1, NS = 4, NP = 16; };
+template <> struct Cfg<1> { static constexpr int NMAT = 1, NACC = 2, NS = 8, NP = 16; };
 constexpr int kBTile = kNT * 128;  // bytes of one operand tile (128 tokens x 64 FP16)
-constexpr int kFTile = kMT * 128;  // bytes of one FP16 weight tile (128 rows x 64)
 
 // ------------------------------------------------------------- tcgen05 glue
 
@@ -85,6 +88,15 @@ __device__ __forceinline__ void umma(uint32_t dtm, uint64_t ad, uint64_t bd, uin
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtm),
                  "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T
+__device__ __forceinline__ void umma_ts(uint32_t dtm, uint32_t atm, uint64_t bd, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(dtm),
+                 "r"(atm), "l"(bd), "r"(idesc), "r"(acc)
                  : "memory");
 }
 
@@ -118,6 +130,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32])
                  : "r"(ta));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+// This warp's 32 TMEM lanes, NW*4 consecutive columns from ta: lane i writes
+// r[0..NW*4) of thread i.
+template <int NW>
+__device__ __forceinline__ void tmem_st(uint32_t ta, const uint32_t (&r)[4 * NW]);
+
+template <>
+__device__ __forceinline__ void tmem_st<8>(uint32_t ta, const uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+                 "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+                 "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+
+template <>
+__device__ __forceinline__ void tmem_st<4>(uint32_t ta, const uint32_t (&r)[16])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(ta),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+                 "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
 {
@@ -211,14 +251,17 @@ __device__ __forceinline__ __half2 nib_h2(uint32_t v)
 }
 
 // One packed word (8 weights of a row) -> 8 FP16 weights in operand order
-// [0,4,1,5,2,6,3,7], w = s*q + b with one rounding.
-__device__ __forceinline__ uint4 dequant_word(uint32_t w, __half2 s2, __half2 b2)
+// [0,4,1,5,2,6,3,7] (four half2 words, low half first), w = s*q + b with one
+// rounding.
+__device__ __forceinline__ void dequant_word(uint32_t w, __half2 s2, __half2 b2, uint32_t *out)
 {
     const uint32_t w8 = w >> 8;
     const __half2 p0 = __hfma2(nib_h2<0>(w), s2, b2), p1 = __hfma2(nib_h2<4>(w), s2, b2);
     const __half2 p2 = __hfma2(nib_h2<0>(w8), s2, b2), p3 = __hfma2(nib_h2<4>(w8), s2, b2);
-    return make_uint4(*reinterpret_cast<const uint32_t *>(&p0), *reinterpret_cast<const uint32_t *>(&p1),
-                      *reinterpret_cast<const uint32_t *>(&p2), *reinterpret_cast<const uint32_t *>(&p3));
+    out[0] = *reinterpret_cast<const uint32_t *>(&p0);
+    out[1] = *reinterpret_cast<const uint32_t *>(&p1);
+    out[2] = *reinterpret_cast<const uint32_t *>(&p2);
+    out[3] = *reinterpret_cast<const uint32_t *>(&p3);
 }
 
 // Position of column c in the operand order [0,4,1,5,2,6,3,7] of its 8-block.
@@ -234,33 +277,33 @@ __device__ __forceinline__ int opos(int c)
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ PfArgs a)
 {
-    constexpr int NMAT = MODE == 0 ? 2 : 1;
-    constexpr int kNP = Depth<MODE>::NP, kNF = Depth<MODE>::NF;
-    constexpr uint32_t kPacked = 128 * 32;  // packed bytes of one matrix tile (128 rows x 64 columns)
-    constexpr uint32_t kStage = NMAT * kFTile + kBTile;  // FP16 weight tiles, then the activation tile
+    constexpr int NMAT = Cfg<MODE>::NMAT, NACC = Cfg<MODE>::NACC, kNS = Cfg<MODE>::NS, kNP = Cfg<MODE>::NP;
+    constexpr uint32_t kPacked = 128 * 32;      // packed bytes of one matrix tile (128 rows x 64 columns)
+    constexpr uint32_t kAccCols = NMAT * kNT;   // TMEM columns of one accumulator buffer
+    constexpr uint32_t kSlotCols = NMAT * 32;   // TMEM columns of one FP16 weight slot (64 K per matrix)
+    static_assert(NACC * kAccCols == kACols && kNS * kSlotCols == kTmemCols - kACols, "TMEM split");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *fring = sm;                                   // kNF x kStage
-    uint8_t *pring = fring + kNF * kStage;                 // kNP x NMAT x kPacked
+    uint8_t *bring = sm;                                   // kNS x kBTile
+    uint8_t *pring = bring + kNS * kBTile;                 // kNP x NMAT x kPacked
     uint64_t *bars = reinterpret_cast<uint64_t *>(pring + kNP * NMAT * kPacked);
-    uint64_t *p_full = bars, *p_empty = bars + kNP, *f_full = bars + 2 * kNP, *f_empty = f_full + kNF;
-    uint64_t *acc_full = f_empty + kNF, *acc_empty = acc_full + 2;
-    uint64_t *mma_done = acc_empty + 2;
+    uint64_t *p_full = bars, *p_empty = bars + kNP, *s_full = bars + 2 * kNP, *s_empty = s_full + kNS;
+    uint64_t *acc_full = s_empty + kNS, *acc_empty = acc_full + NACC;
+    uint64_t *mma_done = acc_empty + NACC;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    constexpr int kCols = MODE == 0 ? 512 : 256;  // two accumulator buffers
 
     if (tid == 0) {
         for (int i = 0; i < kNP; ++i) {
             mbar_init(&p_full[i], 1);
             mbar_init(&p_empty[i], kDqWarps);
         }
-        for (int i = 0; i < kNF; ++i) {
-            mbar_init(&f_full[i], kDqWarps + 1);  // the dequantizing warps + the activation copy
-            mbar_init(&f_empty[i], 1);
+        for (int i = 0; i < kNS; ++i) {
+            mbar_init(&s_full[i], kDqWarps + 1);  // the dequantizing warps + the activation copy
+            mbar_init(&s_empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NACC; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], 4);
         }
@@ -270,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tslot)),
-                     "r"(kCols)
+                     "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -288,8 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
         // stage the MMA reads (released by the MMA).  The whole warp walks the
         // loop; one elected lane issues the copies.
         const bool wts = warp == 0;
-        const int depth = wts ? kNP : kNF;
-        uint64_t *full = wts ? p_full : f_full, *empty = wts ? p_empty : f_empty;
+        const int depth = wts ? kNP : kNS;
+        uint64_t *full = wts ? p_full : s_full, *empty = wts ? p_empty : s_empty;
         int kp = 0, sp = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -316,8 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                         }
                     } else {
                         mbar_arrive_expect_tx(&full[sp], kBTile);
-                        tma_2d(fring + sp * kStage + NMAT * kFTile, U.shared ? &a.xs : &a.xr, 64 * kt, U.slot0,
-                               &full[sp]);
+                        tma_2d(bring + sp * kBTile, U.shared ? &a.xs : &a.xr, 64 * kt, U.slot0, &full[sp]);
                     }
                 }
                 __syncwarp();
@@ -343,44 +385,45 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA
         // The whole warp walks the loop (its control and the descriptors stay
-        // warp-uniform); one elected lane issues the MMAs and commits.
-        int sf = 0, ai = 0;
-        uint32_t phf = 0;
+        // warp-uniform); one elected lane issues the MMAs and commits.  A (the
+        // FP16 weights) comes from TMEM, B (the activations) from shared memory.
+        int ss = 0, ai = 0;
+        uint32_t phs = 0;
         bool ok = true;
-        const uint32_t fring_s = smem_u32(fring);
+        const uint32_t bring_s = smem_u32(bring);
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ai) {
             const Unit U = unit_of(a, u, nR);
-            const int b = ai & 1;
-            if (ai >= 2) {
-                ok = __all_sync(0xffffffffu, bwait(&acc_empty[b], ((ai >> 1) - 1) & 1, a.err, abort));
+            const int b = NACC == 1 ? 0 : (ai & 1);
+            if (ai >= NACC) {
+                ok = __all_sync(0xffffffffu, bwait(&acc_empty[b], ((ai / NACC) - 1) & 1, a.err, abort));
                 if (!ok)
                     break;
             }
             tc_fence_after();
             const uint32_t idesc = idesc_f16(max(16, (U.n + 15) & ~15));
-            const uint32_t d0 = tmem + (uint32_t)(b * (kCols / 2));
+            const uint32_t d0 = tmem + (uint32_t)b * kAccCols;
             for (int kt = 0; kt < U.kt_n; ++kt) {
-                ok = __all_sync(0xffffffffu, bwait(&f_full[sf], phf, a.err, abort));
+                ok = __all_sync(0xffffffffu, bwait(&s_full[ss], phs, a.err, abort));
                 if (!ok)
                     break;
                 tc_fence_after();
                 if (elect_one()) {
-                    // descriptors of the stage; +2 per 16-element K step (32 bytes)
-                    const uint32_t st = fring_s + (uint32_t)(sf * kStage);
-                    const uint64_t ad = sw128_desc(st), bd = sw128_desc(st + NMAT * kFTile);
+                    // +2 per 16-element K step in the B descriptor (32 bytes), +8 TMEM columns in A
+                    const uint64_t bd = sw128_desc(bring_s + (uint32_t)(ss * kBTile));
+                    const uint32_t at = tmem + kACols + (uint32_t)ss * kSlotCols;
 #pragma unroll
                     for (int ks = 0; ks < 4; ++ks) {
                         const uint32_t acc = (kt | ks) ? 1u : 0u;
-                        umma(d0, ad + 2 * ks, bd + 2 * ks, idesc, acc);
+                        umma_ts(d0, at + 8 * ks, bd + 2 * ks, idesc, acc);
                         if (NMAT == 2)
-                            umma(d0 + 128, ad + (kFTile >> 4) + 2 * ks, bd + 2 * ks, idesc, acc);
+                            umma_ts(d0 + kNT, at + 32 + 8 * ks, bd + 2 * ks, idesc, acc);
                     }
-                    umma_commit(&f_empty[sf]);
+                    umma_commit(&s_empty[ss]);
                 }
                 __syncwarp();
-                if (++sf == kNF) {
-                    sf = 0;
-                    phf ^= 1u;
+                if (++ss == kNS) {
+                    ss = 0;
+                    phs ^= 1u;
                 }
             }
             if (ok && elect_one())
@@ -395,15 +438,18 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
         __syncwarp();
     } else if ((kDqMask >> warp) & 1u) {
         // ------------------------------------------------------ dequantize
-        // 256 threads, two per weight row: gate/up -> one matrix each; down ->
-        // four of the row's eight words each
-        const int r2 = __popc(kDqMask & ((1u << warp) - 1u)) * 32 + lane, r = r2 & (kMT - 1), half = r2 >> 7;
-        const int m = MODE == 0 ? half : 0;                 // matrix of this thread
-        const int w0 = MODE == 0 ? 0 : 4 * half;
+        // Thread = (weight row r = its TMEM lane, part).  Gate/up: part =
+        // matrix, all eight words of the row's K tile; down: part = half of
+        // the row's eight words.  The FP16 weights go to the stage's TMEM slot
+        // with one tcgen05.st per thread.
+        const int q = warp & 3, part = (warp - 8) >> 2, r = 32 * q + lane;
+        const int m = MODE == 0 ? part : 0;
+        const int w0 = MODE == 0 ? 0 : 4 * part;
         constexpr int nw = MODE == 0 ? 8 : 4;  // packed words of this thread per K tile
-        int sp = 0, sf = 0, kf = 0;
-        int pend = -1;  // stage whose stores are not yet fenced and published
-        uint32_t php = 0, phf = 0;
+        const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + kACols + (uint32_t)(m * 32 + 4 * w0);
+        int sp = 0, ss = 0, kf = 0;
+        int pend = -1;  // slot whose stores are not yet waited for and published
+        uint32_t php = 0, phs = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit U = unit_of(a, u, nR);
@@ -422,8 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 bv = reinterpret_cast<const uint16_t *>(rec + a.off_b[j]) + (size_t)row * G;
             }
             // the row's scale and bias of group kt, loaded kLook K tiles ahead
-            // into a register ring (the shared-memory carve-out leaves L1 too
-            // small to keep them)
+            // into a register ring
             constexpr int kLook = 4;
             uint16_t s_r[kLook], b_r[kLook];
 #pragma unroll
@@ -442,47 +487,46 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                     s_r[jj] = __ldg(sv + kt + kLook);
                     b_r[jj] = __ldg(bv + kt + kLook);
                 }
-                ok = bwait(&p_full[sp], php, a.err, abort) && (kf < kNF || bwait(&f_empty[sf], phf ^ 1u, a.err, abort));
+                ok = bwait(&p_full[sp], php, a.err, abort) && (kf < kNS || bwait(&s_empty[ss], phs ^ 1u, a.err, abort));
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
-                const uint32_t *src = reinterpret_cast<const uint32_t *>(pring + (sp * NMAT + m) * kPacked + r * 32);
-                uint8_t *dst = fring + sf * kStage + m * kFTile + r * 128;
-                // dequantize into registers, release the packed stage, then store
-                uint4 o[nw];
+                tc_fence_after();
+                const uint4 *src = reinterpret_cast<const uint4 *>(pring + (sp * NMAT + m) * kPacked + r * 32);
+                // dequantize into registers, release the packed stage
+                uint32_t o[4 * nw];
                 if (MODE == 0) {
-                    const uint4 q0 = reinterpret_cast<const uint4 *>(src)[0], q1 = reinterpret_cast<const uint4 *>(src)[1];
+                    const uint4 q0 = src[0], q1 = src[1];
                     const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
                     for (int w = 0; w < nw; ++w)
-                        o[w] = dequant_word(wv[w], s2, b2);
+                        dequant_word(wv[w], s2, b2, o + 4 * w);
                 } else {
-                    const uint4 q = reinterpret_cast<const uint4 *>(src)[half];
-                    const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+                    const uint4 qq = src[part];
+                    const uint32_t wv[4] = {qq.x, qq.y, qq.z, qq.w};
 #pragma unroll
                     for (int w = 0; w < nw; ++w)
-                        o[w] = dequant_word(wv[w], s2, b2);
+                        dequant_word(wv[w], s2, b2, o + 4 * w);
                 }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&p_empty[sp]);
-                // publish the previous tile now: its stores drained behind
-                // this tile's waits, loads and arithmetic
+                // publish the previous slot now: its TMEM stores drained
+                // behind this tile's waits, loads and arithmetic
                 if (pend >= 0) {
-                    fence_async_smem();
+                    tmem_st_wait();
+                    tc_fence_before();
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(&f_full[pend]);
+                        mbar_arrive(&s_full[pend]);
                 }
-#pragma unroll
-                for (int w = 0; w < nw; ++w)
-                    *reinterpret_cast<uint4 *>(dst + (((w0 + w) ^ (r & 7)) << 4)) = o[w];
-                pend = sf;
+                tmem_st<nw>(tl + (uint32_t)ss * kSlotCols, o);
+                pend = ss;
                 ++kf;
-                if (++sf == kNF) {
-                    sf = 0;
-                    phf ^= 1u;
+                if (++ss == kNS) {
+                    ss = 0;
+                    phs ^= 1u;
                 }
                 if (++sp == kNP) {
                     sp = 0;
@@ -490,11 +534,12 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 }
             }
         }
+        tmem_st_wait();
         if (ok && pend >= 0) {
-            fence_async_smem();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&f_full[pend]);
+                mbar_arrive(&s_full[pend]);
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // -------------------------------------------------------- epilogue
@@ -502,20 +547,20 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
         int ai = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++ai) {
             const Unit U = unit_of(a, u, nR);
-            const int b = ai & 1;
-            if (!__all_sync(0xffffffffu, bwait(&acc_full[b], (ai / 2) & 1, a.err, abort)))
+            const int b = NACC == 1 ? 0 : (ai & 1);
+            if (!__all_sync(0xffffffffu, bwait(&acc_full[b], (ai / NACC) & 1, a.err, abort)))
                 break;
             tc_fence_after();
             const int rows = U.shared ? a.rows_s : a.rows;
             const int row = U.row0 + 32 * q + lane;
             const bool valid = row < rows;
-            const uint32_t d0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(b * (kCols / 2));
+            const uint32_t d0 = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)b * kAccCols;
             for (int c0 = 0; c0 < U.n; c0 += 32) {
                 uint32_t g[32];
                 tmem_ld32(d0 + c0, g);
                 if (MODE == 0) {
                     uint32_t v[32];
-                    tmem_ld32(d0 + 128 + c0, v);
+                    tmem_ld32(d0 + kNT + c0, v);
                     __half *H = static_cast<__half *>(U.shared ? a.Hs : a.H);
                     const int ld = U.shared ? a.S : a.I;
                     // lane j fetches the token scale of column c0 + j once
@@ -555,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
     tc_fence_before();
     __syncthreads();
     if (warp == 1)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
 }
 
 // -------------------------------------------------------------- small kernels
@@ -757,8 +802,7 @@ cudaError_t encode_packed(CUtensorMap *m, const void *base, int rows, int cols, 
 template <int MODE>
 size_t gemm_smem()
 {
-    const int nmat = MODE == 0 ? 2 : 1, np = Depth<MODE>::NP, nf = Depth<MODE>::NF;
-    return 1024 + (size_t)nf * (nmat * kFTile + kBTile) + (size_t)np * nmat * 128 * 32 + 512;
+    return 1024 + (size_t)Cfg<MODE>::NS * kBTile + (size_t)Cfg<MODE>::NP * Cfg<MODE>::NMAT * 128 * 32 + 512;
 }
 
 template <int MODE>
