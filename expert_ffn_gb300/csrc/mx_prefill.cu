@@ -58,16 +58,17 @@ constexpr uint32_t kDqMask = 0xFF00u;
 constexpr int kEpiWarp0 = 4;
 constexpr int kBWarp = 2;
 static_assert(__builtin_popcount(kDqMask) == kDqWarps, "dequantizing warps");
-// TMEM (512 columns): accumulators in columns [0, kACols), the FP16 weight
-// slots of the stages above.  Gate/up needs 256 columns per accumulator (gate
-// and up side by side), so it keeps one accumulator and four 64-K weight
-// slots; down double-buffers its 128-column accumulator and has eight slots.
-// A stage = one TMEM weight slot + one activation tile in shared memory; the
-// packed ring (shared memory) runs ahead of the stages.
+// A stage covers AT 64-K atoms.  TMEM (512 columns): accumulators in
+// columns [0, kACols), the FP16 weight slots (one per stage) above.  Gate/up
+// needs 256 columns per accumulator (gate and up side by side), so it keeps
+// one accumulator and four one-atom weight slots; down double-buffers its
+// 128-column accumulator and has four two-atom slots.  The activation ring
+// (NB stages) and the packed ring (NP stages) live in shared memory; the
+// packed ring runs ahead.
 constexpr uint32_t kTmemCols = 512, kACols = 256;
 template <int MODE> struct Cfg;
-template <> struct Cfg<0> { static constexpr int NMAT = 2, NACC = 1, NS = 4, NP = 16; };
-template <> struct Cfg<1> { static constexpr int NMAT = 1, NACC = 2, NS = 8, NP = 16; };
+template <> struct Cfg<0> { static constexpr int NMAT = 2, NACC = 1, AT = 1, NA = 4, NB = 8, NP = 8; };
+template <> struct Cfg<1> { static constexpr int NMAT = 1, NACC = 2, AT = 2, NA = 4, NB = 4, NP = 8; };
 constexpr int kBTile = kNT * 128;  // bytes of one operand tile (128 tokens x 64 FP16)
 
 // ------------------------------------------------------------- tcgen05 glue
@@ -277,18 +278,22 @@ __device__ __forceinline__ int opos(int c)
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ PfArgs a)
 {
-    constexpr int NMAT = Cfg<MODE>::NMAT, NACC = Cfg<MODE>::NACC, kNS = Cfg<MODE>::NS, kNP = Cfg<MODE>::NP;
-    constexpr uint32_t kPacked = 128 * 32;      // packed bytes of one matrix tile (128 rows x 64 columns)
-    constexpr uint32_t kAccCols = NMAT * kNT;   // TMEM columns of one accumulator buffer
-    constexpr uint32_t kSlotCols = NMAT * 32;   // TMEM columns of one FP16 weight slot (64 K per matrix)
-    static_assert(NACC * kAccCols == kACols && kNS * kSlotCols == kTmemCols - kACols, "TMEM split");
+    constexpr int NMAT = Cfg<MODE>::NMAT, NACC = Cfg<MODE>::NACC;
+    constexpr int kNA = Cfg<MODE>::NA, kNB = Cfg<MODE>::NB, kNP = Cfg<MODE>::NP, kAt = Cfg<MODE>::AT;
+    constexpr uint32_t kPacked = 128 * 32;               // packed bytes of one matrix atom (128 rows x 64 K)
+    constexpr uint32_t kPStage = kAt * NMAT * kPacked;   // packed bytes of one stage
+    constexpr uint32_t kBStage = kAt * kBTile;           // activation bytes of one stage
+    constexpr uint32_t kAccCols = NMAT * kNT;            // TMEM columns of one accumulator buffer
+    constexpr uint32_t kSlotCols = kAt * NMAT * 32;      // TMEM columns of one FP16 weight slot
+    static_assert(NACC * kAccCols == kACols && kNA * kSlotCols == kTmemCols - kACols, "TMEM split");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *bring = sm;                                   // kNS x kBTile
-    uint8_t *pring = bring + kNS * kBTile;                 // kNP x NMAT x kPacked
-    uint64_t *bars = reinterpret_cast<uint64_t *>(pring + kNP * NMAT * kPacked);
-    uint64_t *p_full = bars, *p_empty = bars + kNP, *s_full = bars + 2 * kNP, *s_empty = s_full + kNS;
-    uint64_t *acc_full = s_empty + kNS, *acc_empty = acc_full + NACC;
+    uint8_t *bring = sm;                      // kNB x kBStage
+    uint8_t *pring = bring + kNB * kBStage;   // kNP x kPStage
+    uint64_t *bars = reinterpret_cast<uint64_t *>(pring + kNP * kPStage);
+    uint64_t *p_full = bars, *p_empty = p_full + kNP, *b_full = p_empty + kNP, *b_empty = b_full + kNB;
+    uint64_t *a_full = b_empty + kNB, *a_empty = a_full + kNA;
+    uint64_t *acc_full = a_empty + kNA, *acc_empty = acc_full + NACC;
     uint64_t *mma_done = acc_empty + NACC;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
@@ -299,9 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
             mbar_init(&p_full[i], 1);
             mbar_init(&p_empty[i], kDqWarps);
         }
-        for (int i = 0; i < kNS; ++i) {
-            mbar_init(&s_full[i], kDqWarps + 1);  // the dequantizing warps + the activation copy
-            mbar_init(&s_empty[i], 1);
+        for (int i = 0; i < kNB; ++i) {
+            mbar_init(&b_full[i], 1);
+            mbar_init(&b_empty[i], 1);
+        }
+        for (int i = 0; i < kNA; ++i) {
+            mbar_init(&a_full[i], kDqWarps);
+            mbar_init(&a_empty[i], 1);
         }
         for (int i = 0; i < NACC; ++i) {
             mbar_init(&acc_full[i], 1);
@@ -326,19 +335,20 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
 
     if (warp == 0 || warp == kBWarp) {
         // ---------------------------------------------------------- producers
-        // warp 0: packed weight tiles into the packed ring (deep: released by
-        // the dequantizing warps); warp kBWarp: activation tiles into the
-        // stage the MMA reads (released by the MMA).  The whole warp walks the
-        // loop; one elected lane issues the copies.
+        // warp 0: packed weight atoms (released by the dequantizing warps);
+        // warp kBWarp: activation atoms (released by the MMA).  A stage holds
+        // two 64-K atoms (one at the end of an odd K).  The whole warp walks
+        // the loop; one elected lane issues the copies.
         const bool wts = warp == 0;
-        const int depth = wts ? kNP : kNS;
-        uint64_t *full = wts ? p_full : s_full, *empty = wts ? p_empty : s_empty;
+        const int depth = wts ? kNP : kNB;
+        uint64_t *full = wts ? p_full : b_full, *empty = wts ? p_empty : b_empty;
         int kp = 0, sp = 0;
         uint32_t ph = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit U = unit_of(a, u, nR);
-            for (int kt = 0; kt < U.kt_n; ++kt) {
+            for (int kt0 = 0; kt0 < U.kt_n; kt0 += kAt) {
+                const int nat = min(kAt, U.kt_n - kt0);
                 if (kp >= depth) {
                     ok = __all_sync(0xffffffffu, bwait(&empty[sp], ph ^ 1u, a.err, abort));
                     if (!ok)
@@ -346,20 +356,19 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 }
                 if (elect_one()) {
                     if (wts) {
-                        mbar_arrive_expect_tx(&full[sp], NMAT * kPacked);
-                        uint8_t *pk = pring + sp * NMAT * kPacked;
-                        if (U.shared) {
-                            tma_4d(pk, &a.swa, 0, U.row0, kt, 0, &full[sp]);
-                            if (NMAT == 2)
-                                tma_4d(pk + kPacked, &a.swb, 0, U.row0, kt, 0, &full[sp]);
-                        } else {
-                            tma_4d(pk, &a.wa, 0, U.row0, kt, U.e, &full[sp]);
-                            if (NMAT == 2)
-                                tma_4d(pk + kPacked, &a.wb, 0, U.row0, kt, U.e, &full[sp]);
-                        }
+                        mbar_arrive_expect_tx(&full[sp], nat * NMAT * kPacked);
+                        uint8_t *pk = pring + sp * kPStage;
+                        for (int at = 0; at < nat; ++at)
+                            for (int m = 0; m < NMAT; ++m) {
+                                const CUtensorMap *map = U.shared ? (m ? &a.swb : &a.swa) : (m ? &a.wb : &a.wa);
+                                tma_4d(pk + (at * NMAT + m) * kPacked, map, 0, U.row0, kt0 + at, U.shared ? 0 : U.e,
+                                       &full[sp]);
+                            }
                     } else {
-                        mbar_arrive_expect_tx(&full[sp], kBTile);
-                        tma_2d(bring + sp * kBTile, U.shared ? &a.xs : &a.xr, 64 * kt, U.slot0, &full[sp]);
+                        mbar_arrive_expect_tx(&full[sp], nat * kBTile);
+                        for (int at = 0; at < nat; ++at)
+                            tma_2d(bring + sp * kBStage + at * kBTile, U.shared ? &a.xs : &a.xr, 64 * (kt0 + at),
+                                   U.slot0, &full[sp]);
                     }
                 }
                 __syncwarp();
@@ -370,10 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 }
             }
         }
-        // Leave no copy in flight.  The packed ring's phases complete with the
-        // copies; a stage's phase completes once its copy and the dequantizing
-        // warps are done, so after a failure this gives up at one time limit
-        // in all.
+        // leave no copy in flight (the phases complete with the copies)
         if (elect_one()) {
             const unsigned long long t0 = global_ns();
             for (int k = (kp > depth ? kp - depth : 0); k < kp; ++k)
@@ -387,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
         // The whole warp walks the loop (its control and the descriptors stay
         // warp-uniform); one elected lane issues the MMAs and commits.  A (the
         // FP16 weights) comes from TMEM, B (the activations) from shared memory.
-        int ss = 0, ai = 0;
-        uint32_t phs = 0;
+        int sa = 0, sb = 0, ai = 0;
+        uint32_t pha = 0, phb = 0;
         bool ok = true;
         const uint32_t bring_s = smem_u32(bring);
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ai) {
@@ -402,28 +408,38 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
             tc_fence_after();
             const uint32_t idesc = idesc_f16(max(16, (U.n + 15) & ~15));
             const uint32_t d0 = tmem + (uint32_t)b * kAccCols;
-            for (int kt = 0; kt < U.kt_n; ++kt) {
-                ok = __all_sync(0xffffffffu, bwait(&s_full[ss], phs, a.err, abort));
+            for (int kt0 = 0; kt0 < U.kt_n; kt0 += kAt) {
+                const int nat = min(kAt, U.kt_n - kt0);
+                ok = __all_sync(0xffffffffu, bwait(&a_full[sa], pha, a.err, abort) &&
+                                                 bwait(&b_full[sb], phb, a.err, abort));
                 if (!ok)
                     break;
                 tc_fence_after();
                 if (elect_one()) {
                     // +2 per 16-element K step in the B descriptor (32 bytes), +8 TMEM columns in A
-                    const uint64_t bd = sw128_desc(bring_s + (uint32_t)(ss * kBTile));
-                    const uint32_t at = tmem + kACols + (uint32_t)ss * kSlotCols;
+                    const uint64_t bd0 = sw128_desc(bring_s + (uint32_t)(sb * kBStage));
+                    const uint32_t at0 = tmem + kACols + (uint32_t)sa * kSlotCols;
+                    for (int at = 0; at < nat; ++at) {
+                        const uint64_t bd = bd0 + (uint64_t)(at * (kBTile >> 4));
 #pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        const uint32_t acc = (kt | ks) ? 1u : 0u;
-                        umma_ts(d0, at + 8 * ks, bd + 2 * ks, idesc, acc);
-                        if (NMAT == 2)
-                            umma_ts(d0 + kNT, at + 32 + 8 * ks, bd + 2 * ks, idesc, acc);
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint32_t acc = (kt0 | at | ks) ? 1u : 0u;
+#pragma unroll
+                            for (int m = 0; m < NMAT; ++m)
+                                umma_ts(d0 + m * kNT, at0 + (at * NMAT + m) * 32 + 8 * ks, bd + 2 * ks, idesc, acc);
+                        }
                     }
-                    umma_commit(&s_empty[ss]);
+                    umma_commit(&a_empty[sa]);
+                    umma_commit(&b_empty[sb]);
                 }
                 __syncwarp();
-                if (++ss == kNS) {
-                    ss = 0;
-                    phs ^= 1u;
+                if (++sa == kNA) {
+                    sa = 0;
+                    pha ^= 1u;
+                }
+                if (++sb == kNB) {
+                    sb = 0;
+                    phb ^= 1u;
                 }
             }
             if (ok && elect_one())
@@ -439,17 +455,17 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
     } else if ((kDqMask >> warp) & 1u) {
         // ------------------------------------------------------ dequantize
         // Thread = (weight row r = its TMEM lane, part).  Gate/up: part =
-        // matrix, all eight words of the row's K tile; down: part = half of
-        // the row's eight words.  The FP16 weights go to the stage's TMEM slot
-        // with one tcgen05.st per thread.
+        // matrix, all eight words of the row's atom; down: part = half of the
+        // row's eight words.  The FP16 weights of an atom go to the slot with
+        // one tcgen05.st per thread.
         const int q = warp & 3, part = (warp - 8) >> 2, r = 32 * q + lane;
         const int m = MODE == 0 ? part : 0;
         const int w0 = MODE == 0 ? 0 : 4 * part;
-        constexpr int nw = MODE == 0 ? 8 : 4;  // packed words of this thread per K tile
+        constexpr int nw = MODE == 0 ? 8 : 4;  // packed words of this thread per atom
         const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16) + kACols + (uint32_t)(m * 32 + 4 * w0);
-        int sp = 0, ss = 0, kf = 0;
+        int sp = 0, sa = 0, kf = 0;
         int pend = -1;  // slot whose stores are not yet waited for and published
-        uint32_t php = 0, phs = 0;
+        uint32_t php = 0, pha = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             const Unit U = unit_of(a, u, nR);
@@ -467,66 +483,73 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 sv = reinterpret_cast<const uint16_t *>(rec + a.off_s[j]) + (size_t)row * G;
                 bv = reinterpret_cast<const uint16_t *>(rec + a.off_b[j]) + (size_t)row * G;
             }
-            // the row's scale and bias of group kt, loaded kLook K tiles ahead
-            // into a register ring
-            constexpr int kLook = 4;
-            uint16_t s_r[kLook], b_r[kLook];
+            // scale and bias of the row's groups, one stage ahead in registers
+            uint32_t s_nx[kAt], b_nx[kAt];
 #pragma unroll
-            for (int j = 0; j < kLook; ++j) {
-                s_r[j] = (valid && j < U.kt_n) ? __ldg(sv + j) : (uint16_t)0;
-                b_r[j] = (valid && j < U.kt_n) ? __ldg(bv + j) : (uint16_t)0;
+            for (int at = 0; at < kAt; ++at) {
+                s_nx[at] = (valid && at < U.kt_n) ? __ldg(sv + at) : 0u;
+                b_nx[at] = (valid && at < U.kt_n) ? __ldg(bv + at) : 0u;
             }
-            for (int kt4 = 0; kt4 < U.kt_n && ok; kt4 += kLook)
+            for (int kt0 = 0; kt0 < U.kt_n; kt0 += kAt) {
+                const int nat = min(kAt, U.kt_n - kt0);
+                __half2 s2[kAt], b2[kAt];
 #pragma unroll
-            for (int jj = 0; jj < kLook; ++jj) {
-                const int kt = kt4 + jj;
-                if (kt >= U.kt_n)
-                    break;
-                const __half2 s2 = __float2half2_rn(bf2f(s_r[jj])), b2 = __float2half2_rn(bf2f(b_r[jj]));
-                if (valid && kt + kLook < U.kt_n) {
-                    s_r[jj] = __ldg(sv + kt + kLook);
-                    b_r[jj] = __ldg(bv + kt + kLook);
+                for (int at = 0; at < kAt; ++at) {
+                    s2[at] = __float2half2_rn(bf2f((uint16_t)s_nx[at]));
+                    b2[at] = __float2half2_rn(bf2f((uint16_t)b_nx[at]));
+                    const int kn = kt0 + kAt + at;
+                    s_nx[at] = (valid && kn < U.kt_n) ? __ldg(sv + kn) : 0u;
+                    b_nx[at] = (valid && kn < U.kt_n) ? __ldg(bv + kn) : 0u;
                 }
-                ok = bwait(&p_full[sp], php, a.err, abort) && (kf < kNS || bwait(&s_empty[ss], phs ^ 1u, a.err, abort));
+                ok = bwait(&p_full[sp], php, a.err, abort) && (kf < kNA || bwait(&a_empty[sa], pha ^ 1u, a.err, abort));
                 if (!__all_sync(0xffffffffu, ok)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint4 *src = reinterpret_cast<const uint4 *>(pring + (sp * NMAT + m) * kPacked + r * 32);
-                // dequantize into registers, release the packed stage
-                uint32_t o[4 * nw];
-                if (MODE == 0) {
-                    const uint4 q0 = src[0], q1 = src[1];
-                    const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                // dequantize the stage's atoms into registers, release the packed stage
+                uint32_t o[kAt][4 * nw];
 #pragma unroll
-                    for (int w = 0; w < nw; ++w)
-                        dequant_word(wv[w], s2, b2, o + 4 * w);
-                } else {
-                    const uint4 qq = src[part];
-                    const uint32_t wv[4] = {qq.x, qq.y, qq.z, qq.w};
+                for (int at = 0; at < kAt; ++at) {
+                    if (at < nat) {
+                        const uint4 *src =
+                            reinterpret_cast<const uint4 *>(pring + sp * kPStage + (at * NMAT + m) * kPacked + r * 32);
+                        if (MODE == 0) {
+                            const uint4 q0 = src[0], q1 = src[1];
+                            const uint32_t wv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-                    for (int w = 0; w < nw; ++w)
-                        dequant_word(wv[w], s2, b2, o + 4 * w);
+                            for (int w = 0; w < nw; ++w)
+                                dequant_word(wv[w], s2[at], b2[at], o[at] + 4 * w);
+                        } else {
+                            const uint4 qq = src[part];
+                            const uint32_t wv[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                            for (int w = 0; w < nw; ++w)
+                                dequant_word(wv[w], s2[at], b2[at], o[at] + 4 * w);
+                        }
+                    }
                 }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&p_empty[sp]);
                 // publish the previous slot now: its TMEM stores drained
-                // behind this tile's waits, loads and arithmetic
+                // behind this stage's waits, loads and arithmetic
                 if (pend >= 0) {
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0)
-                        mbar_arrive(&s_full[pend]);
+                        mbar_arrive(&a_full[pend]);
                 }
-                tmem_st<nw>(tl + (uint32_t)ss * kSlotCols, o);
-                pend = ss;
+#pragma unroll
+                for (int at = 0; at < kAt; ++at)
+                    if (at < nat)
+                        tmem_st<nw>(tl + (uint32_t)sa * kSlotCols + (uint32_t)(at * NMAT * 32), o[at]);
+                pend = sa;
                 ++kf;
-                if (++ss == kNS) {
-                    ss = 0;
-                    phs ^= 1u;
+                if (++sa == kNA) {
+                    sa = 0;
+                    pha ^= 1u;
                 }
                 if (++sp == kNP) {
                     sp = 0;
@@ -539,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
-                mbar_arrive(&s_full[pend]);
+                mbar_arrive(&a_full[pend]);
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // -------------------------------------------------------- epilogue
@@ -802,7 +825,8 @@ cudaError_t encode_packed(CUtensorMap *m, const void *base, int rows, int cols, 
 template <int MODE>
 size_t gemm_smem()
 {
-    return 1024 + (size_t)Cfg<MODE>::NS * kBTile + (size_t)Cfg<MODE>::NP * Cfg<MODE>::NMAT * 128 * 32 + 512;
+    using C = Cfg<MODE>;
+    return 1024 + (size_t)C::NB * C::AT * kBTile + (size_t)C::NP * C::AT * C::NMAT * 128 * 32 + 512;
 }
 
 template <int MODE>
