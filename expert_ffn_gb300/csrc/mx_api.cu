@@ -299,10 +299,10 @@ mx_status run_pd(const PdIn *in, int n, int T, int pre_norm, float eps, const Pd
             return cuda_fail(e, "encoding the weight tensor maps");
         d.gate = maps.gate;
         d.up = maps.up;
-        d.down = maps.down;
+        d.down = maps.down1;
         d.sgate = maps.sgate;
         d.sup = maps.sup;
-        d.sdown = maps.sdownk;
+        d.sdown = maps.sdown1;
         d.rw = static_cast<const uint32_t *>(c.router->w);
         d.rs = static_cast<const uint16_t *>(c.router->scales);
         d.rb = static_cast<const uint16_t *>(c.router->biases);

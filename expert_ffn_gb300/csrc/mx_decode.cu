@@ -145,18 +145,6 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
                  : "memory");
 }
 
-// Contiguous split of n items over nc CTAs; with n <= nc, CTA c < n takes item c.
-__device__ __forceinline__ void prange(int n, int c, int nc, int &lo, int &hi)
-{
-    if (n <= nc) {
-        lo = c < n ? c : n;
-        hi = c < n ? c + 1 : n;
-    } else {
-        lo = (int)((long long)c * n / nc);
-        hi = (int)((long long)(c + 1) * n / nc);
-    }
-}
-
 // ------------------------------------------------------------ shared memory
 
 struct Rt {  // routing of the current layer (computed by the consumer warps)
@@ -171,23 +159,21 @@ struct Rt {  // routing of the current layer (computed by the consumer warps)
 };
 
 struct Smem {
-    uint64_t *fullL, *emptyL, *fullS, *emptyS, *route_bar;
-    uint8_t *ringL, *ringS;
+    uint64_t *full, *empty, *route_bar;
+    uint8_t *ring;         // NR slots: gate/up items (8 + 8 rows x D) and down items (D/4 rows x 64 columns)
     uint8_t *xraw;         // layer input x_l (act dtype) [T][D]
     uint8_t *xq;           // x_l after the optional rmsnorm (act dtype) [T][D]
     float *xg;             // [T][GD] group sums of xq, canonical order
     uint8_t *xpl;          // planes of xq (layout A, NB plane pairs)
-    uint8_t *hspl;         // planes of hs (layout A, 2 pairs), Gp = nch*GI groups, zero padded
-    float *hsg;            // [T][Gp]
-    uint8_t *hpl;          // planes of h (layout B, 2 pairs), per slot
-    float *hg;             // [T*K][GI]
-    float *red;            // [NL][kCW][32][2] gate/up cross-warp sums, per ring slot
-    int *icnt;             // [NL] warps done with the item in each gate/up slot
+    float *uh;             // [64][4] hidden values of the current unit
+    uint8_t *upl;          // [4][256] their e4m3 planes (2 pairs)
+    float *ux, *ufo;       // [4] their sums and plane back factors
+    uint16_t *dss, *dsb;   // [D] the unit's down-slice scales and biases (BF16 bits)
     float *lg;             // [T][E] logits of the layer
     float *pr;             // scratch
-    float *fx, *fhs, *fh;  // back factors 2^(9-k): x [T], hs [T], h [T*K]
+    float *fx;             // [T] x plane back factors 2^(9-k)
     float *rn, *xsc;       // [T] rmsnorm factors, x plane scales
-    int *vmax;             // [max(T, T*K)] plane maxima (float bits)
+    int *vmax;             // [T] plane maxima (float bits)
     int *flag;             // [4]
     uint8_t *zero;         // 16 zero bytes
     Rt rt;
@@ -197,34 +183,29 @@ __device__ __forceinline__ Smem carve(uint8_t *sm, const PdParams &p)
 {
     const PdSmem &o = p.sm;
     Smem s;
-    s.fullL = reinterpret_cast<uint64_t *>(sm);
-    s.emptyL = s.fullL + o.NL;
-    s.fullS = s.emptyL + o.NL;
-    s.emptyS = s.fullS + o.NS;
-    s.route_bar = s.emptyS + o.NS;
-    s.ringL = sm + o.ringL;
-    s.ringS = sm + o.ringS;
+    s.full = reinterpret_cast<uint64_t *>(sm);
+    s.empty = s.full + o.NR;
+    s.route_bar = s.empty + o.NR;
+    s.ring = sm + o.ring;
     s.xraw = sm + o.xraw;
     s.xq = sm + o.xq;
     s.xg = reinterpret_cast<float *>(sm + o.xg);
     s.xpl = sm + o.xpl;
-    s.hspl = sm + o.hspl;
-    s.hsg = reinterpret_cast<float *>(sm + o.hsg);
-    s.hpl = sm + o.hpl;
-    s.hg = reinterpret_cast<float *>(sm + o.hg);
-    s.red = reinterpret_cast<float *>(sm + o.red);
-    s.icnt = reinterpret_cast<int *>(sm + o.red + (size_t)o.NL * kCW * 64 * 4);
+    s.uh = reinterpret_cast<float *>(sm + o.uh);
+    s.upl = sm + o.upl;
+    s.dss = reinterpret_cast<uint16_t *>(sm + o.dss);
+    s.dsb = s.dss + p.D;
     s.lg = reinterpret_cast<float *>(sm + o.lg);
     s.pr = reinterpret_cast<float *>(sm + o.pr);
     float *m = reinterpret_cast<float *>(sm + o.misc);
     const int TK = p.T * p.K;
     s.fx = m;
-    s.fhs = m + 4;
-    s.rn = m + 8;
-    s.xsc = m + 12;
-    s.flag = reinterpret_cast<int *>(m + 16);
-    s.fh = m + 20;                                         // [TK]
-    s.vmax = reinterpret_cast<int *>(m + 20 + TK);         // [max(T, TK)]
+    s.rn = m + 4;
+    s.xsc = m + 8;
+    s.flag = reinterpret_cast<int *>(m + 12);
+    s.ux = m + 16;
+    s.ufo = m + 20;
+    s.vmax = reinterpret_cast<int *>(m + 24);  // [T]
     int *r = reinterpret_cast<int *>(sm + o.rt);
     const int amax = TK < p.E ? TK : p.E;
     s.rt.n_act = r;
@@ -402,20 +383,6 @@ __device__ __forceinline__ size_t plane_off(bool per_slot, int nvec, int Gp, int
                     : (size_t)g * 256 * nvec + (size_t)m * 128 * nvec + (size_t)nb * 64 * nvec + (2 * v + pp) * 32 + c * 8;
 }
 
-__device__ __forceinline__ void load8(const float *src, size_t ld, int v, int g, int w, int G, float (&x)[8])
-{
-    if (g < G) {
-        const float4 *q = reinterpret_cast<const float4 *>(src + (size_t)v * ld + (size_t)g * 64 + 8 * w);
-        const float4 a = __ldcg(q), b = __ldcg(q + 1);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            x[j] = 0.f;
-    }
-}
-
 __device__ __forceinline__ void store_planes(uint8_t *dst, bool per_slot, int nvec, int Gp, int v, int g, int w,
                                              float sc, float (&x)[8])
 {
@@ -428,73 +395,6 @@ __device__ __forceinline__ void store_planes(uint8_t *dst, bool per_slot, int nv
 #pragma unroll
     for (int p = 0; p < 4; ++p)
         *reinterpret_cast<uint2 *>(dst + plane_off(per_slot, nvec, Gp, v, g, m, p >> 1, p & 1, c)) = pl[p];
-}
-
-__device__ void planes_f32(const float *src, size_t ld, int nvec, int G, int Gp, bool per_slot, uint8_t *dst,
-                           float *gsum, float *back, int *vmax)
-{
-    const int tid = threadIdx.x;
-    const int nw = nvec * Gp * 8;  // 8-value words, padding included
-    constexpr int R = 4;           // words per thread kept in registers
-    for (int v = tid; v < nvec; v += kCT)
-        vmax[v] = 0;
-    csync();
-    const bool in_regs = nw <= R * kCT;
-    float x[R][8];
-    for (int w0 = 0; w0 < nw; w0 += R * kCT) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int wi = w0 + tid + r * kCT, v = wi / (Gp * 8), rem = wi - v * Gp * 8;
-            if (wi < nw)
-                load8(src, ld, v, rem >> 3, rem & 7, G, x[r]);
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int wi = w0 + tid + r * kCT, v = wi / (Gp * 8);
-            float sm = 0.f, mx = 0.f;
-            if (wi < nw) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    sm += x[r][j];
-                    mx = fmaxf(mx, fabsf(x[r][j]));
-                }
-            }
-            // the 8 words of a group sit in 8 consecutive lanes
-            sm += __shfl_xor_sync(0xffffffffu, sm, 1);
-            sm += __shfl_xor_sync(0xffffffffu, sm, 2);
-            sm += __shfl_xor_sync(0xffffffffu, sm, 4);
-            if (wi < nw) {
-                if ((wi & 7) == 0)
-                    gsum[wi >> 3] = sm;
-                if (mx > 0.f)
-                    atomicMax(&vmax[v], __float_as_int(mx));
-            }
-        }
-    }
-    csync();
-    for (int v = tid; v < nvec; v += kCT) {
-        float sc, bk;
-        plane_scale(__int_as_float(vmax[v]), sc, bk);
-        back[v] = bk;
-    }
-    for (int w0 = 0; w0 < nw; w0 += R * kCT) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int wi = w0 + tid + r * kCT, v = wi / (Gp * 8), rem = wi - v * Gp * 8;
-            if (wi < nw && !in_regs)
-                load8(src, ld, v, rem >> 3, rem & 7, G, x[r]);
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int wi = w0 + tid + r * kCT, v = wi / (Gp * 8), rem = wi - v * Gp * 8;
-            if (wi < nw) {
-                float sc, bk;
-                plane_scale(__int_as_float(vmax[v]), sc, bk);
-                store_planes(dst, per_slot, nvec, Gp, v, rem >> 3, rem & 7, sc, x[r]);
-            }
-        }
-    }
-    csync();
 }
 
 // x_l (xraw) -> xq (optionally rmsnorm'd, rounded to the act dtype), its group
@@ -833,67 +733,74 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
 
 // ------------------------------------------------------------------ producer
 
+// Units of a layer: shared units u < GS first, then routed units (active
+// expert j, block u) as r = j * GI + u; unit id i goes to CTA i mod NC.
+__device__ __forceinline__ int first_routed(int C, int NC, int GS) { return ((C - GS) % NC + NC) % NC; }
+
 template <int NB>
 __device__ void producer(const PdParams &p, const Smem &s)
 {
     const int lane = threadIdx.x & 31, C = blockIdx.x, NC = gridDim.x;
-    const int GD = p.D / 64, GI = p.I / 64, GS = p.S / 64;
-    const int GC = GI < GS ? GI : GS, nch = (GS + GC - 1) / GC;  // shared-down K chunks of GC groups
+    const int D = p.D, GD = D / 64, GI = p.I / 64, GS = p.S / 64, R4 = D / 4, R16 = D / 16;
     const PdSmem &o = p.sm;
-    int kL = 0, kS = 0;
+    int k = 0;
     bool ok = true;
-    // reserve the next slot of a ring (lane 0 waits; the verdict is the warp's)
-    auto take = [&](bool ringL, uint32_t bytes, uint8_t *&dst, uint64_t *&bar) -> bool {
-        int &k = ringL ? kL : kS;
-        const int n = ringL ? o.NL : o.NS, sl = k % n;
-        uint64_t *empty = ringL ? s.emptyL : s.emptyS;
+    // reserve the next ring slot (lane 0 waits; the verdict is the warp's)
+    auto take = [&](uint32_t bytes, uint8_t *&dst, uint64_t *&bar) -> bool {
+        const int sl = k % o.NR;
         int good = 1;
-        if (k >= n && lane == 0)
-            good = pwait(&empty[sl], ((k / n) - 1) & 1, p) ? 1 : 0;
+        if (k >= o.NR && lane == 0)
+            good = pwait(&s.empty[sl], ((k / o.NR) - 1) & 1, p) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, good, 0))
             return false;
-        dst = (ringL ? s.ringL + (size_t)sl * o.slotL : s.ringS + (size_t)sl * o.slotS);
-        bar = (ringL ? s.fullL : s.fullS) + sl;
+        dst = s.ring + (size_t)sl * o.slot;
+        bar = s.full + sl;
         if (lane == 0)
             mbar_arrive_expect_tx(bar, bytes);
         __syncwarp();
         ++k;
         return true;
     };
+    // the 12 items of unit (shared or expert e, block u): 8 gate/up items of
+    // 8 + 8 rows, then 4 down items of D/4 rows x the block's 64 columns
+    auto issue_unit = [&](const PdLayer &L, bool shared, int e, int u) -> bool {
+        for (int w = 0; w < 8; ++w) {
+            const int rb = 8 * u + w;  // 8-row block of gate/up
+            uint8_t *dst;
+            uint64_t *bar;
+            if (!take(576u * GD, dst, bar))
+                return false;
+            if (lane == 0) {
+                tma_load_4d(dst, shared ? &L.sgate : &L.gate, 0, 8 * rb, 0, e, bar);
+                tma_load_4d(dst + 256 * GD, shared ? &L.sup : &L.up, 0, 8 * rb, 0, e, bar);
+            } else if (lane <= 4) {
+                const int jj = lane - 1;
+                const uint16_t *src;
+                if (shared) {
+                    src = (jj & 1 ? L.sb[jj >> 1] : L.ss[jj >> 1]) + (size_t)8 * rb * GD;
+                } else {
+                    const uint8_t *rec = L.blob + (uint64_t)e * L.stride;
+                    src = reinterpret_cast<const uint16_t *>(rec + (jj & 1 ? L.off_b[jj >> 1] : L.off_s[jj >> 1])) +
+                          (size_t)8 * rb * GD;
+                }
+                bulk_g2s(dst + 512 * GD + jj * 16 * GD, src, 16u * GD, bar);
+            }
+        }
+        for (int q = 0; q < 4; ++q) {
+            uint8_t *dst;
+            uint64_t *bar;
+            if (!take(32u * R4, dst, bar))
+                return false;
+            if (lane < 4)
+                tma_load_4d(dst + lane * 32 * R16, shared ? &L.sdown : &L.down, 0, q * R4 + lane * R16, u, e, bar);
+            __syncwarp();
+        }
+        return true;
+    };
     for (int l = 0; l < p.n_layers && ok; ++l) {
         const PdLayer &L = p.L[l];
-        int lo, hi;
-        // A1: shared gate/up -> ring L
-        prange(p.S / 8, C, NC, lo, hi);
-        for (int it = lo; it < hi && ok; ++it) {
-            uint8_t *dst;
-            uint64_t *bar;
-            if (!(ok = take(true, 576u * GD, dst, bar)))
-                break;
-            if (lane == 0) {
-                tma_load_4d(dst, &L.sgate, 0, 8 * it, 0, 0, bar);
-                tma_load_4d(dst + 256 * GD, &L.sup, 0, 8 * it, 0, 0, bar);
-            } else if (lane <= 4) {
-                const int j = lane - 1;
-                const uint16_t *src = (j & 1 ? L.sb[j >> 1] : L.ss[j >> 1]) + (size_t)8 * it * GD;
-                bulk_g2s(dst + 512 * GD + j * 16 * GD, src, 16u * GD, bar);
-            }
-        }
-        // SD: shared down, 16 rows x (GC groups of one K chunk) -> ring S
-        prange((p.D / 16) * nch, C, NC, lo, hi);
-        for (int it = lo; it < hi && ok; ++it) {
-            const int rb = it / nch, ch = it - rb * nch;
-            uint8_t *dst;
-            uint64_t *bar;
-            if (!(ok = take(false, 512u * GC + 64u * GS, dst, bar)))
-                break;
-            if (lane == 0) {
-                tma_load_4d(dst, &L.sdown, 0, 16 * rb, ch * GC, 0, bar);
-            } else if (lane <= 2) {
-                const uint16_t *src = (lane == 2 ? L.sb[2] : L.ss[2]) + (size_t)16 * rb * GS;
-                bulk_g2s(dst + 512 * GC + (lane - 1) * 32 * GS, src, 32u * GS, bar);
-            }
-        }
+        for (int u = C; u < GS && ok; u += NC)
+            ok = issue_unit(L, true, 0, u);
         if (!ok)
             break;
         // routing of this layer (from the consumers)
@@ -902,72 +809,60 @@ __device__ void producer(const PdParams &p, const Smem &s)
             good = pwait(s.route_bar, l & 1, p) ? 1 : 0;
         if (!(ok = __shfl_sync(0xffffffffu, good, 0) != 0))
             break;
-        const int na = *s.rt.n_act;
-        // B: routed gate/up -> ring L
-        prange(na * (p.I / 8), C, NC, lo, hi);
-        for (int it = lo; it < hi && ok; ++it) {
-            const int j = it / (p.I / 8), rbi = it - j * (p.I / 8), e = s.rt.act_e[j];
-            uint8_t *dst;
-            uint64_t *bar;
-            if (!(ok = take(true, 576u * GD, dst, bar)))
-                break;
-            if (lane == 0) {
-                tma_load_4d(dst, &L.gate, 0, 8 * rbi, 0, e, bar);
-                tma_load_4d(dst + 256 * GD, &L.up, 0, 8 * rbi, 0, e, bar);
-            } else if (lane <= 4) {
-                const int jj = lane - 1;
-                const uint8_t *rec = L.blob + (uint64_t)e * L.stride;
-                const uint16_t *src =
-                    reinterpret_cast<const uint16_t *>(rec + (jj & 1 ? L.off_b[jj >> 1] : L.off_s[jj >> 1])) +
-                    (size_t)8 * rbi * GD;
-                bulk_g2s(dst + 512 * GD + jj * 16 * GD, src, 16u * GD, bar);
-            }
-        }
-        // RD: routed down, row-block major -> ring S
-        prange((p.D / 16) * na, C, NC, lo, hi);
-        for (int it = lo; it < hi && ok; ++it) {
-            const int rb = it / na, j = it - rb * na, e = s.rt.act_e[j];
-            uint8_t *dst;
-            uint64_t *bar;
-            if (!(ok = take(false, 576u * GI, dst, bar)))
-                break;
-            if (lane == 0) {
-                tma_load_4d(dst, &L.down, 0, 16 * rb, 0, e, bar);
-            } else if (lane <= 2) {
-                const uint8_t *rec = L.blob + (uint64_t)e * L.stride;
-                const uint16_t *src =
-                    reinterpret_cast<const uint16_t *>(rec + (lane == 2 ? L.off_b[2] : L.off_s[2])) +
-                    (size_t)16 * rb * GI;
-                bulk_g2s(dst + 512 * GI + (lane - 1) * 32 * GI, src, 32u * GI, bar);
-            }
-        }
+        const int nr = *s.rt.n_act * GI;
+        for (int r = first_routed(C, NC, GS); r < nr && ok; r += NC)
+            ok = issue_unit(L, false, s.rt.act_e[r / GI], r % GI);
     }
     // Leave no copy in flight: wait (bounded) for the last item of every slot.
     __syncwarp();
-    if (lane == 0) {
-        for (int k = (kL > o.NL ? kL - o.NL : 0); k < kL; ++k)
-            mbar_wait(&s.fullL[k % o.NL], (k / o.NL) & 1, p.err);
-        for (int k = (kS > o.NS ? kS - o.NS : 0); k < kS; ++k)
-            mbar_wait(&s.fullS[k % o.NS], (k / o.NS) & 1, p.err);
-    }
+    if (lane == 0)
+        for (int j = (k > o.NR ? k - o.NR : 0); j < k; ++j)
+            mbar_wait(&s.full[j % o.NR], (j / o.NR) & 1, p.err);
     __syncwarp();
 }
 
 // ----------------------------------------------------------------- consumers
+
+// e4m3 planes (2 pairs), the sum X and the back factor of each of the ne
+// hidden vectors of a unit (64 values each, uh[row * 4 + v]).  One warp: lane
+// = v * 8 + word.
+__device__ void unit_planes(const float *uh, int ne, uint8_t *upl, float *ux, float *ufo)
+{
+    const int lane = threadIdx.x & 31, v = lane >> 3, w = lane & 7;
+    float x[8], sm = 0.f, mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        x[j] = v < ne ? uh[(8 * w + j) * 4 + v] : 0.f;
+        sm += x[j];
+        mx = fmaxf(mx, fabsf(x[j]));
+    }
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) {
+        sm += __shfl_xor_sync(0xffffffffu, sm, d);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+    }
+    if (v < ne) {
+        float sc, bk;
+        plane_scale(mx, sc, bk);
+        store_planes(upl, true, ne, 1, v, 0, w, sc, x);
+        if (w == 0) {
+            ux[v] = sm;
+            ufo[v] = bk;
+        }
+    }
+}
 
 template <int NB>
 __device__ void consumers(const PdParams &p, const Smem &s)
 {
     constexpr int es = NB == 1 ? 2 : 4;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, c = lane & 3;
-    const int C = blockIdx.x, NC = gridDim.x, T = p.T, K = p.K, TK = T * K;
-    const int D = p.D, I = p.I, S = p.S, GD = D / 64, GI = I / 64, GS = S / 64;
-    const int GC = GI < GS ? GI : GS, nch = (GS + GC - 1) / GC;  // shared-down K chunks of GC groups
+    const int C = blockIdx.x, NC = gridDim.x, T = p.T, K = p.K;
+    const int D = p.D, I = p.I, S = p.S, GD = D / 64, GI = I / 64, GS = S / 64, R4 = D / 4;
     const PdSmem &o = p.sm;
-    int kL = 0, kS = 0;
+    int k = 0;  // ring items consumed so far
     bool ok = true;
     const int xgs = 2 * NB * 64 * T, xms = NB * 64 * T, xnbs = 64 * T;  // x planes (layout A)
-    const int hgs = 256 * T;                                             // hs planes (layout A, 2 pairs)
     for (int l = 0; l < p.n_layers && ok; ++l) {
         const PdLayer &L = p.L[l];
         int *ctr = p.ctr + l * p.cstride;
@@ -997,197 +892,125 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             red_add(ctr + 0, 1);
         }
 
-        // ---- gate/up items, all warps on each item, the last warp to finish
-        // an item reduces it (no CTA barrier per item): first the shared
-        // expert's (their weights are already on chip), then -- after the
-        // routing, done once every CTA's logits are in -- the routed ones.
-        int lo, hi, lo1, hi1, na = 0;
-        prange(S / 8, C, NC, lo1, hi1);
-        const int nA1 = hi1 - lo1;
-        lo = hi = 0;
-        for (int q = 0;; ++q) {
-            if (q == nA1) {
-                // shared gate/up of this CTA done: publish hs; then the routing
-                if (!(ok = csync_and(ok)))
-                    break;
-                if (tid == 0 && nA1 > 0) {
-                    __threadfence();
-                    red_add(ctr + 1, nA1);
+        // One unit: the 64 hidden rows [64u, 64u + 64) of the shared expert or
+        // of active expert j -- their gate/up (warp w: rows 8w..8w+7, all of
+        // K), h kept on chip, then that 64-column slice of the down projection
+        // for all D outputs, added into y.  No hidden vector leaves the CTA.
+        auto unit = [&](bool shared, int j, int u) -> bool {
+            const int e = shared ? 0 : s.rt.act_e[j], ne = shared ? T : s.rt.act_n[j];
+            bool good = true;
+            // the down slice's scales and biases (column u of the [D][G] tables)
+            csync();  // the previous unit's down items are done with them
+            {
+                const int G = shared ? GS : GI;
+                const uint16_t *sp, *bq;
+                if (shared) {
+                    sp = L.ss[2] + u;
+                    bq = L.sb[2] + u;
+                } else {
+                    const uint8_t *rec = L.blob + (uint64_t)e * L.stride;
+                    sp = reinterpret_cast<const uint16_t *>(rec + L.off_s[2]) + u;
+                    bq = reinterpret_cast<const uint16_t *>(rec + L.off_b[2]) + u;
                 }
-                if (!(ok = cwait(ctr + 0, NC, p, s)))
-                    break;
-                route_tables(p, L, s);
-                if (tid == 0)
-                    mbar_arrive(s.route_bar);
-                na = *s.rt.n_act;
-                prange(na * (I / 8), C, NC, lo, hi);
-            }
-            if (q >= nA1 && q - nA1 >= hi - lo)
-                break;
-            const bool routed = q >= nA1;
-            const int sl = kL % o.NL;
-            const bool bvalid_s = (gid >> 1) < T;
-            int it, ne, e = 0, rbi = 0, oslot = 0, ot, bt;
-            bool bvalid;
-            if (!routed) {
-                it = lo1 + q;
-                ne = T;
-                bvalid = bvalid_s;
-                bt = gid >> 1;
-                ot = c < T ? c : 0;
-            } else {
-                it = lo + q - nA1;
-                const int j = it / (I / 8);
-                rbi = it - j * (I / 8);
-                e = s.rt.act_e[j];
-                ne = s.rt.act_n[j];
-                bvalid = (gid >> 1) < ne;
-                bt = bvalid ? s.rt.act_slot[4 * j + (gid >> 1)] / K : 0;
-                oslot = c < ne ? s.rt.act_slot[4 * j + c] : 0;
-                ot = oslot / K;
-            }
-            const uint8_t *bp = bvalid ? s.xpl + (2 * bt + (gid & 1)) * 32 + c * 8 : s.zero;
-            const int bgs = bvalid ? xgs : 0, bms = bvalid ? xms : 0, bnbs = bvalid ? xnbs : 0;
-            // a warp whose wait gave up skips the remaining items but keeps to
-            // the loop, so that it reaches the same barriers as the others
-            if (ok && !__all_sync(0xffffffffu, pwait(&s.fullL[sl], (kL / o.NL) & 1, p)))
-                ok = false;
-            if (!ok) {
-                ++kL;
-                continue;
-            }
-            float ag = 0.f, au = 0.f;
-            gu_math<NB>(s.ringL + (size_t)sl * o.slotL, GD, warp, kCW, bp, bgs, bms, bnbs, s.fx[ot], s.xg + ot * GD,
-                        ag, au);
-            float *red = s.red + (size_t)sl * kCW * 64;
-            red[(warp * 32 + lane) * 2] = ag;
-            red[(warp * 32 + lane) * 2 + 1] = au;
-            __syncwarp();
-            int last = 0;
-            if (lane == 0) {
-                __threadfence_block();
-                last = atomicAdd(&s.icnt[sl], 1) == kCW - 1;
-            }
-            if (__shfl_sync(0xffffffffu, last, 0)) {
-                __threadfence_block();
-                if (c < ne) {
-                    float g = 0.f, u = 0.f;
+                constexpr int kR = kPdMaxD / kCT;
+                uint16_t sv[kR], bv[kR];
 #pragma unroll
-                    for (int w = 0; w < kCW; ++w) {
-                        g += red[(w * 32 + lane) * 2];
-                        u += red[(w * 32 + lane) * 2 + 1];
+                for (int i = 0; i < kR; ++i) {
+                    const int r = tid + i * kCT;
+                    sv[i] = r < D ? __ldg(sp + (size_t)r * G) : (uint16_t)0;
+                    bv[i] = r < D ? __ldg(bq + (size_t)r * G) : (uint16_t)0;
+                }
+#pragma unroll
+                for (int i = 0; i < kR; ++i) {
+                    const int r = tid + i * kCT;
+                    if (r < D) {
+                        s.dss[r] = sv[i];
+                        s.dsb[r] = bv[i];
                     }
-                    const float h = gelu_tanh(g) * u;
-                    if (routed)
-                        p.hbuf[(size_t)oslot * I + 8 * rbi + gid] = s.rt.slot_w[oslot] * h;
-                    else
-                        p.hsbuf[(size_t)c * S + 8 * it + gid] = h;
+                }
+            }
+            // gate/up: warp w owns item k + w
+            {
+                const int kk = k + warp, sl = kk % o.NR;
+                int bt, ot, oslot = 0;
+                bool bvalid;
+                if (shared) {
+                    bvalid = (gid >> 1) < T;
+                    bt = gid >> 1;
+                    ot = c < T ? c : 0;
+                } else {
+                    bvalid = (gid >> 1) < ne;
+                    bt = bvalid ? s.rt.act_slot[4 * j + (gid >> 1)] / K : 0;
+                    oslot = c < ne ? s.rt.act_slot[4 * j + c] : 0;
+                    ot = oslot / K;
+                }
+                const uint8_t *bp = bvalid ? s.xpl + (2 * bt + (gid & 1)) * 32 + c * 8 : s.zero;
+                if (!__all_sync(0xffffffffu, pwait(&s.full[sl], (kk / o.NR) & 1, p))) {
+                    good = false;
+                } else {
+                    float ag = 0.f, au = 0.f;
+                    gu_math<NB>(s.ring + (size_t)sl * o.slot, GD, 0, 1, bp, bvalid ? xgs : 0, bvalid ? xms : 0,
+                                bvalid ? xnbs : 0, s.fx[ot], s.xg + ot * GD, ag, au);
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_n(&s.empty[sl], kCW);
+                    if (c < ne) {
+                        float h = gelu_tanh(ag) * au;
+                        if (!shared)
+                            h *= s.rt.slot_w[oslot];
+                        s.uh[(8 * warp + gid) * 4 + c] = h;
+                    }
+                }
+            }
+            if (!(good = csync_and(good)))
+                return false;
+            if (warp == 0)
+                unit_planes(s.uh, ne, s.upl, s.ux, s.ufo);
+            csync();
+            // down: items k + 8 .. k + 11, D/4 rows each; warp w takes row
+            // tiles w, w + 8, ... of every item
+            const bool bvalid = (gid >> 1) < ne;
+            const uint8_t *bp = bvalid ? s.upl + (gid >> 1) * 256 + (gid & 1) * 32 + c * 8 : s.zero;
+            const int ot = c < ne ? (shared ? c : s.rt.act_slot[4 * j + c] / K) : 0;
+            const int oc = c < ne ? c : 0;
+            for (int q = 0; q < 4; ++q) {
+                const int kk = k + 8 + q, sl = kk % o.NR;
+                if (!__all_sync(0xffffffffu, good && pwait(&s.full[sl], (kk / o.NR) & 1, p))) {
+                    good = false;
+                    continue;
+                }
+                const uint8_t *tile = s.ring + (size_t)sl * o.slot;
+                for (int rt = warp; rt < R4 / 16; rt += kCW) {
+                    const int r0 = q * R4 + 16 * rt;
+                    float a0 = 0.f, a8 = 0.f;
+                    dn_math(tile + rt * 512, s.dss + r0, s.dsb + r0, 1, 1, bp, 256, bvalid ? 128 : 0,
+                            bvalid ? 64 : 0, s.ufo[oc], s.ux + oc, a0, a8);
+                    if (c < ne) {
+                        red_fix(y + (size_t)ot * D + r0 + gid, a0);
+                        red_fix(y + (size_t)ot * D + r0 + gid + 8, a8);
+                    }
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    s.icnt[sl] = 0;
-                    mbar_arrive(&s.emptyL[sl]);
-                }
+                if (lane == 0)
+                    mbar_arrive(&s.empty[sl]);
             }
-            (void)e;
-            ++kL;
-        }
+            k += 12;
+            return csync_and(good);
+        };
+
+        for (int u = C; u < GS && ok; u += NC)
+            ok = unit(true, 0, u);
+        // the routing, once every CTA's logits are in
         if (!(ok = csync_and(ok)))
             break;
-        // publish h: one fence, then one count per expert this CTA worked on
-        if (tid == 0) {
-            __threadfence();
-            for (int it = lo; it < hi;) {
-                const int j = it / (I / 8), end = min(hi, (j + 1) * (I / 8));
-                red_add(ctr + 3 + s.rt.act_e[j], end - it);
-                it = end;
-            }
-        }
-
-        // ---- down projections, one warp per item: the shared expert's K
-        // chunks (hs planes), then -- once h of every active expert is in --
-        // the routed ones (h planes)
-        if (!(ok = cwait(ctr + 1, S / 8, p, s)))
+        if (!(ok = cwait(ctr + 0, NC, p, s)))
             break;
-        const int Gp = nch * GC;
-        planes_f32(p.hsbuf, S, T, GS, Gp, false, s.hspl, s.hsg, s.fhs, s.vmax);
-        int slo, shi, rlo, rhi;
-        prange((D / 16) * nch, C, NC, slo, shi);
-        prange((D / 16) * na, C, NC, rlo, rhi);
-        const int nsd = shi - slo, ndn = nsd + (rhi - rlo);
-        bool hstep = false;
-        for (int q = warp;; q += kCW) {
-            if (!hstep && q >= nsd) {
-                // every warp joins this once, after its shared items
-                hstep = true;
-                bool good = ok;
-                if (tid < na)
-                    good = good && gwait(ctr + 3 + s.rt.act_e[tid], I / 8, p);
-                if (!(ok = csync_and(good)))
-                    break;
-                planes_f32(p.hbuf, I, TK, GI, GI, true, s.hpl, s.hg, s.fh, s.vmax);
-            }
-            if (q >= ndn)
-                break;
-            if (!ok)
-                continue;  // skip the work, still join the h step above
-            const int k = kS + q, sl = k % o.NS;
-            const uint8_t *st = s.ringS + (size_t)sl * o.slotS;
-            const uint16_t *sv = reinterpret_cast<const uint16_t *>(st + 512 * (q < nsd ? GC : GI));
-            const uint16_t *bv;
-            const uint8_t *bp;
-            const float *xgo;
-            int rb, ne, pitch, G, bgs, bms, bnbs, ot;
-            float fo;
-            if (q < nsd) {  // shared down, K chunk ch: B = hs planes of every token
-                const int it = slo + q, ch = it % nch;
-                rb = it / nch;
-                ne = T;
-                pitch = GS;
-                G = min(GC, GS - ch * GC);
-                bv = sv + 16 * GS + ch * GC;
-                sv += ch * GC;
-                const bool bvalid = (gid >> 1) < T;
-                bp = bvalid ? s.hspl + (size_t)ch * GC * hgs + gid * 32 + c * 8 : s.zero;
-                bgs = bvalid ? hgs : 0;
-                bms = bvalid ? 128 * T : 0;
-                bnbs = bvalid ? 64 * T : 0;
-                ot = c < T ? c : 0;
-                fo = s.fhs[ot];
-                xgo = s.hsg + ot * Gp + ch * GC;
-            } else {  // routed down of active expert j: B = h planes of its slots
-                const int it = rlo + q - nsd, j = it % na;
-                rb = it / na;
-                ne = s.rt.act_n[j];
-                pitch = GI;
-                G = GI;
-                bv = sv + 16 * GI;
-                const bool bvalid = (gid >> 1) < ne;
-                const int bs = bvalid ? s.rt.act_slot[4 * j + (gid >> 1)] : 0;
-                bp = bvalid ? s.hpl + (size_t)bs * GI * 256 + (gid & 1) * 32 + c * 8 : s.zero;
-                bgs = bvalid ? 256 : 0;
-                bms = bvalid ? 128 : 0;
-                bnbs = bvalid ? 64 : 0;
-                const int oslot = c < ne ? s.rt.act_slot[4 * j + c] : 0;
-                ot = oslot / K;
-                fo = s.fh[oslot];
-                xgo = s.hg + oslot * GI;
-            }
-            if (!__all_sync(0xffffffffu, pwait(&s.fullS[sl], (k / o.NS) & 1, p))) {
-                ok = false;
-                continue;
-            }
-            float a0 = 0.f, a8 = 0.f;
-            dn_math(st, sv, bv, pitch, G, bp, bgs, bms, bnbs, fo, xgo, a0, a8);
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&s.emptyS[sl]);
-            if (c < ne) {
-                red_fix(y + (size_t)ot * D + 16 * rb + gid, a0);
-                red_fix(y + (size_t)ot * D + 16 * rb + gid + 8, a8);
-            }
-        }
-        kS += ndn;
+        route_tables(p, L, s);
+        if (tid == 0)
+            mbar_arrive(s.route_bar);
+        const int nr = *s.rt.n_act * GI;
+        for (int r = first_routed(C, NC, GS); r < nr && ok; r += NC)
+            ok = unit(false, r / GI, r % GI);
         if (!(ok = csync_and(ok)))
             break;
         if (tid == 0) {
@@ -1242,21 +1065,15 @@ __global__ void __launch_bounds__(kPT, 1) pd_kernel(const __grid_constant__ PdPa
     extern __shared__ __align__(1024) uint8_t sm[];
     const Smem s = carve(sm, p);
     if (threadIdx.x == 0) {
-        for (int i = 0; i < p.sm.NL; ++i) {
-            mbar_init(&s.fullL[i], 1);
-            mbar_init(&s.emptyL[i], 1);
-        }
-        for (int i = 0; i < p.sm.NS; ++i) {
-            mbar_init(&s.fullS[i], 1);
-            mbar_init(&s.emptyS[i], 1);
+        for (int i = 0; i < p.sm.NR; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], kCW);  // gate/up items: one warp arrives for all; down items: every warp
         }
         mbar_init(s.route_bar, 1);
         fence_mbar_init();
     }
     if (threadIdx.x < 4)
         reinterpret_cast<uint32_t *>(s.zero)[threadIdx.x] = 0u;
-    if (threadIdx.x < p.sm.NL)
-        s.icnt[threadIdx.x] = 0;
     // Clear this CTA's share of the fixed-point sums of every layer; the first
     // layer's logit exchange orders it before any CTA adds into them.
     {
@@ -1299,41 +1116,34 @@ size_t al(size_t n, size_t a) { return (n + a - 1) / a * a; }
 // Shared-memory plan; returns false if no ring depth fits.
 bool pd_plan(int T, int D, int I, int S, int E, int K, int act, int n_cta, int smem_max, PdSmem *out)
 {
-    if (T < 1 || T > kPdMaxT || n_cta < 1)
+    if (T < 1 || T > kPdMaxT || n_cta < 1 || D % 64 || I % 64 || S % 64 || D > kPdMaxD)
         return false;
     const int NB = act == 0 ? 2 : 1;
-    const int GD = D / 64, GI = I / 64, GS = S / 64, TK = T * K, amax = TK < E ? TK : E;
-    const int GC = GI < GS ? GI : GS, Gp = (GS + GC - 1) / GC * GC;
+    const int GD = D / 64, TK = T * K, amax = TK < E ? TK : E;
     const int es = act == 1 ? 2 : 4;
     const size_t scratch = (size_t)4 * std::max((size_t)T * GD, (size_t)GD * (T + 2));
-    const int depths[][2] = {{4, 8}, {3, 12}, {3, 8}, {2, 8}, {2, 4}};
-    for (const auto &dp : depths) {
+    for (int nr = 8; nr >= 3; --nr) {
         PdSmem o{};
-        o.NL = dp[0];
-        o.NS = dp[1];
-        o.slotL = (int)al((size_t)576 * GD, 128);
-        o.slotS = (int)al((size_t)512 * GI + 64 * (size_t)std::max(GI, GS), 128);
-        size_t off = al((size_t)8 * (2 * o.NL + 2 * o.NS + 1), 128);
+        o.NR = nr;
+        o.slot = (int)al((size_t)576 * GD, 128);  // a gate/up item; a down item takes 512 * GD
+        size_t off = al((size_t)8 * (2 * o.NR + 1), 128);
         auto take = [&](size_t bytes) {
             const size_t at = off;
             off = al(off + bytes, 128);
             return (int)at;
         };
-        o.ringL = take((size_t)o.NL * o.slotL);
-        o.ringS = take((size_t)o.NS * o.slotS);
+        o.ring = take((size_t)o.NR * o.slot);
         o.xraw = take((size_t)T * D * es);
         o.xq = take((size_t)T * D * es);
         o.xg = take((size_t)T * GD * 4);
         o.xpl = take((size_t)GD * 128 * NB * T);
-        o.hspl = take((size_t)Gp * 256 * T);
-        o.hsg = take((size_t)T * Gp * 4);
-        o.hpl = take((size_t)TK * GI * 256);
-        o.hg = take((size_t)TK * GI * 4);
-        o.red = take((size_t)o.NL * (kCW * 64 * 4 + 4));
+        o.uh = take((size_t)64 * 4 * 4);
+        o.upl = take((size_t)4 * 256);
+        o.dss = take((size_t)2 * D * 2);
         o.lg = take((size_t)T * E * 4);
         o.rt = take((size_t)4 * (20 + 6 * amax + 2 * TK + E));
         o.pr = take(scratch);
-        o.misc = take((size_t)4 * (20 + TK + std::max(T, TK)));
+        o.misc = take((size_t)4 * (24 + 4));
         o.zero = take(16);
         o.total = (int)off;
         if ((long long)off <= smem_max) {

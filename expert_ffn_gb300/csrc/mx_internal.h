@@ -87,7 +87,7 @@ struct DnLaunch {
 // down over all experts of the blob, and the shared expert's three matrices.
 struct FfnMaps {
     CUtensorMap gate, up, down, sgate, sup, sdown;
-    CUtensorMap sdownk;  // shared down in K chunks of min(I, S)/64 groups (single-launch path)
+    CUtensorMap down1, sdown1;  // down projections, D/16 rows x one 64-column group (single-launch path)
 };
 cudaError_t get_ffn_maps(const FfnArgs &a, FfnMaps *out);
 
@@ -113,16 +113,17 @@ cudaError_t launch_ffn_decode(const FfnArgs &a, int max_tiles, int num_sms, cuda
 // for T <= kPdMaxT tokens in one persistent cooperative kernel.
 constexpr int kPdMaxT = 4;
 constexpr int kPdMaxLayers = 30;  // layers per launch (the layer table is a kernel parameter)
+constexpr int kPdMaxD = 4096;     // d_model limit of the path (down-slice copies of D/16 rows)
 
 // Byte offsets into the kernel's dynamic shared memory.
 struct PdSmem {
-    int NL, NS, slotL, slotS;  // ring depths and slot bytes (gate/up ring, down ring)
-    int ringL, ringS, xraw, xq, xg, xpl, hspl, hsg, hpl, hg, red, lg, rt, pr, misc, zero;
+    int NR, slot;  // ring depth and slot bytes
+    int ring, xraw, xq, xg, xpl, uh, upl, dss, lg, rt, pr, misc, zero;
     int total;
 };
 
 // One layer: TMA maps of its routed (over all experts of the blob) and shared
-// matrices (the shared down map in K chunks of min(I, S)/64 groups), its
+// matrices (the down maps in slices of D/16 rows x one 64-column group), its
 // router, the s/b offsets of the expert records, its outputs.
 struct PdLayer {
     CUtensorMap gate, up, down, sgate, sup, sdown;

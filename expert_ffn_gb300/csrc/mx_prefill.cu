@@ -84,14 +84,6 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
 // Instruction descriptor: FP16 A and B (K-major), fp32 D, M = 128, N.
 __device__ __forceinline__ uint32_t idesc_f16(int n) { return (1u << 4) | ((uint32_t)(n >> 3) << 17) | (8u << 24); }
 
-__device__ __forceinline__ void umma(uint32_t dtm, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc)
-{
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtm),
-                 "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
-                 : "memory");
-}
-
 // D[tmem] (+)= A[tmem] * B[smem]^T
 __device__ __forceinline__ void umma_ts(uint32_t dtm, uint32_t atm, uint64_t bd, uint32_t idesc, uint32_t acc)
 {
@@ -117,7 +109,6 @@ __device__ __forceinline__ bool elect_one()
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32])
 {

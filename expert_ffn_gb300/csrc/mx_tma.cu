@@ -106,7 +106,9 @@ cudaError_t get_ffn_maps(const FfnArgs &a, FfnMaps *out)
         (e = encode_qmat(&m.sgate, a.sw[0], a.S, a.D, 1, 0, 8)) != cudaSuccess ||
         (e = encode_qmat(&m.sup, a.sw[1], a.S, a.D, 1, 0, 8)) != cudaSuccess ||
         (e = encode_qmat(&m.sdown, a.sw[2], a.D, a.S, 1, 0, 16)) != cudaSuccess ||
-        (e = encode_qmat(&m.sdownk, a.sw[2], a.D, a.S, 1, 0, 16, a.I < a.S ? a.I / 64 : a.S / 64)) != cudaSuccess)
+        (e = encode_qmat(&m.down1, a.blob + a.off_w[2], a.D, a.I, a.E, a.stride, a.D / 16 < 256 ? a.D / 16 : 256, 1)) !=
+            cudaSuccess ||
+        (e = encode_qmat(&m.sdown1, a.sw[2], a.D, a.S, 1, 0, a.D / 16 < 256 ? a.D / 16 : 256, 1)) != cudaSuccess)
         return e;
     std::lock_guard<std::mutex> g(g_mu);
     g_keys[g_next] = k;
