@@ -303,38 +303,52 @@ __device__ __forceinline__ void red_fix(long long *y, float v)
 
 // ---------------------------------------------------------------- the math
 
-// Gate/up item (8 gate rows -> MMA rows 0-7, 8 up rows -> rows 8-15) over the
-// groups g = g0, g0 + gs, ... of K = G groups.  Slot layout: gate tile
-// [G][8][32 B], up tile [G][8][32 B], gate.s, gate.b, up.s, up.b ([8][G] BF16).
-// bp: this lane's B column (plane pair) for group 0; bgs/bms/bnbs: strides of
-// group, k-step, plane pair.  fo, xgo: the lane's output column (slot c).
+// Gate/up item on one warp: 8 gate rows -> MMA rows 0-7, 8 up rows -> rows
+// 8-15, all G groups of K.  Slot layout: gate tile [G][8][32 B], up tile
+// [G][8][32 B], gate.s, gate.b, up.s, up.b ([8][G] BF16).  bp: this lane's B
+// column (plane pair) for group 0; bgs/bms/bnbs: strides of group, k-step,
+// plane pair.  fo, xgo: the lane's output column (slot c).  Four groups in
+// flight, the scale and bias sums kept apart, so the loop carries no long
+// dependency chain.  Lane output: gate and up dot products of row gid, column
+// slot c.
 template <int NB>
-__device__ __forceinline__ void gu_math(const uint8_t *st, int G, int g0, int gs, const uint8_t *bp, int bgs,
-                                        int bms, int bnbs, float fo, const float *xgo, float &accg, float &accu)
+__device__ __forceinline__ void gu_item(const uint8_t *st, int G, const uint8_t *bp, int bgs, int bms, int bnbs,
+                                        float fo, const float *xgo, float &accg, float &accu)
 {
     const int lane = threadIdx.x & 31, gid = lane >> 2, c = lane & 3;
     const uint8_t *gt = st + gid * 32 + c * 8, *ut = gt + 256 * G;
     const uint16_t *sc = reinterpret_cast<const uint16_t *>(st + 512 * G) + gid * G;
     const uint16_t *sg = sc, *bg = sc + 8 * G, *su = sc + 16 * G, *bu = sc + 24 * G;
-#pragma unroll 2
-    for (int g = g0; g < G; g += gs) {
-        const uint2 qg = lds64(gt + 256 * g), qu = lds64(ut + 256 * g);
+    float pg[4] = {0.f, 0.f, 0.f, 0.f}, pu[4] = {0.f, 0.f, 0.f, 0.f};
+    float qg[4] = {0.f, 0.f, 0.f, 0.f}, qu[4] = {0.f, 0.f, 0.f, 0.f};
+    auto group = [&](int g, int j) {
+        const uint2 wg = lds64(gt + 256 * g), wu = lds64(ut + 256 * g);
         float Rg = 0.f, Ru = 0.f;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             float d[4] = {0.f, 0.f, 0.f, 0.f};
             const uint2 b0 = lds64(bp + g * bgs + nb * bnbs), b1 = lds64(bp + g * bgs + bms + nb * bnbs);
-            mma_fp8(d, qg.x & kLo, qu.x & kLo, (qg.x >> 4) & kLo, (qu.x >> 4) & kLo, b0.x, b0.y);
-            mma_fp8(d, qg.y & kLo, qu.y & kLo, (qg.y >> 4) & kLo, (qu.y >> 4) & kLo, b1.x, b1.y);
+            mma_fp8(d, wg.x & kLo, wu.x & kLo, (wg.x >> 4) & kLo, (wu.x >> 4) & kLo, b0.x, b0.y);
+            mma_fp8(d, wg.y & kLo, wu.y & kLo, (wg.y >> 4) & kLo, (wu.y >> 4) & kLo, b1.x, b1.y);
             Rg += d[0] + d[1];
             Ru += d[2] + d[3];
         }
         const float X = xgo[g];
-        accg = fmaf(bf2f(sg[g]), Rg * fo, accg);
-        accg = fmaf(bf2f(bg[g]), X, accg);
-        accu = fmaf(bf2f(su[g]), Ru * fo, accu);
-        accu = fmaf(bf2f(bu[g]), X, accu);
+        pg[j] = fmaf(bf2f(sg[g]), Rg, pg[j]);
+        qg[j] = fmaf(bf2f(bg[g]), X, qg[j]);
+        pu[j] = fmaf(bf2f(su[g]), Ru, pu[j]);
+        qu[j] = fmaf(bf2f(bu[g]), X, qu[j]);
+    };
+    int g = 0;
+    for (; g + 4 <= G; g += 4) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            group(g + j, j);
     }
+    for (; g < G; ++g)
+        group(g, 0);
+    accg = fo * ((pg[0] + pg[1]) + (pg[2] + pg[3])) + ((qg[0] + qg[1]) + (qg[2] + qg[3]));
+    accu = fo * ((pu[0] + pu[1]) + (pu[2] + pu[3])) + ((qu[0] + qu[1]) + (qu[2] + qu[3]));
 }
 
 // Down item: 16 rows x G groups, one warp.  tile [G][16][32 B]; s, b: the
@@ -897,10 +911,14 @@ __device__ void consumers(const PdParams &p, const Smem &s)
         // K), h kept on chip, then that 64-column slice of the down projection
         // for all D outputs, added into y.  No hidden vector leaves the CTA.
         auto unit = [&](bool shared, int j, int u) -> bool {
-            const int e = shared ? 0 : s.rt.act_e[j], ne = shared ? T : s.rt.act_n[j];
+            const int ne = shared ? T : s.rt.act_n[j];
             bool good = true;
-            // the down slice's scales and biases (column u of the [D][G] tables)
-            csync();  // the previous unit's down items are done with them
+            // the down slice's scales and biases (column u of the [D][G]
+            // tables; 16-bit elements at a row pitch TMA cannot take): loaded
+            // now, stored once the gate/up work has hidden their latency
+            csync();  // the previous unit's down items are done with dss/dsb
+            constexpr int kR = kPdMaxD / kCT;
+            uint32_t sbv[kR];  // (bias << 16) | scale of rows tid + i * kCT
             {
                 const int G = shared ? GS : GI;
                 const uint16_t *sp, *bq;
@@ -908,25 +926,15 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                     sp = L.ss[2] + u;
                     bq = L.sb[2] + u;
                 } else {
-                    const uint8_t *rec = L.blob + (uint64_t)e * L.stride;
+                    const uint8_t *rec = L.blob + (uint64_t)s.rt.act_e[j] * L.stride;
                     sp = reinterpret_cast<const uint16_t *>(rec + L.off_s[2]) + u;
                     bq = reinterpret_cast<const uint16_t *>(rec + L.off_b[2]) + u;
                 }
-                constexpr int kR = kPdMaxD / kCT;
-                uint16_t sv[kR], bv[kR];
 #pragma unroll
                 for (int i = 0; i < kR; ++i) {
                     const int r = tid + i * kCT;
-                    sv[i] = r < D ? __ldg(sp + (size_t)r * G) : (uint16_t)0;
-                    bv[i] = r < D ? __ldg(bq + (size_t)r * G) : (uint16_t)0;
-                }
-#pragma unroll
-                for (int i = 0; i < kR; ++i) {
-                    const int r = tid + i * kCT;
-                    if (r < D) {
-                        s.dss[r] = sv[i];
-                        s.dsb[r] = bv[i];
-                    }
+                    sbv[i] = r < D ? (uint32_t)__ldg(sp + (size_t)r * G) | ((uint32_t)__ldg(bq + (size_t)r * G) << 16)
+                                   : 0u;
                 }
             }
             // gate/up: warp w owns item k + w
@@ -945,11 +953,17 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                     ot = oslot / K;
                 }
                 const uint8_t *bp = bvalid ? s.xpl + (2 * bt + (gid & 1)) * 32 + c * 8 : s.zero;
-                if (!__all_sync(0xffffffffu, pwait(&s.full[sl], (kk / o.NR) & 1, p))) {
+                // With fewer slots than gate/up items, item kk reuses the slot of
+                // item kk - NR of this unit, which another warp may not have read
+                // yet; a parity wait on the slot's full barrier would then look
+                // two phases ahead and pass at once.  Wait for that item's
+                // release first: then the wait below is exactly one phase ahead.
+                bool w_ok = warp < o.NR || pwait(&s.empty[sl], ((kk / o.NR) - 1) & 1, p);
+                if (!__all_sync(0xffffffffu, w_ok && pwait(&s.full[sl], (kk / o.NR) & 1, p))) {
                     good = false;
                 } else {
                     float ag = 0.f, au = 0.f;
-                    gu_math<NB>(s.ring + (size_t)sl * o.slot, GD, 0, 1, bp, bvalid ? xgs : 0, bvalid ? xms : 0,
+                    gu_item<NB>(s.ring + (size_t)sl * o.slot, GD, bp, bvalid ? xgs : 0, bvalid ? xms : 0,
                                 bvalid ? xnbs : 0, s.fx[ot], s.xg + ot * GD, ag, au);
                     __syncwarp();
                     if (lane == 0)
@@ -960,6 +974,14 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                             h *= s.rt.slot_w[oslot];
                         s.uh[(8 * warp + gid) * 4 + c] = h;
                     }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < kR; ++i) {
+                const int r = tid + i * kCT;
+                if (r < D) {
+                    s.dss[r] = (uint16_t)sbv[i];
+                    s.dsb[r] = (uint16_t)(sbv[i] >> 16);
                 }
             }
             if (!(good = csync_and(good)))
@@ -980,14 +1002,24 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                     continue;
                 }
                 const uint8_t *tile = s.ring + (size_t)sl * o.slot;
-                for (int rt = warp; rt < R4 / 16; rt += kCW) {
-                    const int r0 = q * R4 + 16 * rt;
-                    float a0 = 0.f, a8 = 0.f;
-                    dn_math(tile + rt * 512, s.dss + r0, s.dsb + r0, 1, 1, bp, 256, bvalid ? 128 : 0,
+                const uint16_t *isv = s.dss + q * R4, *ibv = s.dsb + q * R4;
+                const int nrt = R4 / 16;
+                for (int rt = warp; rt < nrt; rt += 2 * kCW) {
+                    // two row tiles at a time (the second repeats the first past the end)
+                    const int rt2 = rt + kCW < nrt ? rt + kCW : rt;
+                    float a0 = 0.f, a8 = 0.f, b0 = 0.f, b8 = 0.f;
+                    dn_math(tile + rt * 512, isv + 16 * rt, ibv + 16 * rt, 1, 1, bp, 256, bvalid ? 128 : 0,
                             bvalid ? 64 : 0, s.ufo[oc], s.ux + oc, a0, a8);
+                    dn_math(tile + rt2 * 512, isv + 16 * rt2, ibv + 16 * rt2, 1, 1, bp, 256, bvalid ? 128 : 0,
+                            bvalid ? 64 : 0, s.ufo[oc], s.ux + oc, b0, b8);
                     if (c < ne) {
+                        const int r0 = q * R4 + 16 * rt, r2 = q * R4 + 16 * rt2;
                         red_fix(y + (size_t)ot * D + r0 + gid, a0);
                         red_fix(y + (size_t)ot * D + r0 + gid + 8, a8);
+                        if (rt2 != rt) {
+                            red_fix(y + (size_t)ot * D + r2 + gid, b0);
+                            red_fix(y + (size_t)ot * D + r2 + gid + 8, b8);
+                        }
                     }
                 }
                 __syncwarp();
@@ -1005,6 +1037,14 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             break;
         if (!(ok = cwait(ctr + 0, NC, p, s)))
             break;
+        if (l > 0) {
+            // every CTA has rebuilt x_l from y_{l-1} before its logits of layer
+            // l arrived: clear this CTA's share of y_{l-1} for the next call
+            long long *yp = p.ybuf + (size_t)(l - 1) * T * D;
+            const int n = T * D, per = (n + NC - 1) / NC;
+            for (int i = C * per + tid; i < min(n, (C + 1) * per); i += kCT)
+                yp[i] = 0;
+        }
         route_tables(p, L, s);
         if (tid == 0)
             mbar_arrive(s.route_bar);
@@ -1074,15 +1114,10 @@ __global__ void __launch_bounds__(kPT, 1) pd_kernel(const __grid_constant__ PdPa
     }
     if (threadIdx.x < 4)
         reinterpret_cast<uint32_t *>(s.zero)[threadIdx.x] = 0u;
-    // Clear this CTA's share of the fixed-point sums of every layer; the first
-    // layer's logit exchange orders it before any CTA adds into them.
-    {
-        const size_t n = (size_t)p.n_layers * p.T * p.D;
-        const size_t per = (n + gridDim.x - 1) / gridDim.x, b = per * blockIdx.x;
-        for (size_t i = b + threadIdx.x; i < b + per && i < n; i += kPT)
-            p.ybuf[i] = 0;
-        __threadfence();
-    }
+    // The fixed-point sums y of every layer are zero on entry: the workspace
+    // starts zeroed, and every call clears them again once they are read (layer
+    // l - 1 after layer l's logit exchange, the last layer at the end), so a
+    // shared-expert unit may add into y before any exchange of this call.
     __syncthreads();
     if (threadIdx.x >= kCT)
         producer<NB>(p, s);
@@ -1104,6 +1139,10 @@ __global__ void __launch_bounds__(kPT, 1) pd_kernel(const __grid_constant__ PdPa
         const int n = p.n_layers * p.cstride + 1;  // counters + done
         for (int i = threadIdx.x; i < n; i += kPT)
             p.ctr[i] = 0;
+        // every CTA has read the last layer's y: clear it for the next call
+        long long *yp = p.ybuf + (size_t)(p.n_layers - 1) * p.T * p.D;
+        for (int i = threadIdx.x; i < p.T * p.D; i += kPT)
+            yp[i] = 0;
     }
 }
 
