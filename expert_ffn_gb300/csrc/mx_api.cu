@@ -226,7 +226,7 @@ bool pd_usable(const mx_moe_layout *L, int T, PdSmem *sm, int *n_cta)
         return false;
     const int act = L->act_dtype == MX_BF16 ? 1 : 0;
     // leave room for the kernel's static shared memory
-    if (!pd_plan(T, L->d_model, L->d_expert, L->d_shared, L->n_experts, L->top_k, act, d.sms, d.smem_optin - 2048,
+    if (!pd_plan(T, L->d_model, L->d_expert, L->d_shared, L->n_experts, L->top_k, act, d.sms, d.smem_optin - 1280,
                  sm))
         return false;
     *n_cta = d.sms;

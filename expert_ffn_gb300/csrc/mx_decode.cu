@@ -168,7 +168,7 @@ struct Smem {
     float *uh;             // [64][4] hidden values of the current unit
     uint8_t *upl;          // [4][256] their e4m3 planes (2 pairs)
     float *ux, *ufo;       // [4] their sums and plane back factors
-    uint16_t *dss, *dsb;   // [D] the unit's down-slice scales and biases (BF16 bits)
+    uint16_t *dss;         // [2][2][D/4] down-item scales and biases (BF16 bits), two buffers
     float *lg;             // [T][E] logits of the layer
     float *pr;             // scratch
     float *fx;             // [T] x plane back factors 2^(9-k)
@@ -194,7 +194,6 @@ __device__ __forceinline__ Smem carve(uint8_t *sm, const PdParams &p)
     s.uh = reinterpret_cast<float *>(sm + o.uh);
     s.upl = sm + o.upl;
     s.dss = reinterpret_cast<uint16_t *>(sm + o.dss);
-    s.dsb = s.dss + p.D;
     s.lg = reinterpret_cast<float *>(sm + o.lg);
     s.pr = reinterpret_cast<float *>(sm + o.pr);
     float *m = reinterpret_cast<float *>(sm + o.misc);
@@ -307,10 +306,10 @@ __device__ __forceinline__ void red_fix(long long *y, float v)
 // 8-15, all G groups of K.  Slot layout: gate tile [G][8][32 B], up tile
 // [G][8][32 B], gate.s, gate.b, up.s, up.b ([8][G] BF16).  bp: this lane's B
 // column (plane pair) for group 0; bgs/bms/bnbs: strides of group, k-step,
-// plane pair.  fo, xgo: the lane's output column (slot c).  Four groups in
-// flight, the scale and bias sums kept apart, so the loop carries no long
-// dependency chain.  Lane output: gate and up dot products of row gid, column
-// slot c.
+// plane pair.  fo, xgo: the lane's output column (slot c; xgo 16-byte
+// aligned).  Four groups in flight, the scale and bias sums kept apart, so the
+// loop carries no long dependency chain.  Lane output: gate and up dot products
+// of row gid, column slot c.
 template <int NB>
 __device__ __forceinline__ void gu_item(const uint8_t *st, int G, const uint8_t *bp, int bgs, int bms, int bnbs,
                                         float fo, const float *xgo, float &accg, float &accu)
@@ -321,9 +320,12 @@ __device__ __forceinline__ void gu_item(const uint8_t *st, int G, const uint8_t 
     const uint16_t *sg = sc, *bg = sc + 8 * G, *su = sc + 16 * G, *bu = sc + 24 * G;
     float pg[4] = {0.f, 0.f, 0.f, 0.f}, pu[4] = {0.f, 0.f, 0.f, 0.f};
     float qg[4] = {0.f, 0.f, 0.f, 0.f}, qu[4] = {0.f, 0.f, 0.f, 0.f};
-    auto group = [&](int g, int j) {
+    // the MMA part of group g: the row's gate and up dot products (plane
+    // columns summed)
+    auto dots = [&](int g, float &Rg, float &Ru) {
         const uint2 wg = lds64(gt + 256 * g), wu = lds64(ut + 256 * g);
-        float Rg = 0.f, Ru = 0.f;
+        Rg = 0.f;
+        Ru = 0.f;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
             float d[4] = {0.f, 0.f, 0.f, 0.f};
@@ -333,20 +335,45 @@ __device__ __forceinline__ void gu_item(const uint8_t *st, int G, const uint8_t 
             Rg += d[0] + d[1];
             Ru += d[2] + d[3];
         }
-        const float X = xgo[g];
-        pg[j] = fmaf(bf2f(sg[g]), Rg, pg[j]);
-        qg[j] = fmaf(bf2f(bg[g]), X, qg[j]);
-        pu[j] = fmaf(bf2f(su[g]), Ru, pu[j]);
-        qu[j] = fmaf(bf2f(bu[g]), X, qu[j]);
     };
     int g = 0;
-    for (; g + 4 <= G; g += 4) {
+    if ((G & 3) == 0) {
+        // four groups at a time; their scales, biases and x sums in vector loads
+        for (; g < G; g += 4) {
+            const uint2 s4g = lds64(reinterpret_cast<const uint8_t *>(sg + g));
+            const uint2 b4g = lds64(reinterpret_cast<const uint8_t *>(bg + g));
+            const uint2 s4u = lds64(reinterpret_cast<const uint8_t *>(su + g));
+            const uint2 b4u = lds64(reinterpret_cast<const uint8_t *>(bu + g));
+            const float4 X4 = *reinterpret_cast<const float4 *>(xgo + g);
+            const uint32_t wsg[2] = {s4g.x, s4g.y}, wbg[2] = {b4g.x, b4g.y}, wsu[2] = {s4u.x, s4u.y},
+                           wbu[2] = {b4u.x, b4u.y};
+            const float X[4] = {X4.x, X4.y, X4.z, X4.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-            group(g + j, j);
+            for (int j = 0; j < 4; ++j) {
+                float Rg, Ru;
+                dots(g + j, Rg, Ru);
+                const int h = j >> 1;
+                const float fsg = __uint_as_float(j & 1 ? wsg[h] & 0xFFFF0000u : wsg[h] << 16);
+                const float fbg = __uint_as_float(j & 1 ? wbg[h] & 0xFFFF0000u : wbg[h] << 16);
+                const float fsu = __uint_as_float(j & 1 ? wsu[h] & 0xFFFF0000u : wsu[h] << 16);
+                const float fbu = __uint_as_float(j & 1 ? wbu[h] & 0xFFFF0000u : wbu[h] << 16);
+                pg[j] = fmaf(fsg, Rg, pg[j]);
+                qg[j] = fmaf(fbg, X[j], qg[j]);
+                pu[j] = fmaf(fsu, Ru, pu[j]);
+                qu[j] = fmaf(fbu, X[j], qu[j]);
+            }
+        }
+    } else {
+        for (; g < G; ++g) {
+            float Rg, Ru;
+            dots(g, Rg, Ru);
+            const float X = xgo[g];
+            pg[0] = fmaf(bf2f(sg[g]), Rg, pg[0]);
+            qg[0] = fmaf(bf2f(bg[g]), X, qg[0]);
+            pu[0] = fmaf(bf2f(su[g]), Ru, pu[0]);
+            qu[0] = fmaf(bf2f(bu[g]), X, qu[0]);
+        }
     }
-    for (; g < G; ++g)
-        group(g, 0);
     accg = fo * ((pg[0] + pg[1]) + (pg[2] + pg[3])) + ((qg[0] + qg[1]) + (qg[2] + qg[3]));
     accu = fo * ((pu[0] + pu[1]) + (pu[2] + pu[3])) + ((qu[0] + qu[1]) + (qu[2] + qu[3]));
 }
@@ -916,7 +943,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             // the down slice's scales and biases (column u of the [D][G]
             // tables; 16-bit elements at a row pitch TMA cannot take): loaded
             // now, stored once the gate/up work has hidden their latency
-            csync();  // the previous unit's down items are done with dss/dsb
+            csync();  // every warp is done with the previous unit
             constexpr int kR = kPdMaxD / kCT;
             uint32_t sbv[kR];  // (bias << 16) | scale of rows tid + i * kCT
             {
@@ -976,14 +1003,6 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                     }
                 }
             }
-#pragma unroll
-            for (int i = 0; i < kR; ++i) {
-                const int r = tid + i * kCT;
-                if (r < D) {
-                    s.dss[r] = (uint16_t)sbv[i];
-                    s.dsb[r] = (uint16_t)(sbv[i] >> 16);
-                }
-            }
             if (!(good = csync_and(good)))
                 return false;
             if (warp == 0)
@@ -996,13 +1015,25 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             const int ot = c < ne ? (shared ? c : s.rt.act_slot[4 * j + c] / K) : 0;
             const int oc = c < ne ? c : 0;
             for (int q = 0; q < 4; ++q) {
+                // this item's scales and biases into buffer q & 1 (the barrier
+                // also tells that every warp is done with item q - 1, so buffer
+                // q & 1, last read for item q - 2, is free)
+                uint16_t *isv = s.dss + (q & 1) * 2 * R4, *ibv = isv + R4;
+#pragma unroll
+                for (int i = 0; i < kR; ++i) {
+                    const int r = tid + i * kCT - q * R4;
+                    if (r >= 0 && r < R4) {
+                        isv[r] = (uint16_t)sbv[i];
+                        ibv[r] = (uint16_t)(sbv[i] >> 16);
+                    }
+                }
+                csync();
                 const int kk = k + 8 + q, sl = kk % o.NR;
                 if (!__all_sync(0xffffffffu, good && pwait(&s.full[sl], (kk / o.NR) & 1, p))) {
                     good = false;
                     continue;
                 }
                 const uint8_t *tile = s.ring + (size_t)sl * o.slot;
-                const uint16_t *isv = s.dss + q * R4, *ibv = s.dsb + q * R4;
                 const int nrt = R4 / 16;
                 for (int rt = warp; rt < nrt; rt += 2 * kCW) {
                     // two row tiles at a time (the second repeats the first past the end)
@@ -1178,7 +1209,7 @@ bool pd_plan(int T, int D, int I, int S, int E, int K, int act, int n_cta, int s
         o.xpl = take((size_t)GD * 128 * NB * T);
         o.uh = take((size_t)64 * 4 * 4);
         o.upl = take((size_t)4 * 256);
-        o.dss = take((size_t)2 * D * 2);
+        o.dss = take((size_t)2 * 2 * (D / 4) * 2);
         o.lg = take((size_t)T * E * 4);
         o.rt = take((size_t)4 * (20 + 6 * amax + 2 * TK + E));
         o.pr = take(scratch);
