@@ -15,7 +15,7 @@ from .build import LIB as LIB_PATH
 
 __all__ = ["MxError", "lib", "QLinear", "Ffn", "Sub", "Layout", "Options", "LAYOUT_MAGIC", "LAYOUT_VERSION",
            "MX_F32", "MX_BF16", "DeviceLayer", "layer_forward", "layer_forward_ex", "route", "stack_forward",
-           "workspace_bytes", "stack_workspace_bytes", "workspace_init", "EXPORTED"]
+           "workspace_bytes", "stack_workspace_bytes", "workspace_init", "layer_forward_static", "EXPORTED"]
 
 LAYOUT_MAGIC = 0x4D584D45
 LAYOUT_VERSION = 1
@@ -25,7 +25,7 @@ MX_F32, MX_BF16 = 0, 1
 EXPORTED = ("mx_moe_layer_forward", "mx_moe_layer_forward_ex", "mx_moe_workspace_bytes", "mx_moe_workspace_init",
             "mx_moe_route", "mx_moe_stack_forward", "mx_moe_stack_workspace_bytes", "mx_status_string",
             "mx_last_error_string", "mx_version", "mx_moe_profile_enable", "mx_moe_profile_read",
-            "mx_moe_workspace_check")
+            "mx_moe_workspace_check", "mx_moe_layer_forward_static")
 
 
 class MxError(RuntimeError):
@@ -74,6 +74,7 @@ def lib():
             L.mx_moe_layer_forward.argtypes = [P, I32, C.POINTER(QLinear), C.POINTER(Ffn), P, C.POINTER(Layout),
                                                P, P, P]
             L.mx_moe_layer_forward_ex.argtypes = L.mx_moe_layer_forward.argtypes + [C.POINTER(Options), P, P, SZ]
+            L.mx_moe_layer_forward_static.argtypes = L.mx_moe_layer_forward.argtypes + [C.POINTER(Options), P]
             L.mx_moe_workspace_bytes.argtypes = [C.POINTER(Layout), I32]
             L.mx_moe_workspace_bytes.restype = SZ
             L.mx_moe_stack_workspace_bytes.argtypes = [C.POINTER(Layout), I32]
@@ -90,7 +91,8 @@ def lib():
             L.mx_moe_profile_enable.argtypes = [I32]
             L.mx_moe_workspace_check.argtypes = [P, P]
             L.mx_moe_profile_read.argtypes = [C.POINTER(C.c_double), C.POINTER(C.c_int), I32]
-            for name in ("mx_moe_layer_forward", "mx_moe_layer_forward_ex", "mx_moe_workspace_init",
+            for name in ("mx_moe_layer_forward", "mx_moe_layer_forward_ex", "mx_moe_layer_forward_static",
+                         "mx_moe_workspace_init",
                          "mx_moe_route", "mx_moe_stack_forward", "mx_moe_profile_enable", "mx_moe_profile_read",
                          "mx_moe_workspace_check"):
                 getattr(L, name).restype = C.c_int
@@ -209,6 +211,15 @@ def layer_forward_ex(x, T, layer: DeviceLayer, out, topk_idx, topk_w, ws, ws_byt
     _check(lib().mx_moe_layer_forward_ex(_ptr(x), T, C.byref(layer.router), C.byref(layer.shared),
                                          _ptr(layer.blob), C.byref(layer.layout), _ptr(out), _ptr(topk_idx),
                                          _ptr(topk_w), C.byref(opt), _stream_handle(stream), _ptr(ws), ws_bytes))
+
+
+def layer_forward_static(x, T, layer: DeviceLayer, out, topk_idx, topk_w, stream=None, residual=None,
+                         pre_rmsnorm=False, rms_eps=1e-6):
+    """The block for T <= 4 with the library's fixed device scratch (no workspace, no allocation)."""
+    opt = Options(_ptr(residual), 1 if pre_rmsnorm else 0, rms_eps)
+    _check(lib().mx_moe_layer_forward_static(_ptr(x), T, C.byref(layer.router), C.byref(layer.shared),
+                                             _ptr(layer.blob), C.byref(layer.layout), _ptr(out), _ptr(topk_idx),
+                                             _ptr(topk_w), C.byref(opt), _stream_handle(stream)))
 
 
 def route(x, T, layer: DeviceLayer, topk_idx, topk_w, counts, offsets, perm, ws, ws_bytes, logits=None,

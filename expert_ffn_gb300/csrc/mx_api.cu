@@ -583,6 +583,11 @@ OwnedWs g_ws[64];
 
 } // namespace
 
+// Scratch of mx_moe_layer_forward_static: one per device, zero at load.
+static __device__ __align__(256) unsigned char g_static_scratch[MX_STATIC_SCRATCH_BYTES];
+static std::mutex g_static_mu;
+static void *g_static_ptr[64];  // per device ordinal, resolved on the first call
+
 extern "C" {
 
 const char *mx_version(void) { return "0.1.0"; }
@@ -689,6 +694,61 @@ mx_status mx_moe_layer_forward(const void *x, int T, const mx_qlinear *router, c
         w.bytes = need;
     }
     return forward_impl(c, nullptr, w.ptr, w.bytes);
+}
+
+// ------------------------------------------------ allocation-free variant
+
+mx_status mx_moe_layer_forward_static(const void *x, int T, const mx_qlinear *router, const mx_ffn *shared,
+                                      const void *expert_blob, const mx_moe_layout *layout, void *out,
+                                      int32_t *topk_idx, float *topk_w, const mx_moe_options *opt, void *stream)
+{
+    const Call c{x, T, router, shared, expert_blob, layout, out, topk_idx, topk_w, opt};
+    mx_status st = validate_block(c);
+    if (st != MX_OK || T == 0)
+        return st;
+    const int D = layout->d_model, E = layout->n_experts;
+    if (T > kPdMaxT || D > kPdMaxD || E > 256)
+        return fail(MX_ERR_UNSUPPORTED, "the allocation-free call takes T <= %d, d_model <= %d, n_experts <= 256 "
+                                        "(got T=%d, d_model=%d, n_experts=%d)",
+                    kPdMaxT, kPdMaxD, T, D, E);
+    PdSmem sm;
+    int n_cta = 0;
+    if (!pd_usable(layout, T, &sm, &n_cta))
+        return fail(MX_ERR_UNSUPPORTED, "the single-launch decode path is not usable for this layout on this device");
+    // scratch: error word, counters, logits, fixed-point sums (all must start at zero)
+    Plan p{};
+    p.err = 0;
+    p.pd_ctr = 256;
+    p.pd_logits = p.pd_ctr + up256(pd_ctr_ints(E, 1) * sizeof(int));
+    p.pd_y = p.pd_logits + up256((size_t)T * E * sizeof(float));
+    p.pd_h = p.pd_hs = p.pd_y;  // not used by the single-launch kernel
+    const size_t used = p.pd_y + (size_t)T * D * sizeof(long long);
+    if (used > MX_STATIC_SCRATCH_BYTES)
+        return fail(MX_ERR_UNSUPPORTED, "scratch of %zu bytes needed, %u available", used, MX_STATIC_SCRATCH_BYTES);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64)
+        return fail(MX_ERR_UNSUPPORTED, "device ordinal %d", dev);
+    void *base;
+    {
+        std::lock_guard<std::mutex> g(g_static_mu);
+        if (!g_static_ptr[dev]) {
+            void *ptr = nullptr;
+            if ((e = cudaGetSymbolAddress(&ptr, g_static_scratch)) != cudaSuccess)
+                return cuda_fail(e, "cudaGetSymbolAddress");
+            g_static_ptr[dev] = ptr;
+        }
+        base = g_static_ptr[dev];
+    }
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((e = cudaMemsetAsync(base, 0, used, s)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync");
+    const void *res = opt ? opt->residual : nullptr;
+    const PdIn in{router, shared, expert_blob, layout, x, out, res, res ? 2 : 0, topk_idx, topk_w};
+    const int pre = (opt && opt->pre_rmsnorm) ? 1 : 0;
+    return run_pd(&in, 1, T, pre, opt ? opt->rms_eps : 0.0f, sm, n_cta, p, static_cast<uint8_t *>(base), s);
 }
 
 mx_status mx_moe_route(const void *x, int T, const mx_qlinear *router, const mx_moe_layout *layout,

@@ -173,6 +173,35 @@ MX_API mx_status mx_moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 MX_API mx_status mx_moe_workspace_check(const void *ws, void *stream);
 
 /*
+ * The block for 1 <= T <= 4 tokens with no workspace argument and no
+ * allocation: the single-launch decode kernel with its scratch (error word,
+ * counters, logits, fixed-point sums) in one device array of this library,
+ * MX_STATIC_SCRATCH_BYTES long.  The pages have no counterpart to this call;
+ * it exists for callers that may not allocate at all while they run -- a
+ * serving loop whose device memory is budgeted and owned up front, or code
+ * on a path where an allocation's implicit synchronisation or failure under
+ * memory pressure is not acceptable -- and that have no workspace to pass.
+ *   arguments as mx_moe_layer_forward_ex (opt nullable; stream: cudaStream_t,
+ *   NULL = legacy default stream), without ws / ws_bytes.
+ * Limits (else MX_ERR_UNSUPPORTED, nothing launched): T <= 4, d_model <= 4096,
+ * n_experts <= 256, and the single-launch path usable on this device (its
+ * shared-memory plan fits; not disabled by MX_MOE_SINGLE_LAUNCH=0).
+ * The first call on each device resolves the array's address
+ * (cudaGetSymbolAddress); make that first call outside any stream capture.
+ * Every call clears the scratch it uses (cudaMemsetAsync on `stream`) before
+ * the kernel.  Calls allocate nothing, host or device.  There is one scratch
+ * array per device: calls that may overlap on the GPU (other streams, other
+ * host threads) race on it and must be ordered by the caller.  A device-side
+ * wait that gives up is not reported (use mx_moe_layer_forward_ex and
+ * mx_moe_workspace_check where that matters).
+ */
+#define MX_STATIC_SCRATCH_BYTES (144u * 1024u)
+MX_API mx_status mx_moe_layer_forward_static(const void *x, int T, const mx_qlinear *router, const mx_ffn *shared,
+                                      const void *expert_blob, const mx_moe_layout *layout,
+                                      void *out, int32_t *topk_idx, float *topk_w,
+                                      const mx_moe_options *opt, void *stream);
+
+/*
  * Routing alone (router GEMV + top-k + softmax + grouping), for exact checks.
  *   topk_idx  device int32 [T][K];  topk_w device fp32 [T][K]
  *   counts    device int32 [E]      tokens per expert
