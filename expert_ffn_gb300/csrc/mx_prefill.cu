@@ -474,23 +474,33 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 sv = reinterpret_cast<const uint16_t *>(rec + a.off_s[j]) + (size_t)row * G;
                 bv = reinterpret_cast<const uint16_t *>(rec + a.off_b[j]) + (size_t)row * G;
             }
-            // scale and bias of the row's groups, one stage ahead in registers
-            uint32_t s_nx[kAt], b_nx[kAt];
+            // scale and bias of the row's groups, kPf stages ahead in a register
+            // ring (the loads are L2/DRAM latency; a stage takes well under that)
+            constexpr int kPf = 4;
+            uint32_t s_r[kPf][kAt], b_r[kPf][kAt];
 #pragma unroll
-            for (int at = 0; at < kAt; ++at) {
-                s_nx[at] = (valid && at < U.kt_n) ? __ldg(sv + at) : 0u;
-                b_nx[at] = (valid && at < U.kt_n) ? __ldg(bv + at) : 0u;
-            }
-            for (int kt0 = 0; kt0 < U.kt_n; kt0 += kAt) {
+            for (int j = 0; j < kPf; ++j)
+#pragma unroll
+                for (int at = 0; at < kAt; ++at) {
+                    const int kn = j * kAt + at;
+                    s_r[j][at] = (valid && kn < U.kt_n) ? __ldg(sv + kn) : 0u;
+                    b_r[j][at] = (valid && kn < U.kt_n) ? __ldg(bv + kn) : 0u;
+                }
+            for (int kb = 0; kb < U.kt_n && ok; kb += kPf * kAt)
+#pragma unroll
+            for (int jj = 0; jj < kPf; ++jj) {
+                const int kt0 = kb + jj * kAt;
+                if (kt0 >= U.kt_n)
+                    break;
                 const int nat = min(kAt, U.kt_n - kt0);
                 __half2 s2[kAt], b2[kAt];
 #pragma unroll
                 for (int at = 0; at < kAt; ++at) {
-                    s2[at] = __float2half2_rn(bf2f((uint16_t)s_nx[at]));
-                    b2[at] = __float2half2_rn(bf2f((uint16_t)b_nx[at]));
-                    const int kn = kt0 + kAt + at;
-                    s_nx[at] = (valid && kn < U.kt_n) ? __ldg(sv + kn) : 0u;
-                    b_nx[at] = (valid && kn < U.kt_n) ? __ldg(bv + kn) : 0u;
+                    s2[at] = __float2half2_rn(bf2f((uint16_t)s_r[jj][at]));
+                    b2[at] = __float2half2_rn(bf2f((uint16_t)b_r[jj][at]));
+                    const int kn = kt0 + kPf * kAt + at;
+                    s_r[jj][at] = (valid && kn < U.kt_n) ? __ldg(sv + kn) : 0u;
+                    b_r[jj][at] = (valid && kn < U.kt_n) ? __ldg(bv + kn) : 0u;
                 }
                 ok = bwait(&p_full[sp], php, a.err, abort) && (kf < kNA || bwait(&a_empty[sa], pha ^ 1u, a.err, abort));
                 if (!__all_sync(0xffffffffu, ok)) {
