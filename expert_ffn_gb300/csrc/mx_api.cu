@@ -116,7 +116,7 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb)
 struct Plan {
     size_t err, tickets, logits, counts, offsets, perm, tiles, ntiles, xp, xg, hr0, hr1, hs0, hs1;
     // single-launch decode path (T <= kPdMaxT)
-    size_t pd_ctr, pd_logits, pd_h, pd_hs, pd_y, pd_x;
+    size_t pd_ctr, pd_logits, pd_y, pd_x;
     int pd_T;
     // prefill path (T > kDecodeChunk, BF16)
     size_t pf;
@@ -155,8 +155,6 @@ Plan make_plan(const mx_moe_layout *L, int T_route, int T_ffn)
     p.pd_T = (int)Tp;
     p.pd_ctr = take(pd_ctr_ints((int)E, kPdMaxLayers) * 4);
     p.pd_logits = take(Tp * E * 4);
-    p.pd_h = take(Tp * K * I * 4);
-    p.pd_hs = take(Tp * S * 4);
     p.pd_y = take((size_t)kPdMaxLayers * Tp * D * 8);
     p.pd_x = take(Tp * D * es);
     p.pf = (T_route > kDecodeChunk && L->act_dtype == MX_BF16)
@@ -268,8 +266,6 @@ mx_status run_pd(const PdIn *in, int n, int T, int pre_norm, float eps, const Pd
     P.ctr = reinterpret_cast<int *>(ws + p.pd_ctr);
     P.cstride = 3 + P.E;
     P.logits = reinterpret_cast<float *>(ws + p.pd_logits);
-    P.hbuf = reinterpret_cast<float *>(ws + p.pd_h);
-    P.hsbuf = reinterpret_cast<float *>(ws + p.pd_hs);
     P.ybuf = reinterpret_cast<long long *>(ws + p.pd_y);
     P.sm = sm;
     for (int l = 0; l < n; ++l) {
@@ -721,7 +717,6 @@ mx_status mx_moe_layer_forward_static(const void *x, int T, const mx_qlinear *ro
     p.pd_ctr = 256;
     p.pd_logits = p.pd_ctr + up256(pd_ctr_ints(E, 1) * sizeof(int));
     p.pd_y = p.pd_logits + up256((size_t)T * E * sizeof(float));
-    p.pd_h = p.pd_hs = p.pd_y;  // not used by the single-launch kernel
     const size_t used = p.pd_y + (size_t)T * D * sizeof(long long);
     if (used > MX_STATIC_SCRATCH_BYTES)
         return fail(MX_ERR_UNSUPPORTED, "scratch of %zu bytes needed, %u available", used, MX_STATIC_SCRATCH_BYTES);

@@ -150,8 +150,6 @@ struct PdParams {
     int *ctr;              // [n_layers][cstride] counters, then done, abort (zero on entry)
     int cstride;           // 3 + E
     float *logits;         // [T][E]
-    float *hbuf;           // [T*K][I] routed hidden (weighted)
-    float *hsbuf;          // [T][S] shared hidden
     long long *ybuf;       // [n_layers][T][D] fixed-point sums of the down projections
     PdSmem sm;
     PdLayer L[kPdMaxLayers];
