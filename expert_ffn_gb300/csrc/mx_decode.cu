@@ -145,6 +145,22 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
                  : "memory");
 }
 
+// Optional phase trace (built with -DMX_PD_TRACE): consumer thread 0 of every
+// CTA records %globaltimer at the phase edges of one layer.
+#ifdef MX_PD_TRACE
+constexpr int kTraceLayer = 10, kTraceCtas = 160, kTracePts = 24;
+__device__ unsigned long long g_pd_trace[kTraceCtas][kTracePts];
+#define PD_STAMP(l, i)                                                                            \
+    do {                                                                                          \
+        if (threadIdx.x == 0 && (l) == kTraceLayer && blockIdx.x < kTraceCtas)                    \
+            g_pd_trace[blockIdx.x][i] = global_ns();                                              \
+    } while (0)
+#else
+#define PD_STAMP(l, i) \
+    do {               \
+    } while (0)
+#endif
+
 // ------------------------------------------------------------ shared memory
 
 struct Rt {  // routing of the current layer (computed by the consumer warps)
@@ -247,6 +263,24 @@ __device__ bool gwait(const int *c, int target, const PdParams &p)
             }
         }
     }
+}
+
+// Producer-side wait: polls with a short sleep, so the waiting warp leaves the
+// issue slots of its scheduler to the consumer warps.
+__device__ __forceinline__ bool pwait_sleepy(uint64_t *bar, uint32_t parity, const PdParams &p)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        __nanosleep(64);
+        if (global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(p.err, kErrTimeout);
+            set_abort(p);
+            return false;
+        }
+    }
+    return true;
 }
 
 __device__ __forceinline__ bool pwait(uint64_t *bar, uint32_t parity, const PdParams &p)
@@ -791,7 +825,7 @@ __device__ void producer(const PdParams &p, const Smem &s)
         const int sl = k % o.NR;
         int good = 1;
         if (k >= o.NR && lane == 0)
-            good = pwait(&s.empty[sl], ((k / o.NR) - 1) & 1, p) ? 1 : 0;
+            good = pwait_sleepy(&s.empty[sl], ((k / o.NR) - 1) & 1, p) ? 1 : 0;
         if (!__shfl_sync(0xffffffffu, good, 0))
             return false;
         dst = s.ring + (size_t)sl * o.slot;
@@ -847,7 +881,7 @@ __device__ void producer(const PdParams &p, const Smem &s)
         // routing of this layer (from the consumers)
         int good = 1;
         if (lane == 0)
-            good = pwait(s.route_bar, l & 1, p) ? 1 : 0;
+            good = pwait_sleepy(s.route_bar, l & 1, p) ? 1 : 0;
         if (!(ok = __shfl_sync(0xffffffffu, good, 0) != 0))
             break;
         const int nr = *s.rt.n_act * GI;
@@ -919,6 +953,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             rsv = bf2f(__ldg(L.rs + (size_t)C * GD + tid));
             rbv = bf2f(__ldg(L.rb + (size_t)C * GD + tid));
         }
+        PD_STAMP(l, 0);
         if (l == 0) {
             const uint4 *src = reinterpret_cast<const uint4 *>(L.x_in);
             uint4 *dst = reinterpret_cast<uint4 *>(s.xraw);
@@ -927,7 +962,9 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             csync();
         }
         prologue<NB>(p, s);
+        PD_STAMP(l, 1);
         router_rows<NB>(p, L, s, rq, rsv, rbv);  // ends with a consumer barrier
+        PD_STAMP(l, 2);
         if (tid == 0) {
             __threadfence();
             red_add(ctr + 0, 1);
@@ -1063,6 +1100,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
 
         for (int u = C; u < GS && ok; u += NC)
             ok = unit(true, 0, u);
+        PD_STAMP(l, 3);
         // the routing, once every CTA's logits are in
         if (!(ok = csync_and(ok)))
             break;
@@ -1076,14 +1114,17 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             for (int i = C * per + tid; i < min(n, (C + 1) * per); i += kCT)
                 yp[i] = 0;
         }
+        PD_STAMP(l, 4);
         route_tables(p, L, s);
         if (tid == 0)
             mbar_arrive(s.route_bar);
+        PD_STAMP(l, 5);
         const int nr = *s.rt.n_act * GI;
         for (int r = first_routed(C, NC, GS); r < nr && ok; r += NC)
             ok = unit(false, r / GI, r % GI);
         if (!(ok = csync_and(ok)))
             break;
+        PD_STAMP(l, 9);
         if (tid == 0) {
             __threadfence();
             red_add(ctr + 2, 1);
@@ -1092,6 +1133,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
         // ---- y is complete when every CTA has added its part: out = residual + lambda y
         if (!(ok = cwait(ctr + 2, NC, p, s)))
             break;
+        PD_STAMP(l, 10);
         for (int i0 = 0; i0 < T * D; i0 += 4 * kCT) {
             long long yq[4];
 #pragma unroll
@@ -1126,6 +1168,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             }
         }
         csync();
+        PD_STAMP(l, 11);
     }
     (void)lane;
 }
@@ -1225,6 +1268,14 @@ bool pd_plan(int T, int D, int I, int S, int E, int K, int act, int n_cta, int s
 }
 
 size_t pd_ctr_ints(int E, int n_layers) { return (size_t)n_layers * (3 + E) + 2; }
+
+#ifdef MX_PD_TRACE
+// Copies the phase trace ([kTraceCtas][kTracePts] nanosecond stamps) to host.
+extern "C" __attribute__((visibility("default"))) int mx_pd_trace_read(unsigned long long *host)
+{
+    return (int)cudaMemcpyFromSymbol(host, g_pd_trace, sizeof(g_pd_trace));
+}
+#endif
 
 namespace {
 
