@@ -516,7 +516,7 @@ mx_status run_prefill(const Call &c, const Plan &p, uint8_t *ws, cudaStream_t s)
     prof_begin(kStageRoute, s);
     cudaError_t e = launch_prefill_prepare(f, &pp, s);
     if (e == cudaSuccess)
-        e = launch_route_large(ra, pp.X16, pp.xsc, pp.XG, s);
+        e = launch_route_large(ra, pp.X16, pp.xsc, pp.XG, pp.QF, s);
     prof_end(kStageRoute, s);
     if (e != cudaSuccess)
         return cuda_fail(e, "prefill routing");

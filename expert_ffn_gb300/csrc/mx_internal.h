@@ -213,6 +213,7 @@ struct PfCall {
 struct PfPrepared {
     const void *X16;
     const float *xsc, *XG;
+    float *QF;  // route_f32_bytes of scratch for the router
 };
 
 size_t pf_workspace_bytes(int T, int D, int I, int S, int E, int K);
@@ -221,7 +222,9 @@ cudaError_t launch_prefill_prepare(const PfCall &c, PfPrepared *out, cudaStream_
 // After routing: scatter, gate/up GEMM, down GEMM, combine.
 cudaError_t launch_prefill(const PfCall &c, cudaStream_t s);
 // Routing of many tokens from the prepared activations (same logits, bit for bit).
-cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float *xsc, const float *XG,
+// QF: route_f32_bytes(D, E) of workspace for the router's bytes as floats.
+size_t route_f32_bytes(int D, int E);
+cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float *xsc, const float *XG, float *QF,
                                cudaStream_t s);
 
 // Stage profiler (mx_moe_profile_*): event pair around one launch.

@@ -859,6 +859,7 @@ struct PfBufs {
     float *xsc, *XG;
     __half *X16, *Xr, *H, *Hs;
     float *Y, *Ys;
+    float *QF;
     size_t total;
 };
 
@@ -883,6 +884,7 @@ PfBufs pf_carve(uint8_t *w, int T, int D, int I, int S, int E, int K)
     b.Hs = reinterpret_cast<__half *>(take((size_t)T * S * 2));
     b.Y = reinterpret_cast<float *>(take(TK * D * 4));
     b.Ys = reinterpret_cast<float *>(take((size_t)T * D * 4));
+    b.QF = reinterpret_cast<float *>(take(route_f32_bytes(D, E)));
     b.total = (size_t)(p - w);
     return b;
 }
@@ -914,6 +916,7 @@ cudaError_t launch_prefill_prepare(const PfCall &c, PfPrepared *out, cudaStream_
     out->X16 = b.X16;
     out->xsc = b.xsc;
     out->XG = b.XG;
+    out->QF = b.QF;
     return cudaGetLastError();
 }
 

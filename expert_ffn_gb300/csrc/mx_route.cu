@@ -151,13 +151,24 @@ __device__ void group_slots_nw(const RouteArgs &a, float *sm)
     __syncthreads();
     const int chunk = (n + NW - 1) / NW;
     const int lo = min(n, warp * chunk), hi = min(n, lo + chunk);
-    for (int s0 = lo; s0 < hi; s0 += 32) {
-        const int s = s0 + lane;
-        const int e = (s < hi) ? __ldcg(a.topk_idx + s) : -1;
-        const unsigned m = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(m) - 1)
-            wc[warp * E + e] += __popc(m);
-        __syncwarp();
+    // eight 32-slot rows of the warp's range in flight at a time, then counted
+    // in order
+    constexpr int kB = 8;
+    for (int s0 = lo; s0 < hi; s0 += 32 * kB) {
+        int ev[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const int s = s0 + 32 * j + lane;
+            ev[j] = (s < hi) ? __ldcg(a.topk_idx + s) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const int e = ev[j];
+            const unsigned m = __match_any_sync(0xffffffffu, e);
+            if (e >= 0 && lane == __ffs(m) - 1)
+                wc[warp * E + e] += __popc(m);
+            __syncwarp();
+        }
     }
     __syncthreads();
     for (int e = threadIdx.x; e < E; e += (32 * NW)) {
@@ -204,16 +215,24 @@ __device__ void group_slots_nw(const RouteArgs &a, float *sm)
     }
     __syncthreads();
     const unsigned lt = (1u << lane) - 1u;
-    for (int s0 = lo; s0 < hi; s0 += 32) {
-        const int s = s0 + lane;
-        const int e = (s < hi) ? __ldcg(a.topk_idx + s) : -1;
-        const unsigned m = __match_any_sync(0xffffffffu, e);
-        if (e >= 0)
-            a.perm[off[e] + base[warp * E + e] + __popc(m & lt)] = s;
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(m) - 1)
-            base[warp * E + e] += __popc(m);
-        __syncwarp();
+    for (int s0 = lo; s0 < hi; s0 += 32 * kB) {
+        int ev[kB];
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const int s = s0 + 32 * j + lane;
+            ev[j] = (s < hi) ? __ldcg(a.topk_idx + s) : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < kB; ++j) {
+            const int s = s0 + 32 * j + lane, e = ev[j];
+            const unsigned m = __match_any_sync(0xffffffffu, e);
+            if (e >= 0)
+                a.perm[off[e] + base[warp * E + e] + __popc(m & lt)] = s;
+            __syncwarp();
+            if (e >= 0 && lane == __ffs(m) - 1)
+                base[warp * E + e] += __popc(m);
+            __syncwarp();
+        }
     }
     if (a.tiles) {
         for (int e = threadIdx.x; e < E; e += (32 * NW)) {
@@ -550,19 +569,34 @@ cudaError_t launch_tt(const RouteArgs &a, const RouteLaunch &L, cudaStream_t s)
 
 constexpr int kLE = 64;  // experts per block
 
+// The router's bytes as floats, once per call: QF[(g * 64 + c) * Ep + e] =
+// q[e][64 g + c] (Ep = E rounded up to 64, zero padding), so a block's 64 x 64
+// tile of one group is 64 rows of 256 contiguous bytes.
+__global__ void __launch_bounds__(256) router_to_f32(const uint32_t *__restrict__ rw, int E, int Ep, int D,
+                                                     float *__restrict__ QF)
+{
+    const int wi = blockIdx.x, e = blockIdx.y * 256 + threadIdx.x;  // packed word column, expert
+    if (e >= Ep)
+        return;
+    const uint32_t w = e < E ? __ldg(rw + (size_t)e * (D / 4) + wi) : 0u;
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+        QF[(size_t)(4 * wi + b) * Ep + e] = (float)((w >> (8 * b)) & 0xFFu);
+}
+
 // Block of TT tokens x 64 experts; TT/4 x 16 threads, 4 x 4 accumulators each.
-// The next group's activations and router bytes are loaded into registers
+// The next group's activations and router floats are loaded into registers
 // while the current group is multiplied.
 template <int TT>
 __global__ void __launch_bounds__(TT * 4) logits_gemm(const __half *__restrict__ X16, const float *__restrict__ xsc,
-                                                       const float *__restrict__ XG, const uint32_t *__restrict__ rw,
+                                                       const float *__restrict__ XG, const float *__restrict__ QF,
                                                        const uint16_t *__restrict__ rs, const uint16_t *__restrict__ rb,
-                                                       int T, int D, int E, float *__restrict__ logits)
+                                                       int T, int D, int E, int Ep, float *__restrict__ logits)
 {
     constexpr int NT = TT * 4;               // threads
     constexpr int XV = TT * 8 / NT;          // 16-byte activation vectors per thread per group (= 2)
-    constexpr int QV = kLE * 4 / NT;         // 16-byte router vectors per thread per group
-    static_assert(XV * NT == TT * 8 && QV * NT == kLE * 4, "tile shape");
+    constexpr int QV = 64 * kLE / 4 / NT;    // 16-byte router vectors per thread per group
+    static_assert(XV * NT == TT * 8 && QV * NT * 4 == 64 * kLE, "tile shape");
     __shared__ __align__(16) float xs[64][TT];   // [column][token]
     __shared__ __align__(16) float qs[64][kLE];  // [column][expert]
     __shared__ float sS[kLE], sB[kLE], sX[TT];
@@ -570,19 +604,20 @@ __global__ void __launch_bounds__(TT * 4) logits_gemm(const __half *__restrict__
     const int t0 = blockIdx.y * TT, e0 = blockIdx.x * kLE, G = D / 64;
     uint4 xr[XV], qr[QV];
     float xscale[XV];
+    // activations: vector v of thread tid is 8-column chunk ch of token t, with
+    // consecutive threads on consecutive tokens (conflict-free stores below)
     auto fetch = [&](int g) {
 #pragma unroll
         for (int v = 0; v < XV; ++v) {
-            const int i = tid + v * NT, t = i >> 3, ch = i & 7, tt = t0 + t;
+            const int i = tid + v * NT, t = i % TT, ch = i / TT, tt = t0 + t;
             xr[v] = tt < T ? __ldg(reinterpret_cast<const uint4 *>(X16 + (size_t)tt * D + 64 * g) + ch)
                            : make_uint4(0, 0, 0, 0);
             xscale[v] = tt < T ? __ldg(xsc + tt) : 0.f;
         }
 #pragma unroll
         for (int v = 0; v < QV; ++v) {
-            const int i = tid + v * NT, e = i >> 2, w4 = i & 3, ee = e0 + e;
-            qr[v] = ee < E ? __ldg(reinterpret_cast<const uint4 *>(rw + (size_t)ee * (D / 4) + 16 * g) + w4)
-                           : make_uint4(0, 0, 0, 0);
+            const int i = tid + v * NT, c = i >> 4, e4 = i & 15;
+            qr[v] = __ldg(reinterpret_cast<const uint4 *>(QF + (size_t)(64 * g + c) * Ep + e0) + e4);
         }
     };
     float acc[4][4];
@@ -594,11 +629,10 @@ __global__ void __launch_bounds__(TT * 4) logits_gemm(const __half *__restrict__
     fetch(0);
     for (int g = 0; g < G; ++g) {
         // registers -> shared: activations back in column order (operand
-        // position p of an 8-block holds column [0,4,1,5,2,6,3,7][p]), router
-        // bytes as floats
+        // position p of an 8-block holds column [0,4,1,5,2,6,3,7][p])
 #pragma unroll
         for (int v = 0; v < XV; ++v) {
-            const int i = tid + v * NT, t = i >> 3, ch = i & 7;
+            const int i = tid + v * NT, t = i % TT, ch = i / TT;
             const uint32_t u[4] = {xr[v].x, xr[v].y, xr[v].z, xr[v].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -610,16 +644,8 @@ __global__ void __launch_bounds__(TT * 4) logits_gemm(const __half *__restrict__
         }
 #pragma unroll
         for (int v = 0; v < QV; ++v) {
-            const int i = tid + v * NT, e = i >> 2, w4 = i & 3;
-            const uint32_t u[4] = {qr[v].x, qr[v].y, qr[v].z, qr[v].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int c = 16 * w4 + 4 * j;
-                qs[c][e] = (float)(u[j] & 0xFFu);
-                qs[c + 1][e] = (float)((u[j] >> 8) & 0xFFu);
-                qs[c + 2][e] = (float)((u[j] >> 16) & 0xFFu);
-                qs[c + 3][e] = (float)(u[j] >> 24);
-            }
+            const int i = tid + v * NT, c = i >> 4, e4 = i & 15;
+            *reinterpret_cast<uint4 *>(&qs[c][4 * e4]) = qr[v];
         }
         if (tid < kLE) {
             const int ee = e0 + tid;
@@ -760,18 +786,25 @@ cudaError_t launch_route(const RouteArgs &a, const RouteLaunch &L, cudaStream_t 
     }
 }
 
-cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float *xsc, const float *XG, cudaStream_t s)
+size_t route_f32_bytes(int D, int E) { return (size_t)D * ((E + kLE - 1) / kLE * kLE) * sizeof(float); }
+
+cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float *xsc, const float *XG, float *QF,
+                               cudaStream_t s)
 {
-    // 64-token blocks when they fill the GPU twice over, else 32-token blocks
-    const int ne = (a.E + kLE - 1) / kLE;
-    if ((long long)ne * ((a.T + 63) / 64) >= 2 * 152) {
-        logits_gemm<64><<<dim3(ne, (a.T + 63) / 64), 256, 0, s>>>(static_cast<const __half *>(X16), xsc, XG, a.rw,
-                                                                    a.rs, a.rb, a.T, a.D, a.E, a.logits);
-    } else {
-        logits_gemm<32><<<dim3(ne, (a.T + 31) / 32), 128, 0, s>>>(static_cast<const __half *>(X16), xsc, XG, a.rw,
-                                                                    a.rs, a.rb, a.T, a.D, a.E, a.logits);
-    }
+    const int ne = (a.E + kLE - 1) / kLE, Ep = ne * kLE;
+    router_to_f32<<<dim3(a.D / 4, (Ep + 255) / 256), 256, 0, s>>>(a.rw, a.E, Ep, a.D, QF);
     cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    // 64-token blocks when they fill the GPU twice over, else 32-token blocks
+    if ((long long)ne * ((a.T + 63) / 64) >= 2 * 152) {
+        logits_gemm<64><<<dim3(ne, (a.T + 63) / 64), 256, 0, s>>>(static_cast<const __half *>(X16), xsc, XG, QF,
+                                                                    a.rs, a.rb, a.T, a.D, a.E, Ep, a.logits);
+    } else {
+        logits_gemm<32><<<dim3(ne, (a.T + 31) / 32), 128, 0, s>>>(static_cast<const __half *>(X16), xsc, XG, QF,
+                                                                    a.rs, a.rb, a.T, a.D, a.E, Ep, a.logits);
+    }
+    e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
     const size_t topk_smem = ((size_t)kWarps * a.E + (size_t)kWarps * ((a.E + 31) / 32)) * sizeof(float);
