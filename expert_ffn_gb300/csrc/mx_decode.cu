@@ -328,9 +328,31 @@ __device__ __forceinline__ void red_add(int *c, int v)
 // order in which CTAs arrive.
 constexpr float kFix = 4294967296.0f;         // 2^32
 constexpr float kUnfix = 2.3283064365386963e-10f;  // 2^-32
+// round(v * 2^32) as a 64-bit integer with 32-bit conversions (64-bit ones are
+// slow here).  For a = |v|: a = h + f with h = floor(a) an integer and f in
+// [0, 1), both exact, and h * 2^32 even, so round(a 2^32) = h 2^32 +
+// round(f 2^32) (below 2^32); round to nearest even is odd-symmetric.  Exact
+// for |v| < 2^31.
+__device__ __forceinline__ long long to_fix(float v)
+{
+    const float a = fabsf(v), h = floorf(a);
+    const long long m = (long long)(((unsigned long long)__float2uint_rn(h) << 32) |
+                                    (unsigned long long)__float2uint_rn((a - h) * kFix));
+    return v < 0.f ? -m : m;
+}
+
+// The fixed-point sum back as a float: hi + lo 2^-32 (|hi| < 2^24 is exact;
+// within 2 ulp of the exact value, and the same bits on every call).
+__device__ __forceinline__ float from_fix(long long q)
+{
+    const int hi = (int)(q >> 32);
+    const unsigned lo = (unsigned)(q & 0xffffffffll);
+    return (float)hi + __uint2float_rn(lo) * kUnfix;
+}
+
 __device__ __forceinline__ void red_fix(long long *y, float v)
 {
-    const long long q = __float2ll_rn(v * kFix);
+    const long long q = to_fix(v);
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(y), "l"(q) : "memory");
 }
 
@@ -571,10 +593,12 @@ __device__ void prologue(const PdParams &p, const Smem &s)
                 reinterpret_cast<float4 *>(s.xq)[2 * i] = make_float4(v[0], v[1], v[2], v[3]);
                 reinterpret_cast<float4 *>(s.xq)[2 * i + 1] = make_float4(v[4], v[5], v[6], v[7]);
             }
-            // one token per warp-aligned run when D is a multiple of 256 values;
-            // otherwise lanes of a warp may hold two tokens: reduce per lane
-            if (mx > 0.f)
-                atomicMax(&s.vmax[t], __float_as_int(mx));
+            // one shared-memory atomic per token present in the warp (lanes of
+            // a warp hold two tokens when D is not a multiple of 256 values)
+            const unsigned am = __activemask(), m = __match_any_sync(am, t);
+            const int wmx = __reduce_max_sync(m, __float_as_int(mx));
+            if (wmx > 0 && lane == __ffs(m) - 1)
+                atomicMax(&s.vmax[t], wmx);
         }
         (void)lane;
     }
@@ -731,9 +755,16 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
         const int t = i / E, e = i - t * E;
         const float *row = s.lg + t * E;
         const float v = row[e];
-        int rank = 0;
-#pragma unroll 8
-        for (int j = 0; j < E; ++j) {
+        int rank = 0, j = 0;
+        if ((E & 3) == 0) {  // rows 16-byte aligned: four logits per load
+#pragma unroll 4
+            for (; j < E; j += 4) {
+                const float4 u = *reinterpret_cast<const float4 *>(row + j);
+                rank += ((u.x > v) || (u.x == v && j < e)) + ((u.y > v) || (u.y == v && j + 1 < e)) +
+                        ((u.z > v) || (u.z == v && j + 2 < e)) + ((u.w > v) || (u.w == v && j + 3 < e));
+            }
+        }
+        for (; j < E; ++j) {
             const float u = row[j];
             rank += (u > v) || (u == v && j < e);
         }
@@ -743,8 +774,10 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
         }
     }
     csync();
-    if (tid < T) {
-        float *w = rt.slot_w + tid * K;
+    // softmax on warp 1 (lane = token) while warp 0 groups the slots
+    if (warp == 1 && lane < T) {
+        const int t = lane;
+        float *w = rt.slot_w + t * K;
         const float m = w[0];
         float sum = 0.f;
         for (int k = 0; k < K; ++k) {
@@ -754,11 +787,11 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
         for (int k = 0; k < K; ++k) {
             float x = w[k] / sum;
             if (L.pes)
-                x = x * __ldg(L.pes + rt.slot_e[tid * K + k]);
+                x = x * __ldg(L.pes + rt.slot_e[t * K + k]);
             w[k] = x;
             if (blockIdx.x == 0) {
-                L.topk_idx[tid * K + k] = rt.slot_e[tid * K + k];
-                L.topk_w[tid * K + k] = x;
+                L.topk_idx[t * K + k] = rt.slot_e[t * K + k];
+                L.topk_w[t * K + k] = x;
             }
         }
     }
@@ -766,9 +799,6 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
         if (lane < 16)
             rt.emask[lane] = 0u;
         __syncwarp();
-    }
-    csync();
-    if (warp == 0) {
         const int nw = (E + 31) >> 5;
         for (int i = lane; i < T * K; i += 32) {
             const int e = rt.slot_e[i];
@@ -1134,19 +1164,22 @@ __device__ void consumers(const PdParams &p, const Smem &s)
         if (!(ok = cwait(ctr + 2, NC, p, s)))
             break;
         PD_STAMP(l, 10);
-        for (int i0 = 0; i0 < T * D; i0 += 4 * kCT) {
-            long long yq[4];
+        // y from L2: twelve loads per thread in flight at a time (all of y at
+        // d_model <= 3072, T = 1)
+        constexpr int kYB = NB == 1 ? 12 : 6;
+        for (int i0 = 0; i0 < T * D; i0 += kYB * kCT) {
+            long long yq[kYB];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kYB; ++j) {
                 const int i = i0 + tid + j * kCT;
                 yq[j] = i < T * D ? __ldcg(y + i) : 0;
             }
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < kYB; ++j) {
             const int i = i0 + tid + j * kCT;
             if (i >= T * D)
                 break;
-            const float yv = __ll2float_rn(yq[j]) * kUnfix;
+            const float yv = from_fix(yq[j]);
             float res = 0.f;
             if (L.res_mode == 1)
                 res = es == 2 ? bf2f(reinterpret_cast<const uint16_t *>(s.xraw)[i])
