@@ -19,23 +19,23 @@
 // shared memory and rebuilds x_{l+1} from the summed down projections, so
 // layers hand over without another exchange.
 //
-// CTA: 8 consumer warps + 1 producer warp.  The producer streams work items
-// into two rings of shared memory with TMA tensor copies (one copy per block of
-// rows, group-major, see mx_tma.cu) plus bulk copies of the rows' BF16 scales
-// and biases:
-//   ring L  gate/up items: 8 gate + 8 up rows x D (the 16 rows of one MMA tile,
-//           so gelu(g) * u is lane-local); split over the 8 consumer warps;
-//   ring S  down items: 16 rows x one K chunk (shared expert) or x I (routed);
-//           one consumer warp per item.
-// Per layer, each list split over all CTAs in contiguous ranges:
-//   A1  shared gate/up     S/8 items           -> hs = gelu(gate x) * (up x)
-//   SD  shared down        D/16 x K chunks     -> y
-//   B   routed gate/up     n_active * I/8      -> h_slot = w_slot gelu(g) * u
-//   RD  routed down        D/16 x n_active     -> y
-// and the router rows (E rows, round-robin).  Down items add their partial
-// sums into y in 64-bit fixed point, whose integer addition does not depend on
-// the order, so the result is deterministic; every CTA then forms
-// x_{l+1} = residual + lambda * y.
+// CTA: 8 consumer warps + 1 producer warp.  Work comes in units of 64 hidden
+// rows of one expert: rows [64u, 64u + 64) of the shared expert (S/64 units)
+// or of an active routed expert (I/64 units each); unit i runs on CTA i mod
+// the grid, shared units first (they start before the routing is known).
+// The producer streams a unit's 12 items into one ring of shared memory with
+// TMA tensor copies (group-major, see mx_tma.cu) and bulk copies of the rows'
+// BF16 scales and biases:
+//   8 gate/up items: 8 gate + 8 up rows x D (the 16 rows of one MMA tile, so
+//     gelu(g) * u is lane-local), one per consumer warp;
+//   4 down items: D/4 rows x the unit's 64 columns, row tiles over all warps.
+// A unit keeps its 64 hidden values on chip and adds its slice of the down
+// projection, for all D outputs, into y in 64-bit fixed point, whose integer
+// addition does not depend on the order, so the result is deterministic; every
+// CTA then forms x_{l+1} = residual + lambda * y.  Each CTA also computes one
+// router row per E / grid of the layer (round-robin), in the fixed order
+// below; the logits and y are the only grid-wide exchanges of a layer.
+//
 //
 // Math: legacy warp MMA m16n8k32 with FP8 (e4m3) operands and fp32
 // accumulation.  A raw nibble byte n (0..15) is exactly the e4m3 number
