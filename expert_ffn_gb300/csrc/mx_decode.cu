@@ -434,37 +434,42 @@ __device__ __forceinline__ void gu_item(const uint8_t *st, int G, const uint8_t 
     accu = fo * ((pu[0] + pu[1]) + (pu[2] + pu[3])) + ((qu[0] + qu[1]) + (qu[2] + qu[3]));
 }
 
-// Down item: 16 rows x G groups, one warp.  tile [G][16][32 B]; s, b: the
-// rows' BF16 scales and biases with row pitch `pitch` (already offset to the
-// item's first group).  Lane output: rows gid (a0) and gid + 8 (a8), column
-// slot c.  B: 2 plane pairs; bgs/bms/bnbs: strides of group, k-step, pair.
-__device__ __forceinline__ void dn_math(const uint8_t *tile, const uint16_t *s, const uint16_t *b, int pitch, int G,
-                                        const uint8_t *bp, int bgs, int bms, int bnbs, float fo, const float *xgo,
-                                        float &a0, float &a8)
+// One 16-row x 64-column tile of a unit's down slice (one group), one warp;
+// t0: this lane's bytes of the tile (tile + gid * 32 + c * 8); sb0 / sb8: the
+// BF16 scale (low half) and bias (high half) of rows gid and gid + 8.  hb: the
+// B operands of the unit's hidden planes, the same for every tile.
+//   ONE: at most 2 hidden vectors, their 4 planes in the 8 columns of one MMA
+//        (column 4v + p); hb[0], hb[1]: the two k-steps; the plane columns of
+//        vector v sit in lanes c = 2v and 2v + 1 and are added across them.
+//   else: 2 plane pairs in 2 MMAs per k-step; hb = {pair 0 k0, pair 0 k1,
+//        pair 1 k0, pair 1 k1}; column 2v + pp.
+template <bool ONE>
+__device__ __forceinline__ void dn_tile(const uint8_t *t0, const uint2 (&hb)[4], uint32_t sb0, uint32_t sb8,
+                                        float fo, float X, float &a0, float &a8)
 {
-    const int lane = threadIdx.x & 31, gid = lane >> 2, c = lane & 3;
-    const uint8_t *t0 = tile + gid * 32 + c * 8;
-    const uint16_t *s0 = s + gid * pitch, *s8 = s + (gid + 8) * pitch, *b0 = b + gid * pitch,
-                   *b8 = b + (gid + 8) * pitch;
-#pragma unroll 2
-    for (int g = 0; g < G; ++g) {
-        const uint2 q0 = lds64(t0 + 512 * g), q8 = lds64(t0 + 512 * g + 256);
-        const uint32_t l0 = q0.x & kLo, l8 = q8.x & kLo, h0 = (q0.x >> 4) & kLo, h8 = (q8.x >> 4) & kLo;
-        const uint32_t m0 = q0.y & kLo, m8 = q8.y & kLo, k0 = (q0.y >> 4) & kLo, k8 = (q8.y >> 4) & kLo;
-        const uint8_t *bg = bp + g * bgs;
+    const uint2 q0 = lds64(t0), q8 = lds64(t0 + 256);
+    const uint32_t l0 = q0.x & kLo, l8 = q8.x & kLo, h0 = (q0.x >> 4) & kLo, h8 = (q8.x >> 4) & kLo;
+    const uint32_t m0 = q0.y & kLo, m8 = q8.y & kLo, k0 = (q0.y >> 4) & kLo, k8 = (q8.y >> 4) & kLo;
+    float R0, R8;
+    if constexpr (ONE) {
+        float d[4] = {0.f, 0.f, 0.f, 0.f}, f[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_fp8(d, l0, l8, h0, h8, hb[0].x, hb[0].y);
+        mma_fp8(f, m0, m8, k0, k8, hb[1].x, hb[1].y);
+        R0 = (d[0] + d[1]) + (f[0] + f[1]);
+        R8 = (d[2] + d[3]) + (f[2] + f[3]);
+        R0 += __shfl_xor_sync(0xffffffffu, R0, 1);
+        R8 += __shfl_xor_sync(0xffffffffu, R8, 1);
+    } else {
         float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint2 v0 = lds64(bg), v1 = lds64(bg + bms), w0 = lds64(bg + bnbs), w1 = lds64(bg + bms + bnbs);
-        mma_fp8(d, l0, l8, h0, h8, v0.x, v0.y);
-        mma_fp8(e, l0, l8, h0, h8, w0.x, w0.y);
-        mma_fp8(d, m0, m8, k0, k8, v1.x, v1.y);
-        mma_fp8(e, m0, m8, k0, k8, w1.x, w1.y);
-        const float R0 = (d[0] + d[1]) + (e[0] + e[1]), R8 = (d[2] + d[3]) + (e[2] + e[3]);
-        const float X = xgo[g];
-        a0 = fmaf(bf2f(s0[g]), R0 * fo, a0);
-        a0 = fmaf(bf2f(b0[g]), X, a0);
-        a8 = fmaf(bf2f(s8[g]), R8 * fo, a8);
-        a8 = fmaf(bf2f(b8[g]), X, a8);
+        mma_fp8(d, l0, l8, h0, h8, hb[0].x, hb[0].y);
+        mma_fp8(e, l0, l8, h0, h8, hb[2].x, hb[2].y);
+        mma_fp8(d, m0, m8, k0, k8, hb[1].x, hb[1].y);
+        mma_fp8(e, m0, m8, k0, k8, hb[3].x, hb[3].y);
+        R0 = (d[0] + d[1]) + (e[0] + e[1]);
+        R8 = (d[2] + d[3]) + (e[2] + e[3]);
     }
+    a0 = fmaf(bf2f((uint16_t)(sb0 >> 16)), X, bf2f((uint16_t)sb0) * (R0 * fo));
+    a8 = fmaf(bf2f((uint16_t)(sb8 >> 16)), X, bf2f((uint16_t)sb8) * (R8 * fo));
 }
 
 // ----------------------------------------------------------- plane builders
@@ -1006,6 +1011,9 @@ __device__ void consumers(const PdParams &p, const Smem &s)
         // for all D outputs, added into y.  No hidden vector leaves the CTA.
         auto unit = [&](bool shared, int j, int u) -> bool {
             const int ne = shared ? T : s.rt.act_n[j];
+            // phase trace: the stamps inside a unit cover the CTA's first routed unit
+            const bool tr_first = !shared && (j * GI + u) == first_routed(C, NC, GS);
+            (void)tr_first;
             bool good = true;
             // the down slice's scales and biases (column u of the [D][G]
             // tables; 16-bit elements at a row pitch TMA cannot take): loaded
@@ -1072,27 +1080,53 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             }
             if (!(good = csync_and(good)))
                 return false;
+            if (tr_first)
+                PD_STAMP(l, 6);
             if (warp == 0)
                 unit_planes(s.uh, ne, s.upl, s.ux, s.ufo);
             csync();
+            if (tr_first)
+                PD_STAMP(l, 7);
             // down: items k + 8 .. k + 11, D/4 rows each; warp w takes row
             // tiles w, w + 8, ... of every item
             const bool bvalid = (gid >> 1) < ne;
             const uint8_t *bp = bvalid ? s.upl + (gid >> 1) * 256 + (gid & 1) * 32 + c * 8 : s.zero;
-            const int ot = c < ne ? (shared ? c : s.rt.act_slot[4 * j + c] / K) : 0;
-            const int oc = c < ne ? c : 0;
+            // With at most 2 hidden vectors their 4 planes fill the 8 columns of
+            // one MMA: half the MMAs and B operands per tile.
+            const bool one = ne <= 2;
+            uint2 hb[4] = {};
+            int oc;   // this lane's hidden vector
+            bool out; // whether this lane adds its rows into y
+            if (one) {
+                const int v = gid >> 2, pl = gid & 3;
+                if (v < ne) {
+                    const uint8_t *b1p = s.upl + v * 256 + (pl >> 1) * 64 + (pl & 1) * 32 + c * 8;
+                    hb[0] = lds64(b1p);
+                    hb[1] = lds64(b1p + 128);
+                }
+                oc = (c >> 1) < ne ? (c >> 1) : 0;
+                out = (c & 1) == 0 && (c >> 1) < ne;
+            } else {
+                hb[0] = lds64(bp);
+                hb[1] = lds64(bp + (bvalid ? 128 : 0));
+                hb[2] = lds64(bp + (bvalid ? 64 : 0));
+                hb[3] = lds64(bp + (bvalid ? 192 : 0));
+                oc = c < ne ? c : 0;
+                out = c < ne;
+            }
+            const int ot = shared ? oc : s.rt.act_slot[4 * j + oc] / K;  // this lane's token
+            const float hfo = s.ufo[oc], hX = s.ux[oc];
+            long long *yv = y + (size_t)ot * D;
             for (int q = 0; q < 4; ++q) {
-                // this item's scales and biases into buffer q & 1 (the barrier
-                // also tells that every warp is done with item q - 1, so buffer
-                // q & 1, last read for item q - 2, is free)
-                uint16_t *isv = s.dss + (q & 1) * 2 * R4, *ibv = isv + R4;
+                // this item's (scale | bias << 16) words into buffer q & 1 (the
+                // barrier also tells that every warp is done with item q - 1, so
+                // buffer q & 1, last read for item q - 2, is free)
+                uint32_t *isb = reinterpret_cast<uint32_t *>(s.dss) + (q & 1) * R4;
 #pragma unroll
                 for (int i = 0; i < kR; ++i) {
                     const int r = tid + i * kCT - q * R4;
-                    if (r >= 0 && r < R4) {
-                        isv[r] = (uint16_t)sbv[i];
-                        ibv[r] = (uint16_t)(sbv[i] >> 16);
-                    }
+                    if (r >= 0 && r < R4)
+                        isb[r] = sbv[i];
                 }
                 csync();
                 const int kk = k + 8 + q, sl = kk % o.NR;
@@ -1100,29 +1134,36 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                     good = false;
                     continue;
                 }
-                const uint8_t *tile = s.ring + (size_t)sl * o.slot;
+                if (tr_first)
+                    PD_STAMP(l, 12 + q);
+                const uint8_t *tile = s.ring + (size_t)sl * o.slot + gid * 32 + c * 8;
                 const int nrt = R4 / 16;
                 for (int rt = warp; rt < nrt; rt += 2 * kCW) {
                     // two row tiles at a time (the second repeats the first past the end)
                     const int rt2 = rt + kCW < nrt ? rt + kCW : rt;
-                    float a0 = 0.f, a8 = 0.f, b0 = 0.f, b8 = 0.f;
-                    dn_math(tile + rt * 512, isv + 16 * rt, ibv + 16 * rt, 1, 1, bp, 256, bvalid ? 128 : 0,
-                            bvalid ? 64 : 0, s.ufo[oc], s.ux + oc, a0, a8);
-                    dn_math(tile + rt2 * 512, isv + 16 * rt2, ibv + 16 * rt2, 1, 1, bp, 256, bvalid ? 128 : 0,
-                            bvalid ? 64 : 0, s.ufo[oc], s.ux + oc, b0, b8);
-                    if (c < ne) {
-                        const int r0 = q * R4 + 16 * rt, r2 = q * R4 + 16 * rt2;
-                        red_fix(y + (size_t)ot * D + r0 + gid, a0);
-                        red_fix(y + (size_t)ot * D + r0 + gid + 8, a8);
+                    const int r0 = 16 * rt + gid, r2 = 16 * rt2 + gid;
+                    float a0, a8, b0, b8;
+                    if (one) {
+                        dn_tile<true>(tile + rt * 512, hb, isb[r0], isb[r0 + 8], hfo, hX, a0, a8);
+                        dn_tile<true>(tile + rt2 * 512, hb, isb[r2], isb[r2 + 8], hfo, hX, b0, b8);
+                    } else {
+                        dn_tile<false>(tile + rt * 512, hb, isb[r0], isb[r0 + 8], hfo, hX, a0, a8);
+                        dn_tile<false>(tile + rt2 * 512, hb, isb[r2], isb[r2 + 8], hfo, hX, b0, b8);
+                    }
+                    if (out) {
+                        red_fix(yv + q * R4 + r0, a0);
+                        red_fix(yv + q * R4 + r0 + 8, a8);
                         if (rt2 != rt) {
-                            red_fix(y + (size_t)ot * D + r2 + gid, b0);
-                            red_fix(y + (size_t)ot * D + r2 + gid + 8, b8);
+                            red_fix(yv + q * R4 + r2, b0);
+                            red_fix(yv + q * R4 + r2 + 8, b8);
                         }
                     }
                 }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&s.empty[sl]);
+                if (tr_first)
+                    PD_STAMP(l, 16 + q);
             }
             k += 12;
             return csync_and(good);

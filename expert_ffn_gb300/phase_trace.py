@@ -13,7 +13,10 @@ Phases, in kernel order: start of the layer, prologue (RMSNorm, planes of x),
 router rows, the shared-expert units, the logit exchange, top-k / softmax /
 grouping, the routed units, the y exchange, the rebuild of x_{l+1}.  CTAs
 without shared units pass the shared-unit phase at once, and CTAs without
-routed units the routed one.
+routed units the routed one.  Indented rows time the inside of each CTA's
+first routed unit (over the CTAs that hold one): the end of its gate/up work,
+of the planes of h, and when each of its four down items had landed in shared
+memory and was done.
 """
 from __future__ import annotations
 
@@ -23,7 +26,10 @@ import os
 import sys
 
 PHASES = ["layer start", "prologue", "router rows", "shared units", "logit exchange", "top-k + grouping",
-          None, None, None, "routed units", "y exchange", "x rebuild"]
+          "  unit gate/up", "  unit h planes", None, "routed units", "y exchange", "x rebuild",
+          "  down 0 landed", "  down 1 landed", "  down 2 landed", "  down 3 landed",
+          "  down 0 done", "  down 1 done", "  down 2 done", "  down 3 done"]
+UNIT_PHASES = range(6, 20)  # inside the first routed unit of a CTA (CTAs that hold one)
 TRACE_LAYER, TRACE_CTAS, TRACE_PTS = 10, 160, 24
 
 
@@ -86,7 +92,10 @@ def main(argv=None) -> int:
         stamps = buf[:ncta].astype(np.int64)
         t0 = stamps[:, 0].min()
         for i in rows:
-            v = (stamps[:, i] - t0) / 1e3
+            col = stamps[:, i]
+            if i in UNIT_PHASES:
+                col = col[col != 0]  # CTAs that ran a routed unit
+            v = (col - t0) / 1e3
             rows[i].append((np.median(v), v.min(), v.max()))
     print(f"single-launch decode, d_model {cfg.D}, {cfg.E} experts top-{cfg.K}, T={T}, {cfg.layers} layers: "
           f"layer {TRACE_LAYER}, {ncta} CTAs, median of {args.runs} launches (us)")
