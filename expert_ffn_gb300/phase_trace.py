@@ -100,8 +100,9 @@ def main(argv=None) -> int:
     print(f"single-launch decode, d_model {cfg.D}, {cfg.E} experts top-{cfg.K}, T={T}, {cfg.layers} layers: "
           f"layer {TRACE_LAYER}, {ncta} CTAs, median of {args.runs} launches (us)")
     print(f"{'phase ends':18s} {'median CTA':>10s} {'fastest':>9s} {'slowest':>9s}")
-    for i, r in rows.items():
-        a = np.median(np.array(r), axis=0)
+    order = [0, 1, 2, 3, 4, 5, 6, 7, 12, 16, 13, 17, 14, 18, 15, 19, 9, 10, 11]  # kernel order
+    for i in order:
+        a = np.median(np.array(rows[i]), axis=0)
         print(f"{PHASES[i]:18s} {a[0]:10.2f} {a[1]:9.2f} {a[2]:9.2f}")
     return 0
 
