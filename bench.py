@@ -142,6 +142,23 @@ def dist_setup(args):
     return world, rank, local, pg
 
 
+def max_over_ranks(ms: float, pg, device: str) -> float:
+    """The slowest rank's time: every rank's replica ran the same work, so the
+    job took as long as its slowest rank (identity without a process group)."""
+    if pg is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, steps: int, tokens_per_step: float, ms: float) -> float:
+    """Whole-job throughput: every rank processed steps x tokens_per_step
+    tokens (independent replicas, weak scaling) in at most ms milliseconds."""
+    return world * steps * tokens_per_step / (ms / 1e3)
+
+
 # ----------------------------------------------------------- workload bytes
 
 def qbytes(rows, cols, bits):
@@ -242,14 +259,10 @@ def bench_ours(args, cfg, world, rank, local, pg):
         torch.cuda.synchronize()
         tw1 = time.time()
     barrier()
-    ms = ev0.elapsed_time(ev1)
-    if pg is not None:
-        t = torch.tensor([ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, "cuda")
     clocks = clk.summary(tw0, tw1)
     ms_per_step = ms / args.steps
-    value = world * args.steps * T / (ms / 1e3)
+    value = job_tokens_per_s(world, args.steps, T, ms)
 
     # stage timing (events on the launching stream, direct API calls)
     mx.profile_enable(True)
@@ -294,11 +307,7 @@ def bench_ours(args, cfg, world, rank, local, pg):
             e2e_step(stream)
         e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if pg is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, "cuda")
     es = x_init.element_size()
     h2d = T * D * es
     d2h = T * D * es + n_layers * T * K * 8
@@ -357,7 +366,7 @@ def bench_ours(args, cfg, world, rank, local, pg):
         "stage_us": stages_us,
         "roofline": roof,
         "clocks": clocks,
-        "e2e": {"value": round(world * args.steps * T / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(world, args.steps, T, e2e_ms), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host input copied in, the C-ABI call (no graph), outputs copied out, every step"},
         "gpu_launches": args.steps * launches,
