@@ -145,8 +145,9 @@ void oracle_router_logits(const oracle_qmat *router, const float *x, int T, floa
 
 /* highest_K then softmax(logits[topK]) * per_expert_scale[topK]
  * [Mference, "Decode", router formula].  Order: descending logit, ties to the
- * lower expert index (lowest-index-wins); NaN ranks as -inf.  The softmax is
- * taken over the K selected logits, shifted by the largest, in fp32. */
+ * lower expert index (lowest-index-wins); NaN ranks as -inf, and enters the
+ * softmax as -inf.  The softmax is taken over the K selected logits, shifted
+ * by the largest, in fp32. */
 int oracle_topk_softmax(const float *logits, int T, int E, int K,
                         const float *per_expert_scale, int32_t *topk_idx, float *topk_w)
 {
@@ -172,10 +173,14 @@ int oracle_topk_softmax(const float *logits, int T, int E, int K,
             taken[best] = 1;
             topk_idx[(long)t * K + k] = best;
         }
-        float m = l[topk_idx[(long)t * K]];
+        /* a NaN logit is -inf here too (the reading above), so a selected NaN
+         * gets weight 0 */
+        const float m0 = l[topk_idx[(long)t * K]];
+        const float m = isnan(m0) ? -INFINITY : m0;
         float sum = 0.0f;
         for (int k = 0; k < K; ++k) {
-            ev[k] = expf(l[topk_idx[(long)t * K + k]] - m);
+            const float v = l[topk_idx[(long)t * K + k]];
+            ev[k] = expf((isnan(v) ? -INFINITY : v) - m);
             sum = sum + ev[k];
         }
         for (int k = 0; k < K; ++k) {

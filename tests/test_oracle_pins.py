@@ -183,6 +183,24 @@ def test_topk_tie_selects_lower_index(orc):
     assert np.all(idx2 == [2, 4]) and np.all(w2[:, 0] == w2[:, 1])
 
 
+def test_topk_nan_ranks_as_minus_infinity_and_degenerate_k(orc):
+    """The reading for NaN logits: they rank as -inf (after every finite
+    logit, ties among them to the lower index).  K = 1 gives weight exactly 1;
+    K = E gives the softmax of the whole row."""
+    logits = np.array([[0.5, np.nan, -3.0, np.nan, 2.0, -np.inf]], dtype=np.float32)
+    idx, w = orc.topk_softmax(logits, 6)
+    assert list(idx[0]) == [4, 0, 2, 1, 3, 5]   # finite desc, then NaN/-inf by index
+    assert np.all(w[0, 3:] == 0.0)              # exp(-inf - max) = 0
+    idx1, w1 = orc.topk_softmax(logits, 1)
+    assert idx1[0, 0] == 4 and w1[0, 0] == 1.0
+    rng = np.random.default_rng(8)
+    full = rng.standard_normal((4, 9)).astype(np.float32)
+    idx9, w9 = orc.topk_softmax(full, 9)
+    ref = np.exp(full.astype(np.float64) - full.max(1, keepdims=True))
+    ref /= ref.sum(1, keepdims=True)
+    assert np.max(np.abs(w9 - np.take_along_axis(ref, idx9, 1))) <= 2e-7
+
+
 def test_softmax_weights(orc):
     rng = np.random.default_rng(6)
     logits = (3 * rng.standard_normal((50, 128))).astype(np.float32)
