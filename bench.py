@@ -318,7 +318,9 @@ def bench_ours(args, cfg, world, rank, local, pg):
     if prefill:
         # the gate/up grouped GEMM (tcgen05, FP16 operands, fp32 accumulation)
         # is the dominant kernel: its algorithmic FLOPs per launch
-        launches = n_layers * 6  # route, index, gather, gate/up GEMM, down GEMM, combine
+        # norm, router floats, logits GEMM, top-k, grouping, tile index, scatter,
+        # gate/up GEMM, down GEMM, combine
+        launches = n_layers * 10
         kname = "pf_gemm<0>"
         gu_flops = 2 * 2 * T * (K * cfg.I + cfg.S) * D
         achieved = gu_flops / gu_s / 1e12
