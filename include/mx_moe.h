@@ -30,7 +30,7 @@
  *   scales, biases: BF16 [rows][cols/64]; w[r,c] = s[r,c/64]*q[r,c] + b[r,c/64].
  *
  * Top-k order: descending logit, ties to the lower expert index; NaN logits
- * rank as -inf.  Routing logits are computed in a fixed fp32 order (per group
+ * rank as -inf and enter the softmax as -inf (weight 0).  Routing logits are computed in a fixed fp32 order (per group
  * of 64: P = fma chain of q*x, X = add chain of x; then per group, ascending,
  * acc = fma(s, P, acc), acc = fma(b, X, acc)) so the top-k choice is
  * reproducible bit for bit.
