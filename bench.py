@@ -5,11 +5,15 @@ Default workload: single-token decode through a 30-layer stack of MoE blocks
 (attention omitted; RMSNorm -> block -> residual per layer), d_model 2816, 128
 experts top-8, expert width 704, shared width 2112, 4-bit group-64 experts,
 8-bit router, BF16 activations, seed 1.  One step = one token through all 30
-layers; ``value`` = tokens/s over all ranks.  ``--config 2|3|4`` times one
-block on the other workloads (prefill T=512, skewed decode T=64, prefill
-T=4096) instead.
+layers; ``value`` = tokens/s over all ranks, timed over exactly --steps graph
+replays.  The same line then carries, under ``configs``, every other workload
+(tiny T=4, prefill T=512, skewed decode T=64, prefill T=4096): for each, the
+median, p10 and p90 of --calls timed calls, e2e, the dominant kernel's
+roofline, whole-step HBM and tensor fractions and the oracle's CPU baselines.
+``--config C`` makes workload C the headline instead.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C]
+                    [--calls N] [--no-all-configs] [--no-cpu-baseline]
 
 ``--impl reference`` times the CPU oracle (the plain C reference) on the host
 cores, a bounded sample per step.  Under torchrun (N > 1) each rank runs its own
@@ -183,148 +187,168 @@ def flops(cfg, T):
 
 # ------------------------------------------------------------------ ours
 
-def bench_ours(args, cfg, world, rank, local, pg):
+PD_LAUNCH_NOTE = "single-launch decode kernel (all layers of the step in one persistent launch)"
+
+
+def l2_flush_bytes():
+    return 256 << 20  # twice the 129 MB L2
+
+
+def time_calls(run, n, stream, flush=None):
+    """Per-call device times (ms) of n calls, each between two events on the
+    launching stream; ``flush`` (outside the event pair) evicts L2 first."""
     import torch
-
-    import __graft_entry__
-    import expert_ffn_gb300 as mx
-    __graft_entry__.build()
-    torch.cuda.set_device(local)
-    dev_name = torch.cuda.get_device_name(local)
-    stream = torch.cuda.Stream()
-    n_layers = cfg.layers
-    T, K, D = cfg.T, cfg.K, cfg.D
-    act = mx.MX_BF16 if cfg.act == "bf16" else mx.MX_F32
-
-    t0 = time.time()
-    hosts = [synth.make_layer(cfg, l) for l in range(n_layers)]
-    devs = [mx.DeviceLayer(h, act) for h in hosts]
-    x0 = synth.make_x(cfg)
-    gen_s = time.time() - t0
-    xv = x0.view(np.int16) if x0.dtype == np.uint16 else x0
-    x_init = torch.from_numpy(xv).cuda()
-    x_io = torch.empty_like(x_init)
-    idx = torch.zeros((n_layers, T, K), dtype=torch.int32, device="cuda")
-    wts = torch.zeros((n_layers, T, K), dtype=torch.float32, device="cuda")
-    stack = mx.Stack(devs)
-    if n_layers > 1:
-        nbytes = mx.stack_workspace_bytes(devs[0].layout, T)
-    else:
-        nbytes = mx.workspace_bytes(devs[0].layout, T)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-    mx.workspace_init(ws, nbytes, stream)
-    out1 = torch.empty_like(x_init)
-
-    def step(s):
-        """One step: the workload's input through the block(s), on stream s."""
-        if n_layers > 1:
-            x_io.copy_(x_init)
-            mx.stack_forward(x_io, T, stack, idx, wts, ws, nbytes, rms_eps=1e-6, stream=s)
-        else:
-            mx.layer_forward_ex(x_init, T, devs[0], out1, idx[0], wts[0], ws, nbytes, stream=s)
-
-    # CUDA graph of one step (the library allocates nothing and syncs nothing)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
     with torch.cuda.stream(stream):
-        step(stream)
+        for a, b in evs:
+            if flush is not None:
+                flush()
+            a.record(stream)
+            run()
+            b.record(stream)
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step(stream)
-    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
 
-    # routing statistics for the byte counts
-    idx_h = idx.cpu().numpy()
-    per_layer = [stage_bytes(cfg, len(np.unique(idx_h[l])), T) for l in range(n_layers)]
-    step_bytes = sum(b["total"] for b in per_layer)
-    gu_bytes_per_launch = statistics.mean(b["gate_up"] for b in per_layer)
-    step_flops = n_layers * flops(cfg, T)
 
-    def barrier():
-        if pg is not None:
-            pg.barrier()
+def pct(v, q):
+    return float(np.percentile(np.asarray(v, dtype=np.float64), q))
 
-    for _ in range(args.warmup):
-        graph.replay()
-    torch.cuda.synchronize()
-    barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        tw0 = time.time()
+
+class Workload:
+    """One workload on the device: its layers, a captured CUDA graph of one
+    step, and the routing the step produced (for the byte counts)."""
+
+    def __init__(self, mx, cfg, stream):
+        import torch
+        self.cfg = cfg
+        self.stream = stream
+        n_layers, T, K = cfg.layers, cfg.T, cfg.K
+        act = mx.MX_BF16 if cfg.act == "bf16" else mx.MX_F32
+        t0 = time.time()
+        self.hosts = [synth.make_layer(cfg, l) for l in range(n_layers)]
+        self.devs = [mx.DeviceLayer(h, act) for h in self.hosts]
+        self.x0 = synth.make_x(cfg)
+        self.gen_s = time.time() - t0
+        xv = self.x0.view(np.int16) if self.x0.dtype == np.uint16 else self.x0
+        self.xv = xv
+        self.x_init = torch.from_numpy(xv).cuda()
+        self.x_io = torch.empty_like(self.x_init)
+        self.idx = torch.zeros((n_layers, T, K), dtype=torch.int32, device="cuda")
+        self.wts = torch.zeros((n_layers, T, K), dtype=torch.float32, device="cuda")
+        self.stack = mx.Stack(self.devs)
+        self.nbytes = (mx.stack_workspace_bytes(self.devs[0].layout, T) if n_layers > 1
+                       else mx.workspace_bytes(self.devs[0].layout, T))
+        self.ws = torch.empty(self.nbytes, dtype=torch.uint8, device="cuda")
+        mx.workspace_init(self.ws, self.nbytes, stream)
+        self.out1 = torch.empty_like(self.x_init)
+        self.mx = mx
         with torch.cuda.stream(stream):
-            ev0.record(stream)
-            for _ in range(args.steps):
-                graph.replay()
-            ev1.record(stream)
+            self.step(stream)
         torch.cuda.synchronize()
-        tw1 = time.time()
-    barrier()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, "cuda")
-    clocks = clk.summary(tw0, tw1)
-    ms_per_step = ms / args.steps
-    value = job_tokens_per_s(world, args.steps, T, ms)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            self.step(stream)
+        torch.cuda.synchronize()
+        mx.workspace_check(self.ws, stream)
+        idx_h = self.idx.cpu().numpy()
+        self.per_layer = [stage_bytes(cfg, len(np.unique(idx_h[l])), T) for l in range(n_layers)]
+        self.step_bytes = sum(b["total"] for b in self.per_layer)
+        self.step_flops = n_layers * flops(cfg, T)
 
-    # stage timing (events on the launching stream, direct API calls)
-    mx.profile_enable(True)
-    nprof = max(3, min(args.steps, 50))
-    with torch.cuda.stream(stream):
-        for _ in range(nprof):
-            step(stream)
-    torch.cuda.synchronize()
-    prof = mx.profile_read(reset=True)
-    mx.profile_enable(False)
+    def step(self, s):
+        """One step: the workload's input through the block(s), on stream s."""
+        cfg, mx = self.cfg, self.mx
+        if cfg.layers > 1:
+            self.x_io.copy_(self.x_init)
+            mx.stack_forward(self.x_io, cfg.T, self.stack, self.idx, self.wts, self.ws, self.nbytes, rms_eps=1e-6,
+                             stream=s)
+        else:
+            mx.layer_forward_ex(self.x_init, cfg.T, self.devs[0], self.out1, self.idx[0], self.wts[0], self.ws,
+                                self.nbytes, stream=s)
+
+    def stage_profile(self, n):
+        """Per-stage event timing of n direct API calls (not graph replays)."""
+        import torch
+        mx = self.mx
+        mx.profile_enable(True)
+        mx.profile_read(reset=True)
+        with torch.cuda.stream(self.stream):
+            for _ in range(n):
+                self.step(self.stream)
+        torch.cuda.synchronize()
+        prof = mx.profile_read(reset=True)
+        mx.profile_enable(False)
+        return prof
+
+    def e2e(self, steps, warmup):
+        """Pinned host input -> device, the C-ABI call (no graph), outputs ->
+        pinned host, every step; returns (ms for all steps, h2d, d2h bytes)."""
+        import torch
+        cfg, mx, s = self.cfg, self.mx, self.stream
+        T, K, n_layers = cfg.T, cfg.K, cfg.layers
+        x_pin = torch.from_numpy(self.xv.copy()).pin_memory()
+        out_pin = torch.empty(self.x_init.shape, dtype=self.x_init.dtype).pin_memory()
+        idx_pin = torch.empty(self.idx.shape, dtype=torch.int32).pin_memory()
+        w_pin = torch.empty(self.wts.shape, dtype=torch.float32).pin_memory()
+        x_dev = torch.empty_like(self.x_init)
+
+        def e2e_step():
+            x_dev.copy_(x_pin, non_blocking=True)
+            if n_layers > 1:
+                mx.stack_forward(x_dev, T, self.stack, self.idx, self.wts, self.ws, self.nbytes, rms_eps=1e-6,
+                                 stream=s)
+                out_pin.copy_(x_dev, non_blocking=True)
+            else:
+                mx.layer_forward_ex(x_dev, T, self.devs[0], self.out1, self.idx[0], self.wts[0], self.ws,
+                                    self.nbytes, stream=s)
+                out_pin.copy_(self.out1, non_blocking=True)
+            idx_pin.copy_(self.idx, non_blocking=True)
+            w_pin.copy_(self.wts, non_blocking=True)
+
+        with torch.cuda.stream(s):
+            for _ in range(warmup):
+                e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for _ in range(steps):
+                e2e_step()
+            e1.record(s)
+        torch.cuda.synchronize()
+        es = self.x_init.element_size()
+        return e0.elapsed_time(e1), T * cfg.D * es, T * cfg.D * es + n_layers * T * K * 8
+
+
+def path_of(cfg):
+    single = cfg.T <= PD_MAX_T and os.environ.get("MX_MOE_SINGLE_LAUNCH", "1") != "0"
+    prefill = cfg.T > 64 and cfg.act == "bf16" and os.environ.get("MX_MOE_PREFILL_GEMM", "1") != "0"
+    return "prefill" if prefill else ("single" if single else "multi")
+
+
+def launches_per_step(cfg):
+    path = path_of(cfg)
+    if path == "prefill":
+        # norm, router floats, logits GEMM, top-k, grouping, tile index,
+        # scatter, gate/up GEMM, down GEMM, combine
+        return cfg.layers * 10
+    if path == "single":
+        return -(-cfg.layers // PD_MAX_LAYERS)
+    return cfg.layers * 3 * ((cfg.T + 63) // 64)
+
+
+def roofline_of(wl, prof, peaks, peak_src):
+    """The dominant kernel's achieved rate against its roof: the algorithmic
+    bytes (or FLOPs) of one launch over its mean CUDA-event duration."""
+    cfg, path = wl.cfg, path_of(wl.cfg)
+    T, K, D = cfg.T, cfg.K, cfg.D
     gu_ms, gu_n = prof["gate_up"]
     gu_s = gu_ms / 1e3 / max(gu_n, 1)
-    peaks, peak_src = load_peaks()
-
-    # end to end: pinned host input -> device, API calls, result -> host, every step
-    x_pin = torch.from_numpy(xv.copy()).pin_memory()
-    out_pin = torch.empty(x_init.shape, dtype=x_init.dtype).pin_memory()
-    idx_pin = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
-    w_pin = torch.empty(wts.shape, dtype=torch.float32).pin_memory()
-    x_dev = torch.empty_like(x_init)
-
-    def e2e_step(s):
-        x_dev.copy_(x_pin, non_blocking=True)
-        if n_layers > 1:
-            mx.stack_forward(x_dev, T, stack, idx, wts, ws, nbytes, rms_eps=1e-6, stream=s)
-            out_pin.copy_(x_dev, non_blocking=True)
-        else:
-            mx.layer_forward_ex(x_dev, T, devs[0], out1, idx[0], wts[0], ws, nbytes, stream=s)
-            out_pin.copy_(out1, non_blocking=True)
-        idx_pin.copy_(idx, non_blocking=True)
-        w_pin.copy_(wts, non_blocking=True)
-
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            e2e_step(stream)
-    torch.cuda.synchronize()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step(stream)
-        e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), pg, "cuda")
-    es = x_init.element_size()
-    h2d = T * D * es
-    d2h = T * D * es + n_layers * T * K * 8
-
-    workload = cfg.name if n_layers == synth.CONFIGS[args.config].layers else f"{cfg.name}[{n_layers} layers]"
-    single = T <= PD_MAX_T and os.environ.get("MX_MOE_SINGLE_LAUNCH", "1") != "0"
-    prefill = T > 64 and cfg.act == "bf16" and os.environ.get("MX_MOE_PREFILL_GEMM", "1") != "0"
-    if prefill:
-        # the gate/up grouped GEMM (tcgen05, FP16 operands, fp32 accumulation)
-        # is the dominant kernel: its algorithmic FLOPs per launch
-        # norm, router floats, logits GEMM, top-k, grouping, tile index, scatter,
-        # gate/up GEMM, down GEMM, combine
-        launches = n_layers * 10
+    workload = cfg.name
+    if path == "prefill":
         kname = "pf_gemm<0>"
         gu_flops = 2 * 2 * T * (K * cfg.I + cfg.S) * D
         achieved = gu_flops / gu_s / 1e12
-        # FP16 and BF16 run at the same tensor rate: the BF16 cuBLAS peak applies
         roof = {"bound": "tensor", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
                 "peak_source": peak_src + " (bf16 burst; fp16 is the same tensor rate)",
@@ -334,48 +358,155 @@ def bench_ours(args, cfg, world, rank, local, pg):
         if dn_n:
             dn_flops = 2 * T * (K * cfg.I + cfg.S) * D
             roof["down_gemm_tflops"] = round(dn_flops / (dn_ms / 1e3 / dn_n) / 1e12, 1)
+        return roof
+    if path == "single":
+        launches = -(-cfg.layers // PD_MAX_LAYERS)
+        kname, bytes_launch = "pd_kernel", wl.step_bytes / launches
     else:
-        if single:
-            # one persistent launch runs every layer of the step (up to 30 per
-            # launch): its algorithmic bytes are the whole step's
-            launches = -(-n_layers // PD_MAX_LAYERS)
-            kname, bytes_launch = "pd_kernel", step_bytes / launches
-        else:
-            launches = n_layers * 3 * ((T + 63) // 64)
-            kname, bytes_launch = "gateup_kernel", gu_bytes_per_launch
-        achieved = bytes_launch / gu_s / 1e9
-        roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "peak_source": peak_src,
-                "traffic": committed_traffic(kname, workload),
-                "bytes_per_launch": int(bytes_launch), "launch_us": round(gu_s * 1e6, 2),
-                "launches_timed": gu_n}
-    step_gbs = step_bytes / (ms_per_step / 1e3) / 1e9
-    stages_us = {k: round(v[0] * 1e3 / max(v[1], 1), 2) for k, v in prof.items()}
+        kname, bytes_launch = "gateup_kernel", statistics.mean(b["gate_up"] for b in wl.per_layer)
+    achieved = bytes_launch / gu_s / 1e9
+    roof = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_source": peak_src,
+            "traffic": committed_traffic(kname, workload), "bytes_per_launch": int(bytes_launch),
+            "launch_us": round(gu_s * 1e6, 2), "launches_timed": gu_n}
+    if cfg.T * cfg.D * 2 * 64 < 128e6 and wl.step_bytes < 100e6:
+        roof["note"] = "working set inside L2 (L2 flushed between timed calls): latency-bound, not HBM-bound"
+    return roof
+
+
+def step_fractions(wl, ms_per_step, peaks):
+    gbs = wl.step_bytes / (ms_per_step / 1e3) / 1e9
+    tfs = wl.step_flops / (ms_per_step / 1e3) / 1e12
+    return {"step_bytes": int(wl.step_bytes), "step_hbm_gbs": round(gbs, 1),
+            "step_hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "step_flops": int(wl.step_flops),
+            "step_tflops": round(tfs, 3), "step_tensor_frac": round(tfs / peaks["bf16_tflops"], 4)}
+
+
+def config_entry(args, ci, mx, stream, peaks, peak_src, want_cpu):
+    """A non-headline workload: per-call distribution over >= 100 timed calls,
+    stage profile, e2e, roofline and the CPU baselines."""
+    import torch
+    cfg = synth.CONFIGS[ci]
+    wl = Workload(mx, cfg, stream)
+    flush = None
+    if wl.step_bytes < 2 * 129e6:
+        buf = torch.empty(l2_flush_bytes(), dtype=torch.uint8, device="cuda")
+        flush = lambda: buf.fill_(1)  # noqa: E731
+    for _ in range(max(args.warmup, 5)):
+        wl.graph.replay()
+    torch.cuda.synchronize()
+    calls = time_calls(wl.graph.replay, args.calls, stream, flush)
+    med = pct(calls, 50)
+    prof = wl.stage_profile(max(3, min(args.calls, 30)))
+    e2e_ms, h2d, d2h = wl.e2e(max(10, min(args.steps, 50)), 3)
+    n_e2e = max(10, min(args.steps, 50))
+    entry = {"index": ci, "workload": cfg.name, "T": cfg.T, "layers": cfg.layers, "path": path_of(cfg),
+             "value": round(cfg.T / (med / 1e3), 2), "unit": "tokens/s", "ms_per_step": round(med, 5),
+             "ms_p10": round(pct(calls, 10), 5), "ms_p90": round(pct(calls, 90), 5), "timed_calls": len(calls),
+             "l2": "flushed between timed calls" if flush else "inputs larger than L2",
+             "e2e": {"value": round(n_e2e * cfg.T / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+             "roofline": roofline_of(wl, prof, peaks, peak_src),
+             "stage_us": {k: round(v[0] * 1e3 / max(v[1], 1), 2) for k, v in prof.items()},
+             "gpu_launches_per_step": launches_per_step(cfg)}
+    entry.update(step_fractions(wl, med, peaks))
+    if want_cpu:
+        entry["cpu_baseline"] = cpu_baseline(cfg, wl.hosts, wl.x0, budget_s=args.cpu_budget)
+    del wl
+    torch.cuda.empty_cache()
+    return entry
+
+
+def bench_ours(args, cfg, world, rank, local, pg):
+    import torch
+
+    import __graft_entry__
+    import expert_ffn_gb300 as mx
+    __graft_entry__.build()
+    torch.cuda.set_device(local)
+    dev_name = torch.cuda.get_device_name(local)
+    stream = torch.cuda.Stream()
+    T = cfg.T
+    peaks, peak_src = load_peaks()
+
+    wl = Workload(mx, cfg, stream)
+    flush = None
+    if wl.step_bytes < 2 * 129e6:
+        buf = torch.empty(l2_flush_bytes(), dtype=torch.uint8, device="cuda")
+        flush = lambda: buf.fill_(1)  # noqa: E731
+
+    def barrier():
+        if pg is not None:
+            pg.barrier()
+
+    for _ in range(args.warmup):
+        wl.graph.replay()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        tw0 = time.time()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                if flush is not None:
+                    flush()
+                wl.graph.replay()
+            ev1.record(stream)
+        torch.cuda.synchronize()
+        tw1 = time.time()
+    barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg, "cuda")
+    clocks = clk.summary(tw0, tw1)
+    ms_per_step = ms / args.steps
+    value = job_tokens_per_s(world, args.steps, T, ms)
+
+    # the per-call distribution (>= 100 calls, outside the headline region)
+    calls = time_calls(wl.graph.replay, args.calls, stream, flush)
+    prof = wl.stage_profile(max(3, min(args.steps, 50)))
+    roof = roofline_of(wl, prof, peaks, peak_src)
+    e2e_ms, h2d, d2h = wl.e2e(args.steps, args.warmup)
+    e2e_ms = max_over_ranks(e2e_ms, pg, "cuda")
+
+    n_layers = cfg.layers
+    workload = cfg.name if n_layers == synth.CONFIGS[args.config].layers else f"{cfg.name}[{n_layers} layers]"
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if cfg.act == "bf16" else "f32", "data": "synthetic (seeded; random-init "
         "4-bit experts, 8-bit router)",
-        "config": {"workload": workload, "T": T, "layers": n_layers, "d_model": D, "experts": cfg.E, "top_k": K,
-                   "d_expert": cfg.I, "d_shared": cfg.S, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2 ({sum(h.blob.nbytes for h in hosts) / 1e9:.1f} GB of expert "
-                         "weights; each step reads its selected experts from HBM)",
+        "config": {"workload": workload, "T": T, "layers": n_layers, "d_model": cfg.D, "experts": cfg.E,
+                   "top_k": cfg.K, "d_expert": cfg.I, "d_shared": cfg.S, "parallelism": f"replicas x{world}",
+                   "l2": ("flushed between timed steps" if flush else
+                          f"inputs larger than L2 ({sum(h.blob.nbytes for h in wl.hosts) / 1e9:.1f} GB of expert "
+                          "weights; each step reads its selected experts from HBM)"),
                    "timing": "CUDA graph replay of the step, CUDA events on the launching stream"},
-        "step_bytes": int(step_bytes), "step_hbm_gbs": round(step_gbs, 1),
-        "step_hbm_frac": round(step_gbs / peaks["hbm_gbs"], 4),
-        "step_tflops": round(step_flops / (ms_per_step / 1e3) / 1e12, 3),
-        "stage_us": stages_us,
+        "ms_p10": round(pct(calls, 10), 5), "ms_p50": round(pct(calls, 50), 5), "ms_p90": round(pct(calls, 90), 5),
+        "timed_calls": len(calls),
+        "stage_us": {k: round(v[0] * 1e3 / max(v[1], 1), 2) for k, v in prof.items()},
         "roofline": roof,
         "clocks": clocks,
         "e2e": {"value": round(job_tokens_per_s(world, args.steps, T, e2e_ms), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host input copied in, the C-ABI call (no graph), outputs copied out, every step"},
-        "gpu_launches": args.steps * launches,
-        "device": dev_name, "gen_s": round(gen_s, 1),
+        "gpu_launches": args.steps * launches_per_step(cfg),
+        "device": dev_name, "gen_s": round(wl.gen_s, 1),
     }
-    if rank == 0 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(cfg, hosts, x0, budget_s=args.cpu_budget)
+    res.update(step_fractions(wl, ms_per_step, peaks))
+    want_cpu = rank == 0 and not args.no_cpu_baseline
+    if want_cpu:
+        res["cpu_baseline"] = cpu_baseline(cfg, wl.hosts, wl.x0, budget_s=args.cpu_budget)
+    del wl
+    torch.cuda.empty_cache()
+    if args.all_configs:
+        others = {}
+        for ci in sorted(synth.CONFIGS):
+            if ci == args.config:
+                continue
+            e = config_entry(args, ci, mx, stream, peaks, peak_src, want_cpu)
+            others[e["workload"]] = e
+        res["configs"] = others
     return res
 
 
@@ -391,9 +522,15 @@ def oracle_step(cfg, hosts, x0, n_layers_sample: int, n_tokens: int):
 
 
 def cpu_baseline(cfg, hosts, x0, budget_s: float = 20.0, kind: str = "oracle"):
-    """Time the oracle as it stands on a bounded sample; scale to tokens/s."""
+    """Time the oracle as it stands on a bounded sample; scale to tokens/s.
+    One host core, then every core (one thread per core, each running the
+    single-threaded oracle on its own tokens -- or, for the one-token stack, its
+    own independent token stream; ctypes releases the GIL during the call)."""
+    import concurrent.futures as cf
+
     import oracle
     oracle.build()
+    cores = os.cpu_count() or 1
     if cfg.layers > 1:
         # one token through the layers; time one layer first to size the sample
         t0 = time.perf_counter()
@@ -405,6 +542,12 @@ def cpu_baseline(cfg, hosts, x0, budget_s: float = 20.0, kind: str = "oracle"):
         dt = time.perf_counter() - t0
         value = (nl / cfg.layers) / dt
         sample = f"1 token through {nl} of {cfg.layers} layers (tokens/s scaled by {nl}/{cfg.layers})"
+        with cf.ThreadPoolExecutor(max_workers=cores) as ex:
+            t0 = time.perf_counter()
+            list(ex.map(lambda _: oracle_step(cfg, hosts, x0, nl, 1), range(cores)))
+            dt_all = time.perf_counter() - t0
+        value_all = cores * (nl / cfg.layers) / dt_all
+        sample_all = f"{cores} independent one-token streams through {nl} of {cfg.layers} layers, one per core"
     else:
         t0 = time.perf_counter()
         oracle_step(cfg, hosts, x0, 1, 1)
@@ -415,8 +558,15 @@ def cpu_baseline(cfg, hosts, x0, budget_s: float = 20.0, kind: str = "oracle"):
         dt = time.perf_counter() - t0
         value = n / dt
         sample = f"{n} of {cfg.T} tokens through the block"
+        n_all = int(max(1, min(cfg.T, cores * budget_s // max(per_tok, 1e-6))))
+        t0 = time.perf_counter()
+        oracle.block_forward_tokens(hosts[0], x0, np.arange(n_all), threads=cores)
+        dt_all = time.perf_counter() - t0
+        value_all = n_all / dt_all
+        sample_all = f"{n_all} of {cfg.T} tokens split over {cores} threads"
     return {"value": round(value, 4), "unit": "tokens/s", "cores": 1, "kind": kind, "sample": sample,
-            "cpu": platform_cpu()}
+            "cpu": platform_cpu(),
+            "all_cores": {"value": round(value_all, 4), "unit": "tokens/s", "cores": cores, "sample": sample_all}}
 
 
 def platform_cpu():
@@ -469,9 +619,12 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--cpu-budget", type=float, default=8.0, help="seconds of oracle work per CPU sample")
+    ap.add_argument("--calls", type=int, default=100, help="timed calls of the per-call distribution")
+    ap.add_argument("--no-all-configs", dest="all_configs", action="store_false",
+                    help="time only --config (the other workloads are added under 'configs' by default)")
     ap.add_argument("--layers", type=int, default=0,
                     help="run only the first N layers of the workload (profiling captures; 0 = all)")
     args = ap.parse_args()

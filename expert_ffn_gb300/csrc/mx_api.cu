@@ -249,7 +249,12 @@ mx_status run_pd(const PdIn *in, int n, int T, int pre_norm, float eps, const Pd
                  uint8_t *ws, cudaStream_t s)
 {
     const mx_moe_layout *L0 = in[0].L;
-    static thread_local PdParams P;  // ~31 KB: kept off the stack
+    // ~31 KB of kernel parameters: one static block (not thread-local, whose
+    // lazy per-thread allocation would make a host thread's first call
+    // allocate), held under a lock until the launch has copied it
+    static PdParams P;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
     std::memset(&P, 0, sizeof P);
     P.T = T;
     P.D = L0->d_model;
@@ -598,6 +603,7 @@ const char *mx_status_string(mx_status s)
     case MX_ERR_WORKSPACE: return "MX_ERR_WORKSPACE";
     case MX_ERR_CUDA: return "MX_ERR_CUDA";
     case MX_ERR_DEVICE_TIMEOUT: return "MX_ERR_DEVICE_TIMEOUT";
+    case MX_ERR_RANGE: return "MX_ERR_RANGE";
     }
     return "MX_ERR_UNKNOWN";
 }
@@ -642,8 +648,11 @@ mx_status mx_moe_workspace_check(const void *ws, void *stream)
         e = cudaStreamSynchronize(s);
     if (e != cudaSuccess)
         return cuda_fail(e, "reading the workspace error word");
-    if (word != 0)
+    if (word & 1u)
         return fail(MX_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (error word 0x%x)", word);
+    if (word != 0)
+        return fail(MX_ERR_RANGE, "a partial sum fell outside the fixed-point range of the decode path "
+                                  "(error word 0x%x)", word);
     return MX_OK;
 }
 
@@ -842,7 +851,7 @@ mx_status mx_moe_stack_forward(void *x_io, int T, int n_layers, const mx_qlinear
             // inside a launch; between launches it passes through the
             // workspace; the last layer writes x_io
             uint8_t *w = static_cast<uint8_t *>(ws);
-            static thread_local PdIn in[kPdMaxLayers];
+            PdIn in[kPdMaxLayers];
             for (int l0 = 0; l0 < n_layers; l0 += kPdMaxLayers) {
                 const int n = n_layers - l0 < kPdMaxLayers ? n_layers - l0 : kPdMaxLayers;
                 for (int i = 0; i < n; ++i) {

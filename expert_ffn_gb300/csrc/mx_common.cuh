@@ -101,7 +101,8 @@ __device__ __forceinline__ float byte_f(uint32_t w)
 // error code in the caller's error word and returns false.
 
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrTimeout = 1u;  // a bounded wait gave up
+constexpr unsigned kErrRange = 2u;    // a value outside a fixed-point range (left out)
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 

@@ -190,6 +190,7 @@ struct Smem {
     float *fx;             // [T] x plane back factors 2^(9-k)
     float *rn, *xsc;       // [T] rmsnorm factors, x plane scales
     int *vmax;             // [T] plane maxima (float bits)
+    float *yfx;            // [2] fixed-point factor of the layer's y and its inverse
     int *flag;             // [4]
     uint8_t *zero;         // 16 zero bytes
     Rt rt;
@@ -221,6 +222,7 @@ __device__ __forceinline__ Smem carve(uint8_t *sm, const PdParams &p)
     s.ux = m + 16;
     s.ufo = m + 20;
     s.vmax = reinterpret_cast<int *>(m + 24);  // [T]
+    s.yfx = m + 28;
     int *r = reinterpret_cast<int *>(sm + o.rt);
     const int amax = TK < p.E ? TK : p.E;
     s.rt.n_act = r;
@@ -323,11 +325,29 @@ __device__ __forceinline__ void red_add(int *c, int v)
     asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(c), "r"(v) : "memory");
 }
 
-// The down projections' partial sums are added into y in 64-bit fixed point
-// (2^-32 units): integer addition is associative, so y does not depend on the
-// order in which CTAs arrive.
+// The down projections' partial sums are added into y in 64-bit fixed point:
+// integer addition is associative, so y does not depend on the order in which
+// CTAs arrive.  The unit is 2^-32 / f with a per-layer power of two f that
+// follows the square of the block input's magnitude (the hidden vectors are
+// products of two projections of x, and y is linear in them): with E =
+// floor(log2(max |x|)) over the layer's tokens, f = 2^(4 - 2E), clamped to
+// 2^[-100, 100] -- f = 1 for inputs of magnitude 4..8.  Each partial sum must
+// satisfy |v f| < 2^23 (at most 2^23 units of 2^32: a few hundred additions
+// stay far inside the 64-bit range); a partial outside that range is not
+// added and sets kErrRange in the error word.
 constexpr float kFix = 4294967296.0f;         // 2^32
 constexpr float kUnfix = 2.3283064365386963e-10f;  // 2^-32
+constexpr float kFixLimit = 8388608.0f;       // 2^23
+
+// The layer's factor f (and 1/f) from the largest input magnitude m.
+__device__ __forceinline__ void fix_factor(float m, float &f, float &inv)
+{
+    int E = m > 0.f ? (int)((__float_as_uint(m) >> 23) & 0xFF) - 127 : 0;
+    int k = 4 - 2 * E;
+    k = k > 100 ? 100 : (k < -100 ? -100 : k);
+    f = __uint_as_float((uint32_t)(127 + k) << 23);
+    inv = __uint_as_float((uint32_t)(127 - k) << 23);
+}
 // round(v * 2^32) as a 64-bit integer with 32-bit conversions (64-bit ones are
 // slow here).  For a = |v|: a = h + f with h = floor(a) an integer and f in
 // [0, 1), both exact, and h * 2^32 even, so round(a 2^32) = h 2^32 +
@@ -350,9 +370,16 @@ __device__ __forceinline__ float from_fix(long long q)
     return (float)hi + __uint2float_rn(lo) * kUnfix;
 }
 
-__device__ __forceinline__ void red_fix(long long *y, float v)
+// Adds v f into the fixed-point sum; a value outside the range is reported
+// (kErrRange) and left out.
+__device__ __forceinline__ void red_fix(long long *y, float v, float f, unsigned *err)
 {
-    const long long q = to_fix(v);
+    const float a = v * f;
+    if (!(fabsf(a) < kFixLimit)) {
+        atomicOr(err, kErrRange);
+        return;
+    }
+    const long long q = to_fix(a);
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(y), "l"(q) : "memory");
 }
 
@@ -613,6 +640,12 @@ __device__ void prologue(const PdParams &p, const Smem &s)
         plane_scale(__int_as_float(s.vmax[tid]), sc, bk);
         s.xsc[tid] = sc;
         s.fx[tid] = bk;
+    }
+    if (tid == 0) {
+        int m = 0;
+        for (int t = 0; t < T; ++t)
+            m = max(m, s.vmax[t]);
+        fix_factor(__int_as_float(m), s.yfx[0], s.yfx[1]);
     }
     csync();
     // group sums in the canonical order (the router's X), and the planes
@@ -1115,7 +1148,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 out = c < ne;
             }
             const int ot = shared ? oc : s.rt.act_slot[4 * j + oc] / K;  // this lane's token
-            const float hfo = s.ufo[oc], hX = s.ux[oc];
+            const float hfo = s.ufo[oc], hX = s.ux[oc], yf = s.yfx[0];
             long long *yv = y + (size_t)ot * D;
             for (int q = 0; q < 4; ++q) {
                 // this item's (scale | bias << 16) words into buffer q & 1 (the
@@ -1151,11 +1184,11 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                         dn_tile<false>(tile + rt2 * 512, hb, isb[r2], isb[r2 + 8], hfo, hX, b0, b8);
                     }
                     if (out) {
-                        red_fix(yv + q * R4 + r0, a0);
-                        red_fix(yv + q * R4 + r0 + 8, a8);
+                        red_fix(yv + q * R4 + r0, a0, yf, p.err);
+                        red_fix(yv + q * R4 + r0 + 8, a8, yf, p.err);
                         if (rt2 != rt) {
-                            red_fix(yv + q * R4 + r2, b0);
-                            red_fix(yv + q * R4 + r2 + 8, b8);
+                            red_fix(yv + q * R4 + r2, b0, yf, p.err);
+                            red_fix(yv + q * R4 + r2 + 8, b8, yf, p.err);
                         }
                     }
                 }
@@ -1208,6 +1241,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
         // y from L2: twelve loads per thread in flight at a time (all of y at
         // d_model <= 3072, T = 1)
         constexpr int kYB = NB == 1 ? 12 : 6;
+        const float yinv = s.yfx[1];
         for (int i0 = 0; i0 < T * D; i0 += kYB * kCT) {
             long long yq[kYB];
 #pragma unroll
@@ -1220,7 +1254,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             const int i = i0 + tid + j * kCT;
             if (i >= T * D)
                 break;
-            const float yv = from_fix(yq[j]);
+            const float yv = from_fix(yq[j]) * yinv;
             float res = 0.f;
             if (L.res_mode == 1)
                 res = es == 2 ? bf2f(reinterpret_cast<const uint16_t *>(s.xraw)[i])
@@ -1330,7 +1364,7 @@ bool pd_plan(int T, int D, int I, int S, int E, int K, int act, int n_cta, int s
         o.lg = take((size_t)T * E * 4);
         o.rt = take((size_t)4 * (20 + 6 * amax + 2 * TK + E));
         o.pr = take(scratch);
-        o.misc = take((size_t)4 * (24 + 4));
+        o.misc = take((size_t)4 * (24 + 4 + 4));
         o.zero = take(16);
         o.total = (int)off;
         if ((long long)off <= smem_max) {
@@ -1357,19 +1391,11 @@ template <int NB>
 cudaError_t launch_nb(const PdParams &p, cudaStream_t st)
 {
     auto k = pd_kernel<NB>;
-    static std::mutex mu;
-    static int configured = 0;
-    {
-        std::lock_guard<std::mutex> g(mu);
-        if (p.sm.total > configured) {
-            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, p.sm.total);
-            if (e != cudaSuccess)
-                return e;
-            configured = p.sm.total;
-        }
-    }
+    cudaError_t e = smem_optin(reinterpret_cast<const void *>(k), (size_t)p.sm.total);
+    if (e != cudaSuccess)
+        return e;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kPT, p.sm.total);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kPT, p.sm.total);
     if (e != cudaSuccess)
         return e;
     if (per_sm < 1)

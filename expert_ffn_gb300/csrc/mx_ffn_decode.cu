@@ -591,31 +591,6 @@ cudaError_t launch_pdl(Kern k, dim3 grid, dim3 block, size_t smem, cudaStream_t 
     return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
-// Opt a kernel into more than 48 KiB of dynamic shared memory (cached per kernel).
-cudaError_t ensure_smem(const void *k, size_t smem)
-{
-    static std::mutex mu;
-    static const void *keys[64];
-    static size_t vals[64];
-    static int n = 0;
-    if (smem <= 48 * 1024)
-        return cudaSuccess;
-    std::lock_guard<std::mutex> g(mu);
-    int i = 0;
-    while (i < n && keys[i] != k)
-        ++i;
-    if (i < n && vals[i] >= smem)
-        return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess)
-        return e;
-    if (i == n && n < 64)
-        keys[n++] = k;
-    if (i < n)
-        vals[i] = smem;
-    return cudaSuccess;
-}
-
 size_t align128(size_t n) { return (n + 127) & ~size_t(127); }
 
 constexpr size_t kSmemLimit = 227 * 1024;  // dynamic shared memory per CTA
@@ -632,7 +607,7 @@ size_t meta_bytes(const FfnArgs &a, int max_tiles) { return align128(4 * (3 * (s
 template <int NTD>
 cudaError_t launch_down(const FfnArgs &a, const DnLaunch &dl, const FfnMaps &maps, size_t smem, cudaStream_t s)
 {
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(down_kernel<NTD>), smem);
+    cudaError_t e = smem_optin(reinterpret_cast<const void *>(down_kernel<NTD>), smem);
     if (e != cudaSuccess)
         return e;
     return launch_pdl(down_kernel<NTD>, dim3(a.D / 16), dim3(kThreads), smem, s, a, dl, maps);
@@ -667,7 +642,7 @@ cudaError_t launch_nt(const FfnArgs &a, const FfnMaps &maps, int max_tiles, int 
     if (grid < 1)
         grid = 1;
     auto kg = gateup_kernel<NT, NS, BS>;
-    cudaError_t e = ensure_smem(reinterpret_cast<const void *>(kg), smem_gu);
+    cudaError_t e = smem_optin(reinterpret_cast<const void *>(kg), smem_gu);
     if (e != cudaSuccess)
         return e;
     prof_begin(kStageGateUp, s);

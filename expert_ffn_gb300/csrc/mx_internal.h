@@ -227,6 +227,11 @@ size_t route_f32_bytes(int D, int E);
 cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float *xsc, const float *XG, float *QF,
                                cudaStream_t s);
 
+// Opt kernel `k` into `bytes` of dynamic shared memory on the current device.
+// cudaFuncSetAttribute acts on the current device only, so the opt-in is
+// remembered per (device, kernel); sizes up to 48 KiB need none.
+cudaError_t smem_optin(const void *k, size_t bytes);
+
 // Stage profiler (mx_moe_profile_*): event pair around one launch.
 enum Stage { kStageRoute = 0, kStageGateUp = 1, kStageDown = 2 };
 void prof_begin(int stage, cudaStream_t s);

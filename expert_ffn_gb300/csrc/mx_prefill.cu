@@ -20,18 +20,21 @@
 //   down     grouped GEMM: y = W_down h, fp32 [slot][D] and [T][D]
 //   combine  out = residual + lambda * (shared + sum_k w_k y_k), k ascending
 //
-// The GEMM kernel is persistent (one CTA per SM) and warp-specialised:
-//   warp 0      TMA producer: packed 4-bit weight rows (one group of 64
-//               columns per stage) and the 128-token operand tile
-//               (SWIZZLE_128B) into a ring of stages;
-//   warp 1      allocates TMEM; one thread issues tcgen05.mma (M = 128,
-//               N = the tile's tokens rounded up to 16, K = 16, FP16 in, fp32
-//               accumulate) and commits to mbarriers;
-//   warps 2-9   dequantize: w = s*q + b in FP16 (one fused multiply-add on a
-//               half2 of exact integers), written in the 128-byte swizzled
-//               K-major layout the MMA reads (two threads per weight row);
-//   warps 10-13 epilogue: tcgen05.ld of the accumulators (two TMEM buffers,
-//               so the next tile's MMAs overlap this tile's epilogue).
+// The GEMM kernel is persistent (one CTA per SM) and warp-specialised
+// (16 warps; warp w runs on scheduler w % 4):
+//   warp 0      TMA producer of the packed 4-bit weight tiles (a deep ring of
+//               stages in shared memory);
+//   warp 1      allocates TMEM; the whole warp walks the MMA loop and one
+//               elected lane issues tcgen05.mma (A = the FP16 weights in TMEM,
+//               B = the activation tile in shared memory, M = 128, N = the
+//               tile's tokens rounded up to 16, K = 16, fp32 accumulators in
+//               TMEM) and commits to mbarriers;
+//   warp 2      TMA producer of the 128-token FP16 activation tiles
+//               (SWIZZLE_128B);
+//   warps 4-7   epilogue: tcgen05.ld of the accumulators (TMEM lane quadrant
+//               = warp % 4), gelu(g) * u for gate/up, fp32 rows for down;
+//   warps 8-15  dequantize: w = s*q + b in FP16 (one fused multiply-add on a
+//               half2 of exact integers), tcgen05.st into a TMEM weight slot.
 // Why FP16 and not BF16: BF16 rounding of the dequantized weights (8-bit
 // significand) alone gives ~1.6e-3 relative error per GEMM, above the 1e-3
 // rel-L2 bar on BF16 outputs; FP16 (11-bit significand) gives ~2e-4.  BF16
@@ -835,17 +838,9 @@ cudaError_t launch_gemm(const PfArgs &a, int n_cta, cudaStream_t s)
 {
     auto k = pf_gemm<MODE>;
     const size_t smem = gemm_smem<MODE>();
-    static std::mutex mu;
-    static bool configured = false;
-    {
-        std::lock_guard<std::mutex> g(mu);
-        if (!configured) {
-            cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess)
-                return e;
-            configured = true;
-        }
-    }
+    cudaError_t e = smem_optin(reinterpret_cast<const void *>(k), smem);
+    if (e != cudaSuccess)
+        return e;
     k<<<n_cta, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
@@ -900,18 +895,9 @@ cudaError_t launch_prefill_prepare(const PfCall &c, PfPrepared *out, cudaStream_
 {
     const PfBufs b = pf_carve(c.ws, c.T, c.D, c.I, c.S, c.E, c.K);
     const size_t gsm = (size_t)(c.D + 64 + c.D / 64) * 4;
-    cudaError_t e;
-    if (gsm > 48 * 1024) {
-        static std::mutex mu;
-        static size_t configured = 0;
-        std::lock_guard<std::mutex> g(mu);
-        if (gsm > configured) {
-            if ((e = cudaFuncSetAttribute(pf_norm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gsm)) !=
-                cudaSuccess)
-                return e;
-            configured = gsm;
-        }
-    }
+    cudaError_t e = smem_optin(reinterpret_cast<const void *>(pf_norm), gsm);
+    if (e != cudaSuccess)
+        return e;
     pf_norm<<<c.T, 256, gsm, s>>>(static_cast<const uint16_t *>(c.x), c.D, c.pre_norm, c.eps, b.X16, b.xsc, b.XG);
     out->X16 = b.X16;
     out->xsc = b.xsc;

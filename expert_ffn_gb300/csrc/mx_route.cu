@@ -527,12 +527,10 @@ template <int TT>
 cudaError_t launch_tt(const RouteArgs &a, const RouteLaunch &L, cudaStream_t s)
 {
     auto k = route_kernel<TT>;
-    static size_t configured = 0;  // largest dynamic smem opted into so far
-    if (L.smem > 48 * 1024 && L.smem > configured) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
+    {
+        cudaError_t e = smem_optin(reinterpret_cast<const void *>(k), L.smem);
         if (e != cudaSuccess)
             return e;
-        configured = L.smem;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.n_et, L.n_tt);
@@ -812,17 +810,8 @@ cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float 
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
     const size_t group_smem = (2 * (size_t)kGroupWarps * a.E + 3 * (size_t)a.E) * sizeof(float);
-    {
-        static std::mutex mu;
-        static size_t configured = 0;
-        std::lock_guard<std::mutex> g(mu);
-        if (group_smem > 48 * 1024 && group_smem > configured) {
-            if ((e = cudaFuncSetAttribute(group_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)group_smem)) != cudaSuccess)
-                return e;
-            configured = group_smem;
-        }
-    }
+    if ((e = smem_optin(reinterpret_cast<const void *>(group_kernel), group_smem)) != cudaSuccess)
+        return e;
     group_kernel<<<1, 32 * kGroupWarps, group_smem, s>>>(a);
     return cudaGetLastError();
 }

@@ -75,6 +75,37 @@ int g_n = 0, g_next = 0;
 
 } // namespace
 
+cudaError_t smem_optin(const void *k, size_t bytes)
+{
+    if (bytes <= 48 * 1024)
+        return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    struct Entry {
+        int dev;
+        const void *k;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static Entry done[256];
+    static int n = 0;
+    std::lock_guard<std::mutex> g(mu);
+    int i = 0;
+    while (i < n && !(done[i].dev == dev && done[i].k == k))
+        ++i;
+    if (i < n && done[i].bytes >= bytes)
+        return cudaSuccess;
+    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes)) != cudaSuccess)
+        return e;
+    if (i == n && n < 256)
+        done[n++] = Entry{dev, k, 0};
+    if (i < n)
+        done[i].bytes = bytes;
+    return cudaSuccess;
+}
+
 cudaError_t get_ffn_maps(const FfnArgs &a, FfnMaps *out)
 {
     Key k;

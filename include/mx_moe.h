@@ -66,7 +66,8 @@ typedef enum {
     MX_ERR_UNSUPPORTED = -3,    /* valid but unsupported shape / bit width / group     */
     MX_ERR_WORKSPACE = -4,      /* workspace too small or could not be allocated       */
     MX_ERR_CUDA = -5,           /* a CUDA runtime call failed                          */
-    MX_ERR_DEVICE_TIMEOUT = -6  /* a device-side bounded wait gave up                  */
+    MX_ERR_DEVICE_TIMEOUT = -6, /* a device-side bounded wait gave up                  */
+    MX_ERR_RANGE = -7           /* a device-side range check failed (see below)        */
 } mx_status;
 
 typedef enum { MX_F32 = 0, MX_BF16 = 1 } mx_dtype;
@@ -167,8 +168,21 @@ MX_API mx_status mx_moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  * Device-side error word of a workspace.  Kernels that wait on asynchronous
  * copies give up after a bounded time, record it in the workspace's first word
  * and skip their math; this call synchronises on `stream`, reads the word, and
- * returns MX_ERR_DEVICE_TIMEOUT if it is set (MX_OK otherwise).  The word stays
- * set until the workspace is re-initialised (mx_moe_workspace_init).
+ * returns MX_ERR_DEVICE_TIMEOUT if a wait gave up, MX_ERR_RANGE if a range
+ * check failed, MX_OK otherwise.  The word stays set until the workspace is
+ * re-initialised (mx_moe_workspace_init).
+ *
+ * Range of the single-launch decode path (T <= 4): its down projections are
+ * summed over the grid in 64-bit fixed point, so that the sum does not depend
+ * on the order of the additions.  With E = floor(log2(max |x|)) over the
+ * layer's tokens (x as the block reads it, after the optional rmsnorm), every
+ * partial sum v -- one expert slice's contribution to one output element,
+ * before the layer scalar -- is scaled by f = 2^(4 - 2E) (clamped to
+ * 2^[-100, 100]) and kept to 32 fractional bits at that scale: the absolute
+ * resolution is 2^-32 / f, about 2^-32 |y| / |x|^2.  A partial with
+ * |v f| >= 2^23 is left out of the sum and sets MX_ERR_RANGE.  For inputs of
+ * magnitude 4..8 (f = 1) that is |v| < 8.4e6 at a resolution of 2.3e-10.
+ * The other paths accumulate in fp32 and have no such limit.
  */
 MX_API mx_status mx_moe_workspace_check(const void *ws, void *stream);
 
@@ -189,7 +203,15 @@ MX_API mx_status mx_moe_workspace_check(const void *ws, void *stream);
  * The first call on each device resolves the array's address
  * (cudaGetSymbolAddress); make that first call outside any stream capture.
  * Every call clears the scratch it uses (cudaMemsetAsync on `stream`) before
- * the kernel.  Calls allocate nothing, host or device.  There is one scratch
+ * the kernel.  A call that succeeds (with the stage profiler off) makes no
+ * allocation of its own, host or device: no cudaMalloc, cudaFree or malloc,
+ * and no thread-local storage (whose first use on a host thread would be
+ * allocated lazily); the kernel parameters sit in one static block guarded by
+ * a lock, so concurrent host calls serialise on it.  The CUDA runtime itself
+ * may load the kernel's code on the first launch on a device, as for any
+ * kernel.  A call that fails records its message in the calling thread's
+ * message buffer (mx_last_error_string), which that thread's first error may
+ * allocate.  There is one scratch
  * array per device: calls that may overlap on the GPU (other streams, other
  * host threads) race on it and must be ordered by the caller.  A device-side
  * wait that gives up is not reported (use mx_moe_layer_forward_ex and

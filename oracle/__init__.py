@@ -203,6 +203,33 @@ def block_forward(layer, x: np.ndarray, residual: np.ndarray | None = None):
     return out, idx, w
 
 
+def block_forward_tokens(layer, x: np.ndarray, tokens=None, threads: int | None = None):
+    """``block_forward`` on the rows ``tokens`` of ``x`` (all rows if None),
+    split over host threads: each thread runs the plain single-threaded oracle
+    on its own share of the tokens (ctypes releases the GIL during the call,
+    and every token is independent of the others).  Returns (out, idx, w) for
+    the selected rows, in the order given."""
+    import concurrent.futures as cf
+    x = np.ascontiguousarray(x)
+    tok = np.arange(x.shape[0]) if tokens is None else np.asarray(tokens, dtype=np.int64)
+    n = len(tok)
+    threads = max(1, min(threads or (os.cpu_count() or 1), n))
+    parts = np.array_split(np.arange(n), threads)
+    out = np.zeros((n, x.shape[1]), dtype=x.dtype if x.dtype == np.uint16 else np.float32)
+    idx = np.zeros((n, layer.K), dtype=np.int32)
+    w = np.zeros((n, layer.K), dtype=np.float32)
+
+    def run(part):
+        if len(part):
+            o, i, ww = block_forward(layer, np.ascontiguousarray(x[tok[part]]))
+            out[part], idx[part], w[part] = o, i, ww
+
+    lib()
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(run, parts))
+    return out, idx, w
+
+
 def rmsnorm_bf16(x_bits: np.ndarray, eps: float = 1e-6) -> np.ndarray:
     x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
     T, D = x_bits.shape

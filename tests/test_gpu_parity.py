@@ -141,15 +141,29 @@ def test_skewed_decode_T64_full(orc, gu):
     check_block(orc, gu, cfg, layer, x)
 
 
-def _sample_tokens(T, n, seed):
-    rng = np.random.default_rng(seed)
-    return np.unique(np.concatenate([[0, T - 1], rng.choice(T, n, replace=False)]))
+def covering_tokens(counts, offsets, perm, K, T, tile=128):
+    """Tokens that put at least one output row through every work unit of the
+    grouped GEMMs: for each expert, the first slot of each 128-slot tile of its
+    slot range and its last slot; the first token of every 128-token tile (the
+    shared expert's units); and every token of the last, ragged, token tile."""
+    tok = set(range(((T - 1) // tile) * tile, T))
+    tok.update(range(0, T, tile))
+    for e in range(len(counts)):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        for a in range(lo, hi, tile):
+            tok.add(int(perm[a]) // K)
+        if hi > lo:
+            tok.add(int(perm[hi - 1]) // K)
+    return np.array(sorted(tok), dtype=np.int64)
 
 
 @pytest.mark.parametrize("ci", [2, 4])
-def test_prefill_route_exact_and_sampled_outputs(orc, gu, ci):
+def test_prefill_route_exact_and_full_outputs(orc, gu, ci):
     """Full-size prefill: every token's top-k, the counts and the permutation
-    exact (the oracle routes all T tokens); outputs on a sample of tokens."""
+    exact (the oracle routes all T tokens).  Outputs: every token of the
+    T=512 workload; at T=4096 the tokens that cover every (expert, 128-slot
+    tile) unit, every shared-expert token tile and the whole last token tile
+    (the oracle runs on all host cores)."""
     import expert_ffn_gb300 as mx
     cfg = synth.CONFIGS[ci]
     layer = synth.make_layer(cfg)
@@ -159,12 +173,133 @@ def test_prefill_route_exact_and_sampled_outputs(orc, gu, ci):
     ridx_all, rw_all = orc.topk_softmax(orc.router_logits(layer.router, gu.as_f32(x)), cfg.K)
     assert np.array_equal(idx, ridx_all)
     assert rel_l2(w, rw_all) <= 1e-4
-    ridx, _, _, _, perm, _ = gu.run_route(dev, x)
+    ridx, _, counts, offsets, perm, _ = gu.run_route(dev, x)
     rc, ro, rp = orc.permute(ridx_all, cfg.E)
     assert np.array_equal(ridx, ridx_all) and np.array_equal(perm, rp)
-    tok = _sample_tokens(cfg.T, 10 if ci == 2 else 6, ci)
-    ref, _, _ = orc.block_forward(layer, x[tok])
+    assert np.array_equal(counts, rc) and np.array_equal(offsets, ro)
+    tok = np.arange(cfg.T) if ci == 2 else covering_tokens(rc, ro, rp, cfg.K, cfg.T)
+    ref, ridx_t, _ = orc.block_forward_tokens(layer, x, tok)
+    assert np.array_equal(ridx_t, ridx_all[tok])
     check_out(out[tok], ref, cfg.act)
+
+
+# ------------------------------------------- routing edge cases and options
+
+def skewed_router_layer(cfg, hot=5, n_empty=16):
+    """The layer of ``cfg`` with its router rewritten so that, for activations
+    >= 0, expert ``hot`` (all router bytes 255, scale 2^-11, bias 0) has the
+    largest logit of every token and the ``n_empty`` experts after it (all
+    bytes 0, bias -0.03) have logits below every other expert's: they receive
+    no token.  The oracle's routing is checked to confirm it."""
+    layer = synth.make_layer(cfg)
+    r = layer.router
+    empty = [(hot + 1 + j) % cfg.E for j in range(n_empty)]
+    r.w[hot] = 0xFFFFFFFF
+    r.s[hot] = synth.f32_to_bf16_bits(np.full(r.s.shape[1], 2.0 ** -11, np.float32))
+    r.b[hot] = 0
+    for e in empty:
+        r.w[e] = 0
+        r.b[e] = synth.f32_to_bf16_bits(np.full(r.b.shape[1], -0.03, np.float32))
+    return layer, hot, empty
+
+
+def nonneg_x(cfg):
+    x = synth.make_x(cfg)
+    return (x & np.uint16(0x7FFF)) if x.dtype == np.uint16 else np.abs(x)
+
+
+@pytest.mark.parametrize("T", [3, 40, 200], ids=["single_launch_T3", "multi_launch_T40", "prefill_T200"])
+def test_empty_experts_and_one_expert_with_every_token(orc, gu, T):
+    """Sixteen of 64 experts receive no token and one expert receives every
+    token (more than one 128-slot tile at T = 200): the decode kernels at T = 3
+    and T = 40, the grouped tensor-core GEMMs at T = 200."""
+    import expert_ffn_gb300 as mx
+    cfg = synth.small_config(T=T, D=512, E=64, K=2, I=256, S=128, act="bf16", seed=400 + T)
+    layer, hot, empty = skewed_router_layer(cfg)
+    x = nonneg_x(cfg)
+    ridx, _ = orc.topk_softmax(orc.router_logits(layer.router, gu.as_f32(x)), cfg.K)
+    rc, _, _ = orc.permute(ridx, cfg.E)
+    assert rc[hot] == T and np.all(rc[empty] == 0)
+    mx.profile_enable(True)
+    try:
+        mx.profile_read(reset=True)
+        check_block(orc, gu, cfg, layer, x)
+        prof = mx.profile_read(reset=True)
+    finally:
+        mx.profile_enable(False)
+    if T > 64:
+        assert prof["down"][1] == 1, prof          # the grouped GEMMs ran
+    dev = mx.DeviceLayer(layer, mx.MX_BF16)
+    _, _, counts, _, _, _ = gu.run_route(dev, x)
+    assert np.array_equal(counts, rc)
+
+
+PES_CASES = [(2, 1), (2, 0), (24, 0), (130, 1)]
+
+
+@pytest.mark.parametrize("case", PES_CASES, ids=["single_launch_T2", "multi_launch_T2", "multi_launch_T24",
+                                                 "prefill_T130"])
+def test_per_expert_scale(orc, gu, case, monkeypatch):
+    """A per-expert scale multiplies each selected expert's softmax weight on
+    every path (router formula of the "Decode" section)."""
+    T, single = case
+    monkeypatch.setenv("MX_MOE_SINGLE_LAUNCH", str(single))
+    cfg = synth.small_config(T=T, D=384, E=32, K=4, I=192, S=128, act="bf16", seed=500 + T)
+    layer = synth.make_layer(cfg)
+    layer.per_expert_scale = np.random.default_rng(T).uniform(0.5, 2.0, cfg.E).astype(np.float32)
+    x = synth.make_x(cfg)
+    _, _, w, = check_block(orc, gu, cfg, layer, x)[1:]
+    _, rw_plain = orc.topk_softmax(orc.router_logits(layer.router, gu.as_f32(x)), cfg.K)
+    assert rel_l2(w, rw_plain) > 1e-2            # the scale did change the weights
+
+
+# --------------------------------- the decode path's fixed-point sums: range
+
+def check_scaled(got, ref):
+    g, r = got.astype(np.float64), ref.astype(np.float64)
+    assert np.all(np.isfinite(g))
+    assert rel_l2(g, r) <= 1e-4, rel_l2(g, r)
+    assert max_abs_rel(g, r) <= 2e-2
+
+
+@pytest.mark.parametrize("e", [-20, 20], ids=["x_times_2^-20", "x_times_2^20"])
+def test_fixed_point_range_follows_input(orc, gu, e):
+    """fp32 inputs scaled by 2^-20 (block outputs near 1e-10: far below the
+    fixed-point unit of unscaled inputs) and by 2^20 (outputs above 2^31)
+    through the single-launch decode kernel: the fp32 bars of the oracle."""
+    import expert_ffn_gb300 as mx
+    cfg = synth.small_config(T=4, D=256, E=16, K=2, I=128, S=128, act="f32", seed=600)
+    layer = synth.make_layer(cfg)
+    x = (synth.make_x(cfg) * np.float32(2.0 ** e)).astype(np.float32)
+    dev = mx.DeviceLayer(layer, mx.MX_F32)
+    out, idx, w = gu.run_block(dev, x)
+    ref, ridx, rw = orc.block_forward(layer, x)
+    assert np.array_equal(idx, ridx) and rel_l2(w, rw) <= 1e-4
+    check_scaled(out, ref)
+    if e > 0:
+        assert np.max(np.abs(ref)) > 2.0 ** 31
+
+
+def test_fixed_point_out_of_range_is_reported(orc, gu):
+    """A shared down projection with scales of 2^20 drives the partial sums
+    past the fixed-point range: the call reports MX_ERR_RANGE through the
+    workspace check; after re-initialising the workspace an ordinary call
+    matches the oracle again."""
+    import expert_ffn_gb300 as mx
+    cfg = synth.small_config(T=1, D=256, E=16, K=2, I=128, S=128, act="bf16", seed=601)
+    layer = synth.make_layer(cfg)
+    big = synth.make_layer(cfg)
+    big.shared_down.s[:] = synth.f32_to_bf16_bits(np.full(big.shared_down.s.shape, 2.0 ** 20, np.float32))
+    x = synth.make_x(cfg)
+    ws = gu.Workspace(mx.workspace_bytes(mx.DeviceLayer(layer, mx.MX_BF16).layout, 1))
+    with pytest.raises(mx.MxError) as ei:
+        gu.run_block(mx.DeviceLayer(big, mx.MX_BF16), x, ws=ws)
+    assert ei.value.status == -7                 # MX_ERR_RANGE
+    mx.workspace_init(ws.t, ws.nbytes)
+    out, idx, w = gu.run_block(mx.DeviceLayer(layer, mx.MX_BF16), x, ws=ws)
+    ref, ridx, rw = orc.block_forward(layer, x)
+    assert np.array_equal(idx, ridx)
+    check_out(out, ref, "bf16")
 
 
 def test_decode_stack_30_layers(orc, gu):

@@ -46,6 +46,10 @@ CASES = [
 @pytest.mark.gpu
 @pytest.mark.parametrize("case", range(len(CASES)), ids=["T2_bf16", "T4_f32_opts", "decode_T1_D2816"])
 def test_static_matches_workspace_call(case):
+    """Two static calls in a row equal the workspace call bit for bit, and
+    after a first (warm-up) static call they change neither the device's free
+    memory nor torch's allocator statistics: the calls themselves allocate
+    nothing on the device."""
     import torch
     from tests.gpu_util import Workspace, to_dev
 
@@ -57,11 +61,14 @@ def test_static_matches_workspace_call(case):
     res = to_dev(synth.make_x(cfg, T)[::-1].copy()) if opts else None
     s = torch.cuda.current_stream()
     ws = Workspace(mx.workspace_bytes(dev.layout, T))
+    out = torch.empty_like(x)
+    idx = torch.full((T, K), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((T, K), dtype=torch.float32, device="cuda")
 
     def run(static: bool):
-        out = torch.empty_like(x)
-        idx = torch.full((T, K), -1, dtype=torch.int32, device="cuda")
-        w = torch.zeros((T, K), dtype=torch.float32, device="cuda")
+        out.fill_(0)
+        idx.fill_(-1)
+        w.fill_(0)
         if static:
             mx.layer_forward_static(x, T, dev, out, idx, w, stream=s, residual=res, pre_rmsnorm=opts)
         else:
@@ -71,8 +78,13 @@ def test_static_matches_workspace_call(case):
 
     ref = run(False)
     mx.workspace_check(ws.t, s)
+    run(True)  # warm-up: the first static call on the device resolves the scratch address
+    free0 = torch.cuda.mem_get_info()[0]
+    stats0 = torch.cuda.memory_stats().get("num_alloc_retries", 0), torch.cuda.memory_allocated()
     for _ in range(2):  # two calls in a row: each leaves the scratch ready for the next
         got = run(True)
         for g, r in zip(got, ref):
             assert np.array_equal(g, r)
+    assert torch.cuda.mem_get_info()[0] == free0
+    assert (torch.cuda.memory_stats().get("num_alloc_retries", 0), torch.cuda.memory_allocated()) == stats0
     assert np.all(ref[1] >= 0)
