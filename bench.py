@@ -322,7 +322,7 @@ class Workload:
 
 def path_of(cfg):
     single = cfg.T <= PD_MAX_T and os.environ.get("MX_MOE_SINGLE_LAUNCH", "1") != "0"
-    prefill = cfg.T > 64 and cfg.act == "bf16" and os.environ.get("MX_MOE_PREFILL_GEMM", "1") != "0"
+    prefill = cfg.T > PD_MAX_T and cfg.act == "bf16" and os.environ.get("MX_MOE_PREFILL_GEMM", "1") != "0"
     return "prefill" if prefill else ("single" if single else "multi")
 
 

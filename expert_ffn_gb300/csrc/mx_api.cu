@@ -118,7 +118,7 @@ struct Plan {
     // single-launch decode path (T <= kPdMaxT)
     size_t pd_ctr, pd_logits, pd_y, pd_x;
     int pd_T;
-    // prefill path (T > kDecodeChunk, BF16)
+    // prefill path (T > kPrefillAbove, BF16)
     size_t pf;
     size_t total;
     int max_tiles_route;
@@ -157,7 +157,7 @@ Plan make_plan(const mx_moe_layout *L, int T_route, int T_ffn)
     p.pd_logits = take(Tp * E * 4);
     p.pd_y = take((size_t)kPdMaxLayers * Tp * D * 8);
     p.pd_x = take(Tp * D * es);
-    p.pf = (T_route > kDecodeChunk && L->act_dtype == MX_BF16)
+    p.pf = (T_route > kPrefillAbove && L->act_dtype == MX_BF16)
                ? take(pf_workspace_bytes(T_route, (int)D, (int)I, (int)S, (int)E, (int)K))
                : o;
     p.total = o;
@@ -535,8 +535,11 @@ mx_status forward_impl(const Call &c, cudaStream_t s, void *ws, size_t ws_bytes)
 {
     const int D = c.L->d_model, K = c.L->top_k;
     const size_t es = c.L->act_dtype == MX_F32 ? 4 : 2;
+    // BF16 with more than kPrefillAbove tokens: the grouped tensor-core GEMMs
+    // (MX_MOE_PREFILL_GEMM=0 in the environment keeps such calls on the decode
+    // kernels instead)
     const char *pf_env = getenv("MX_MOE_PREFILL_GEMM");
-    if (c.T > kDecodeChunk && c.L->act_dtype == MX_BF16 && !(pf_env && pf_env[0] == '0')) {
+    if (c.T > kPrefillAbove && c.L->act_dtype == MX_BF16 && !(pf_env && pf_env[0] == '0')) {
         const Plan p = make_plan(c.L, c.T, ffn_tokens(c.T));
         if (!ws || ws_bytes < p.total)
             return fail(MX_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes, p.total);

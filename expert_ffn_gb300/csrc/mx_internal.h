@@ -13,6 +13,9 @@ namespace mx {
 constexpr int kTileTokens = 64;
 // Largest T one pass of the decode path handles; longer inputs run in chunks.
 constexpr int kDecodeChunk = 64;
+// BF16 calls with more tokens than this run the grouped tensor-core GEMMs
+// (each expert's weights dequantized once per tile of up to 128 of its tokens).
+constexpr int kPrefillAbove = 4;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;
 constexpr int kMaxDim = 16384;
@@ -161,7 +164,7 @@ size_t pd_ctr_ints(int E, int n_layers);
 cudaError_t launch_pd(const PdParams &p, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
-// Prefill path (mx_prefill.cu): T > kDecodeChunk tokens with BF16 activations;
+// Prefill path (mx_prefill.cu): T > kPrefillAbove tokens with BF16 activations;
 // grouped GEMMs on tcgen05 tensor cores.
 
 // Arguments of the grouped-GEMM kernel (one per launch: gate/up or down).

@@ -208,12 +208,19 @@ def nonneg_x(cfg):
     return (x & np.uint16(0x7FFF)) if x.dtype == np.uint16 else np.abs(x)
 
 
-@pytest.mark.parametrize("T", [3, 40, 200], ids=["single_launch_T3", "multi_launch_T40", "prefill_T200"])
-def test_empty_experts_and_one_expert_with_every_token(orc, gu, T):
+EMPTY_CASES = [(3, "1"), (40, "0"), (40, "1"), (200, "1")]
+
+
+@pytest.mark.parametrize("case", EMPTY_CASES, ids=["single_launch_T3", "decode_kernels_T40", "grouped_gemm_T40",
+                                                   "grouped_gemm_T200"])
+def test_empty_experts_and_one_expert_with_every_token(orc, gu, case, monkeypatch):
     """Sixteen of 64 experts receive no token and one expert receives every
-    token (more than one 128-slot tile at T = 200): the decode kernels at T = 3
-    and T = 40, the grouped tensor-core GEMMs at T = 200."""
+    token (more than one 128-slot tile at T = 200): the single-launch decode
+    kernel at T = 3, the multi-launch decode kernels at T = 40
+    (MX_MOE_PREFILL_GEMM=0), the grouped tensor-core GEMMs at T = 40 and 200."""
     import expert_ffn_gb300 as mx
+    T, gemm = case
+    monkeypatch.setenv("MX_MOE_PREFILL_GEMM", gemm)
     cfg = synth.small_config(T=T, D=512, E=64, K=2, I=256, S=128, act="bf16", seed=400 + T)
     layer, hot, empty = skewed_router_layer(cfg)
     x = nonneg_x(cfg)
@@ -227,8 +234,10 @@ def test_empty_experts_and_one_expert_with_every_token(orc, gu, T):
         prof = mx.profile_read(reset=True)
     finally:
         mx.profile_enable(False)
-    if T > 64:
-        assert prof["down"][1] == 1, prof          # the grouped GEMMs ran
+    if T <= 4:
+        assert prof["route"][1] == 0 and prof["gate_up"][1] == 1, prof   # the single launch
+    else:
+        assert prof["route"][1] == 1 and prof["gate_up"][1] == 1 and prof["down"][1] == 1, prof
     dev = mx.DeviceLayer(layer, mx.MX_BF16)
     _, _, counts, _, _, _ = gu.run_route(dev, x)
     assert np.array_equal(counts, rc)
@@ -425,7 +434,10 @@ def test_decode_stack_paths_agree(orc, gu, monkeypatch):
 
 PREFILL_SHAPES = [
     # T, D, E, K, I, S
-    (65, 256, 16, 4, 128, 64),       # one past the decode range
+    (5, 256, 16, 4, 128, 64),        # one past the single-launch range
+    (16, 512, 32, 8, 192, 128),      # a batch of 16: many experts with one token
+    (64, 768, 64, 8, 128, 256),      # a full decode batch
+    (65, 256, 16, 4, 128, 64),
     (200, 320, 8, 3, 192, 320),      # D, I, S not multiples of 128; T ragged; experts with >128 slots
     (300, 512, 4, 2, 704, 128),      # few experts: several token tiles each
     (129, 1024, 64, 8, 256, 384),
@@ -435,7 +447,7 @@ PREFILL_SHAPES = [
 @pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=[f"T{s[0]}_D{s[1]}_E{s[2]}_K{s[3]}_I{s[4]}_S{s[5]}"
                                                        for s in PREFILL_SHAPES])
 def test_prefill_gemm_shapes(orc, gu, shape, monkeypatch):
-    """BF16 inputs with T > 64 run the grouped tensor-core GEMMs (stage
+    """BF16 inputs with T > 4 run the grouped tensor-core GEMMs (stage
     profiler: one routing launch, the GEMM sequence under gate/up); against
     the oracle, and against the decode kernels on the same inputs."""
     import expert_ffn_gb300 as mx
