@@ -272,6 +272,18 @@ mx_status run_pd(const PdIn *in, int n, int T, int pre_norm, float eps, const Pd
     P.cstride = 3 + P.E;
     P.logits = reinterpret_cast<float *>(ws + p.pd_logits);
     P.ybuf = reinterpret_cast<long long *>(ws + p.pd_y);
+    // Failure injection on the host, for tests of the bounded waits:
+    // MX_MOE_WAIT_LIMIT_US shortens every wait on another CTA (default 2 s),
+    // MX_MOE_HOLD_CTA=c keeps CTA c from arriving at the first logit exchange.
+    P.wait_ns = 2000000000ull;
+    P.hold_cta = -1;
+    if (const char *v = getenv("MX_MOE_WAIT_LIMIT_US")) {
+        const long long us = atoll(v);
+        if (us > 0)
+            P.wait_ns = (unsigned long long)us * 1000ull;
+    }
+    if (const char *v = getenv("MX_MOE_HOLD_CTA"))
+        P.hold_cta = atoi(v);
     P.sm = sm;
     for (int l = 0; l < n; ++l) {
         const PdIn &c = in[l];

@@ -243,7 +243,7 @@ __device__ __forceinline__ int *abort_word(const PdParams &p) { return p.ctr + p
 
 __device__ __forceinline__ void set_abort(const PdParams &p) { atomicExch(abort_word(p), 1); }
 
-// Spin until *c >= target.  False after kWaitLimitNs (error word set) or when
+// Spin until *c >= target.  False after p.wait_ns (error word set) or when
 // another CTA has given up.
 __device__ bool gwait(const int *c, int target, const PdParams &p)
 {
@@ -258,7 +258,7 @@ __device__ bool gwait(const int *c, int target, const PdParams &p)
         if ((it & 63u) == 63u) {
             if (ld_acquire(ab))
                 return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (global_ns() - t0 > p.wait_ns) {
                 atomicOr(p.err, kErrTimeout);
                 set_abort(p);
                 return false;
@@ -268,15 +268,20 @@ __device__ bool gwait(const int *c, int target, const PdParams &p)
 }
 
 // Producer-side wait: polls with a short sleep, so the waiting warp leaves the
-// issue slots of its scheduler to the consumer warps.
+// issue slots of its scheduler to the consumer warps.  Gives up after
+// p.wait_ns, or once any CTA has given up (its consumers may then never
+// release a slot or publish a routing).
 __device__ __forceinline__ bool pwait_sleepy(uint64_t *bar, uint32_t parity, const PdParams &p)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    const int *ab = abort_word(p);
+    for (unsigned it = 0; !mbar_try_wait(bar, parity); ++it) {
         __nanosleep(64);
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if ((it & 63u) == 63u && ld_acquire(ab))
+            return false;
+        if (global_ns() - t0 > p.wait_ns) {
             atomicOr(p.err, kErrTimeout);
             set_abort(p);
             return false;
@@ -1033,7 +1038,9 @@ __device__ void consumers(const PdParams &p, const Smem &s)
         PD_STAMP(l, 1);
         router_rows<NB>(p, L, s, rq, rsv, rbv);  // ends with a consumer barrier
         PD_STAMP(l, 2);
-        if (tid == 0) {
+        // (hold_cta: a CTA told by the host not to arrive at the first logit
+        // exchange, so that every other CTA's bounded wait runs out)
+        if (tid == 0 && !(l == 0 && C == p.hold_cta)) {
             __threadfence();
             red_add(ctr + 0, 1);
         }

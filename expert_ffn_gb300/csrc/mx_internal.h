@@ -154,6 +154,8 @@ struct PdParams {
     int cstride;           // 3 + E
     float *logits;         // [T][E]
     long long *ybuf;       // [n_layers][T][D] fixed-point sums of the down projections
+    unsigned long long wait_ns;  // bound of every wait on another CTA
+    int hold_cta;          // -1, or a CTA that does not arrive at the first logit exchange
     PdSmem sm;
     PdLayer L[kPdMaxLayers];
 };

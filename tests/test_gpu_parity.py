@@ -479,3 +479,32 @@ def test_prefill_residual_and_prenorm(orc, gu):
     ref, ridx, rw = orc.block_forward(layer, xn, residual=x)
     assert np.array_equal(idx, ridx)
     check_out(out, ref, "bf16")
+
+
+# ------------------------------------------- failure detection (no GPU fault)
+
+def test_device_wait_runs_out_and_is_reported(orc, gu, monkeypatch):
+    """A CTA held back (on the host's say-so) from the first logit exchange of
+    the single-launch decode kernel: every other CTA's bounded wait runs out
+    after 1 ms, the kernel returns, and the workspace check reports
+    MX_ERR_DEVICE_TIMEOUT (the failed eager-fill case of the "Decode" section:
+    the step is abandoned rather than emitting a result).  After the workspace
+    is re-initialised, an ordinary call matches the oracle again."""
+    import expert_ffn_gb300 as mx
+    cfg = synth.CONFIGS[0]
+    layer = synth.make_layer(cfg)
+    x = synth.make_x(cfg)
+    dev = mx.DeviceLayer(layer, mx.MX_F32)
+    ws = gu.Workspace(mx.workspace_bytes(dev.layout, cfg.T))
+    monkeypatch.setenv("MX_MOE_WAIT_LIMIT_US", "1000")
+    monkeypatch.setenv("MX_MOE_HOLD_CTA", "3")
+    with pytest.raises(mx.MxError) as ei:
+        gu.run_block(dev, x, ws=ws)
+    assert ei.value.status == -6                 # MX_ERR_DEVICE_TIMEOUT
+    monkeypatch.delenv("MX_MOE_WAIT_LIMIT_US")
+    monkeypatch.delenv("MX_MOE_HOLD_CTA")
+    mx.workspace_init(ws.t, ws.nbytes)
+    out, idx, w = gu.run_block(dev, x, ws=ws)
+    ref, ridx, rw = orc.block_forward(layer, x)
+    assert np.array_equal(idx, ridx)
+    check_out(out, ref, "f32")
