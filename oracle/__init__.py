@@ -48,7 +48,10 @@ class Layer(C.Structure):
                 ("router", QMat), ("shared_gate", QMat), ("shared_up", QMat), ("shared_down", QMat),
                 ("blob", C.c_void_p), ("record_stride", C.c_uint64),
                 ("off_w", C.c_uint64 * 3), ("off_s", C.c_uint64 * 3), ("off_b", C.c_uint64 * 3),
-                ("per_expert_scale", C.c_void_p)]
+                ("per_expert_scale", C.c_void_p),
+                ("expert_slot", C.c_void_p), ("n_slots", C.c_int32),
+                ("router_scale", C.c_void_p), ("post_norm", C.c_void_p), ("post_eps", C.c_float),
+                ("shared_expert_gate", C.c_void_p)]
 
 
 def lib():
@@ -105,6 +108,20 @@ def layer_struct(layer) -> Layer:
     for j, name in enumerate(("gate", "up", "down")):
         L.off_w[j], L.off_s[j], L.off_b[j] = o[name]
     L.per_expert_scale = _ptr(layer.per_expert_scale)
+    opt = lambda name, dt: _ptr(None if getattr(layer, name, None) is None  # noqa: E731
+                                else np.ascontiguousarray(getattr(layer, name), dtype=dt))
+    # the arrays must be the layer's own (contiguous, of the right dtype) so they outlive the struct
+    for name, dt in (("expert_slot", np.int16), ("router_scale", np.uint16), ("post_norm", np.uint16),
+                     ("shared_expert_gate", np.uint16)):
+        a = getattr(layer, name, None)
+        if a is not None:
+            assert a.dtype == dt and a.flags["C_CONTIGUOUS"], f"{name} must be contiguous {dt.__name__}"
+    L.expert_slot = opt("expert_slot", np.int16)
+    L.n_slots = int(getattr(layer, "n_slots", 0) or 0)
+    L.router_scale = opt("router_scale", np.uint16)
+    L.post_norm = opt("post_norm", np.uint16)
+    L.post_eps = float(getattr(layer, "post_eps", 1e-6))
+    L.shared_expert_gate = opt("shared_expert_gate", np.uint16)
     return L
 
 
@@ -181,6 +198,10 @@ def expert_ffn(gate, up, down, x: np.ndarray) -> np.ndarray:
     return y
 
 
+class ExpertNotResident(ValueError):
+    pass
+
+
 def block_forward(layer, x: np.ndarray, residual: np.ndarray | None = None):
     """Run the block on the tokens in ``x`` (fp32 or BF16 bits, [T, D]).
 
@@ -198,6 +219,8 @@ def block_forward(layer, x: np.ndarray, residual: np.ndarray | None = None):
     L = layer_struct(layer)
     rc = lib().oracle_block_forward(C.byref(L), _ptr(x), dtype, T, _ptr(residual), _ptr(out),
                                     _ptr(idx), _ptr(w))
+    if rc == -2:
+        raise ExpertNotResident("oracle_block_forward: a selected expert is not resident in the blob")
     if rc:
         raise ValueError("oracle_block_forward: bad arguments")
     return out, idx, w

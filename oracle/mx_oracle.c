@@ -240,12 +240,12 @@ void oracle_expert_ffn(const oracle_qmat *gate, const oracle_qmat *up, const ora
     free(u);
 }
 
-/* View of routed expert e inside the fixed-stride blob [Mference, ".gturbo
+/* View of record r inside the fixed-stride blob [Mference, ".gturbo
  * directory": 128 fixed-stride expert blobs per layer file, each sub-tensor
  * at its own offset]. */
-static void expert_mats(const oracle_layer *L, int e, oracle_qmat m[3])
+static void record_mats(const oracle_layer *L, int r, oracle_qmat m[3])
 {
-    const uint8_t *rec = L->blob + (uint64_t)e * L->record_stride;
+    const uint8_t *rec = L->blob + (uint64_t)r * L->record_stride;
     const int D = L->d_model, I = L->d_expert;
     for (int j = 0; j < 3; ++j) {
         m[j].w = (const uint32_t *)(rec + L->off_w[j]);
@@ -257,15 +257,61 @@ static void expert_mats(const oracle_layer *L, int e, oracle_qmat m[3])
     }
 }
 
+/* Record of expert e: the resident-set table when given [Mference, "Load and
+ * ownership": a GPU-visible expert-to-slot table, Int16 per expert, -1 for
+ * absent; slot n is the n-th fixed-stride blob], else record e.  -1 when the
+ * expert is not resident. */
+static int expert_record(const oracle_layer *L, int e)
+{
+    if (!L->expert_slot)
+        return e;
+    int r = L->expert_slot[e];
+    return (r >= 0 && r < L->n_slots) ? r : -1;
+}
+
+/* RMSNorm of one fp32 vector with a BF16 weight vector [Mference, "Decode",
+ * cb2 row: the layer tail applies the post-FFN norms].  READING: an RMSNorm
+ * with weight, as the pre-norms of the same family; canonical order as
+ * oracle_rmsnorm_bf16 (per group of 64 an fmaf chain of squares, groups
+ * ascending, r = 1/sqrtf(ss/D + eps)); y_d = (y_d * r) * w_d in fp32. */
+static void post_norm(float *y, int D, const uint16_t *w, float eps)
+{
+    float ss = 0.0f;
+    for (int g = 0; g < D / 64; ++g) {
+        float p = 0.0f;
+        for (int i = 0; i < 64; ++i)
+            p = fmaf(y[64 * g + i], y[64 * g + i], p);
+        ss = ss + p;
+    }
+    float r = 1.0f / sqrtf(ss / (float)D + eps);
+    for (int d = 0; d < D; ++d)
+        y[d] = (y[d] * r) * oracle_bf16_to_f32(w[d]);
+}
+
+/* Gate of the shared branch [Mference, pinned families: "a gated shared
+ * expert" (Qwen 3.6)].  READING: a learned vector g [D]; the gate is
+ * sigmoid(g . x) per token, the dot product an fmaf chain in column order,
+ * sigmoid(z) = 1 / (1 + expf(-z)). */
+static float shared_gate_value(const uint16_t *g, const float *x, int D)
+{
+    float z = 0.0f;
+    for (int i = 0; i < D; ++i)
+        z = fmaf(oracle_bf16_to_f32(g[i]), x[i], z);
+    return 1.0f / (1.0f + expf(-z));
+}
+
 /* The block on T tokens.
  *   router -> top-K -> softmax weights               [Mference, "Decode"]
  *   routed: sum_k w_k * expert_k(x)                   [Mference, "Metal execution"]
  *   shared: added without a routing weight            [Mference, "Why ... shape"]
  *   out = lambda * (shared + routed)                  [Mference, "Decode", cb2 row]
- * READING: the post-FFN norms of the layer tail are outside the block; the
- * router reads x as given (any pre-normalisation is the caller's); the
- * residual, when given, is added in fp32 before the one rounding to the
- * activation dtype. */
+ * Optional parts (each absent unless given): the router reads
+ * x * router_scale / sqrt(D) [Mference, "Decode", router formula, second
+ * line; READING: router_scale is a vector over the model dimension, the
+ * product (x_i * rs_i) * (1 / sqrtf(D)) in fp32 with no rounding to the
+ * activation dtype]; the shared branch times its gate; the post-FFN norm of
+ * the combined output before the layer scalar.  READING: the residual, when
+ * given, is added in fp32 before the one rounding to the activation dtype. */
 int oracle_block_forward(const oracle_layer *L, const void *x, int x_dtype, int T,
                          const void *residual, void *out,
                          int32_t *topk_idx, float *topk_w)
@@ -274,27 +320,48 @@ int oracle_block_forward(const oracle_layer *L, const void *x, int x_dtype, int 
     if (T < 0 || D % 64 || L->d_expert % 64 || K < 1 || K > E)
         return -1;
     float *xf = (float *)malloc(sizeof(float) * (size_t)T * D);
+    float *xr = (float *)malloc(sizeof(float) * (size_t)T * D);
     float *logits = (float *)malloc(sizeof(float) * (size_t)T * E);
     float *sh = (float *)malloc(sizeof(float) * (size_t)D);
     float *y = (float *)malloc(sizeof(float) * (size_t)D);
+    int rc = 0;
     for (long i = 0; i < (long)T * D; ++i)
         xf[i] = load_act(x, x_dtype, i);
+    if (L->router_scale) {
+        const float c = 1.0f / sqrtf((float)D);
+        for (long i = 0; i < (long)T * D; ++i)
+            xr[i] = (xf[i] * oracle_bf16_to_f32(L->router_scale[i % D])) * c;
+    } else {
+        memcpy(xr, xf, sizeof(float) * (size_t)T * D);
+    }
 
-    oracle_router_logits(&L->router, xf, T, logits);
+    oracle_router_logits(&L->router, xr, T, logits);
     oracle_topk_softmax(logits, T, E, K, L->per_expert_scale, topk_idx, topk_w);
 
-    for (int t = 0; t < T; ++t) {
+    for (int t = 0; t < T && rc == 0; ++t) {
         const float *xt = xf + (long)t * D;
         oracle_expert_ffn(&L->shared_gate, &L->shared_up, &L->shared_down, xt, sh);
+        if (L->shared_expert_gate) {
+            const float gv = shared_gate_value(L->shared_expert_gate, xt, D);
+            for (int d = 0; d < D; ++d)
+                sh[d] = gv * sh[d];
+        }
         float *acc = sh; /* acc starts as the shared branch */
         for (int k = 0; k < K; ++k) {
+            const int r = expert_record(L, topk_idx[(long)t * K + k]);
+            if (r < 0) {
+                rc = -2;
+                break;
+            }
             oracle_qmat m[3];
-            expert_mats(L, topk_idx[(long)t * K + k], m);
+            record_mats(L, r, m);
             oracle_expert_ffn(&m[0], &m[1], &m[2], xt, y);
             float w = topk_w[(long)t * K + k];
             for (int d = 0; d < D; ++d)
                 acc[d] = acc[d] + w * y[d];
         }
+        if (L->post_norm)
+            post_norm(acc, D, L->post_norm, L->post_eps);
         for (int d = 0; d < D; ++d) {
             float v = L->layer_scalar * acc[d];
             if (residual)
@@ -303,10 +370,11 @@ int oracle_block_forward(const oracle_layer *L, const void *x, int x_dtype, int 
         }
     }
     free(xf);
+    free(xr);
     free(logits);
     free(sh);
     free(y);
-    return 0;
+    return rc;
 }
 
 /* ------------------------------------------------------ RMSNorm and stack */

@@ -61,6 +61,20 @@ typedef struct {
     uint64_t record_stride;
     uint64_t off_w[3], off_s[3], off_b[3];       /* gate, up, down        */
     const float *per_expert_scale;               /* NULL = all ones       */
+    /* Optional parts of the layer (each NULL = absent):
+     *   expert_slot   [E]: record of expert e in the blob is expert_slot[e]
+     *                 (-1 = not resident), n_slots records; NULL = record e;
+     *   router_scale  BF16 [D]: the router reads x * router_scale / sqrt(D);
+     *   post_norm     BF16 [D]: the FFN output y becomes rmsnorm(y) * post_norm
+     *                 (eps post_eps) before the layer scalar and residual;
+     *   shared_expert_gate  BF16 [D]: the shared branch is scaled per token
+     *                 by sigmoid(shared_expert_gate . x). */
+    const int16_t *expert_slot;
+    int32_t n_slots;
+    const uint16_t *router_scale;
+    const uint16_t *post_norm;
+    float post_eps;
+    const uint16_t *shared_expert_gate;
 } oracle_layer;
 
 /* Activation dtypes: 0 = fp32, 1 = bf16 (uint16 bit patterns). */
@@ -90,7 +104,9 @@ void oracle_expert_ffn(const oracle_qmat *gate, const oracle_qmat *up, const ora
                        const float *x, float *y);
 
 /* The block: out[t] = residual[t] + lambda * (shared(x_t) + sum_k w_k * expert_k(x_t)),
- * rounded to the activation dtype.  residual may be NULL.  Returns 0 or -1. */
+ * rounded to the activation dtype (with the optional parts of the layer as
+ * above).  residual may be NULL.  Returns 0, -1 on bad arguments, or -2 if a
+ * selected expert is not resident in the blob (expert_slot). */
 int oracle_block_forward(const oracle_layer *L, const void *x, int x_dtype, int T,
                          const void *residual, void *out,
                          int32_t *topk_idx, float *topk_w);

@@ -88,6 +88,13 @@ class MoeLayer:
     offsets: dict                        # name -> (w_off, s_off, b_off)
     per_expert_scale: np.ndarray | None = None
     meta: dict = field(default_factory=dict)
+    # optional parts of the layer (None = absent)
+    expert_slot: np.ndarray | None = None       # int16 [E]: record of expert e (-1 = not resident)
+    n_slots: int = 0                            # records in the blob when expert_slot is set
+    router_scale: np.ndarray | None = None      # BF16 bits [D]
+    post_norm: np.ndarray | None = None         # BF16 bits [D]
+    post_eps: float = 1e-6
+    shared_expert_gate: np.ndarray | None = None  # BF16 bits [D]
 
     def expert(self, e: int) -> tuple[QMat, QMat, QMat]:
         """Views of expert e's (gate, up, down) inside the blob."""
