@@ -18,7 +18,7 @@ __all__ = ["MxError", "lib", "QLinear", "Ffn", "Sub", "Layout", "Options", "LAYO
            "workspace_bytes", "stack_workspace_bytes", "workspace_init", "layer_forward_static", "EXPORTED"]
 
 LAYOUT_MAGIC = 0x4D584D45
-LAYOUT_VERSION = 1
+LAYOUT_VERSION = 2
 MX_F32, MX_BF16 = 0, 1
 
 # Every symbol include/mx_moe.h declares.
@@ -51,7 +51,10 @@ class Layout(C.Structure):
     _fields_ = [("magic", C.c_uint32), ("version", C.c_uint32), ("d_model", C.c_int32), ("d_expert", C.c_int32),
                 ("n_experts", C.c_int32), ("top_k", C.c_int32), ("d_shared", C.c_int32), ("group", C.c_int32),
                 ("bits", C.c_int32), ("record_stride", C.c_uint64), ("gate", Sub), ("up", Sub), ("down", Sub),
-                ("act_dtype", C.c_int32), ("layer_scalar", C.c_float), ("per_expert_scale", C.c_void_p)]
+                ("act_dtype", C.c_int32), ("layer_scalar", C.c_float), ("per_expert_scale", C.c_void_p),
+                # version 2: optional parts of the layer (NULL = absent)
+                ("expert_slot", C.c_void_p), ("n_slots", C.c_int32), ("router_scale", C.c_void_p),
+                ("post_norm", C.c_void_p), ("post_eps", C.c_float), ("shared_expert_gate", C.c_void_p)]
 
 
 class Options(C.Structure):
@@ -129,7 +132,8 @@ def make_qlinear(w, s, b, rows: int, cols: int, bits: int) -> QLinear:
     return QLinear(_ptr(w), _ptr(s), _ptr(b), rows, cols, bits)
 
 
-def make_layout(D, I, E, K, S, stride, offsets, act_dtype, lam, per_expert_scale=None) -> Layout:
+def make_layout(D, I, E, K, S, stride, offsets, act_dtype, lam, per_expert_scale=None, expert_slot=None,
+                n_slots=0, router_scale=None, post_norm=None, post_eps=0.0, shared_expert_gate=None) -> Layout:
     L = Layout()
     L.magic, L.version = LAYOUT_MAGIC, LAYOUT_VERSION
     L.d_model, L.d_expert, L.n_experts, L.top_k, L.d_shared = D, I, E, K, S
@@ -141,6 +145,12 @@ def make_layout(D, I, E, K, S, stride, offsets, act_dtype, lam, per_expert_scale
     L.act_dtype = act_dtype
     L.layer_scalar = lam
     L.per_expert_scale = _ptr(per_expert_scale)
+    L.expert_slot = _ptr(expert_slot)
+    L.n_slots = n_slots if expert_slot is not None else 0
+    L.router_scale = _ptr(router_scale)
+    L.post_norm = _ptr(post_norm)
+    L.post_eps = post_eps
+    L.shared_expert_gate = _ptr(shared_expert_gate)
     return L
 
 
@@ -149,9 +159,12 @@ class DeviceLayer:
 
     ``host`` is any object with attributes D, E, K, I, S, lam, router, shared_gate,
     shared_up, shared_down (each with .w .s .b .rows .cols .bits numpy arrays),
-    blob, stride, offsets and optionally per_expert_scale."""
+    blob, stride, offsets and optionally per_expert_scale and the layer's
+    optional parts expert_slot (int16 [E]) with n_slots, router_scale,
+    post_norm (with post_eps) and shared_expert_gate (BF16 bits [D])."""
 
     def __init__(self, host, act_dtype: int, device="cuda"):
+        import numpy as np
         import torch
         self.host = host
         self.act_dtype = act_dtype
@@ -173,8 +186,18 @@ class DeviceLayer:
         assert self.blob.data_ptr() % 256 == 0
         pes = getattr(host, "per_expert_scale", None)
         self.pes = None if pes is None else torch.from_numpy(pes.astype("float32")).to(device)
+        def opt(name, dtype):
+            a = getattr(host, name, None)
+            return None if a is None else torch.from_numpy(np.ascontiguousarray(a, dtype=dtype)).to(device)
+
+        self.expert_slot = opt("expert_slot", np.int16)
+        self.router_scale = opt("router_scale", np.uint16)
+        self.post_norm = opt("post_norm", np.uint16)
+        self.shared_expert_gate = opt("shared_expert_gate", np.uint16)
         self.layout = make_layout(host.D, host.I, host.E, host.K, host.S, host.stride, host.offsets, act_dtype,
-                                  host.lam, self.pes)
+                                  host.lam, self.pes, self.expert_slot, int(getattr(host, "n_slots", 0) or 0),
+                                  self.router_scale, self.post_norm, float(getattr(host, "post_eps", 0.0)),
+                                  self.shared_expert_gate)
 
     def set_layer_scalar(self, lam: float):
         self.layout.layer_scalar = lam

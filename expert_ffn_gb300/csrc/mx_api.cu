@@ -9,6 +9,7 @@
 #include "mx_moe.h"
 #include "mx_internal.h"
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -61,7 +62,7 @@ mx_status check_layout(const mx_moe_layout *L)
         return fail(MX_ERR_INVALID_ARG, "layout is NULL");
     if (L->magic != MX_MOE_LAYOUT_MAGIC)
         return fail(MX_ERR_INVALID_ARG, "layout magic 0x%08x is not 0x%08x", L->magic, MX_MOE_LAYOUT_MAGIC);
-    if (L->version != MX_MOE_LAYOUT_VERSION)
+    if (L->version != 1u && L->version != MX_MOE_LAYOUT_VERSION)
         return fail(MX_ERR_INVALID_ARG, "layout version %u is not supported", L->version);
     const int D = L->d_model, I = L->d_expert, E = L->n_experts, K = L->top_k, S = L->d_shared;
     if (L->group != 64)
@@ -102,8 +103,45 @@ mx_status check_layout(const mx_moe_layout *L)
     }
     if (L->per_expert_scale && !aligned(L->per_expert_scale, 4))
         return fail(MX_ERR_ALIGNMENT, "per_expert_scale must be 4-byte aligned");
+    if (L->version >= 2u) {
+        if (L->expert_slot) {
+            if (!aligned(L->expert_slot, 2))
+                return fail(MX_ERR_ALIGNMENT, "expert_slot must be 2-byte aligned");
+            if (L->n_slots < 1 || L->n_slots > 32767)
+                return fail(MX_ERR_INVALID_ARG, "n_slots %d must be in [1, 32767] with an expert_slot table",
+                            L->n_slots);
+        }
+        const void *vecs[3] = {L->router_scale, L->post_norm, L->shared_expert_gate};
+        const char *vnames[3] = {"router_scale", "post_norm", "shared_expert_gate"};
+        for (int j = 0; j < 3; ++j)
+            if (vecs[j] && !aligned(vecs[j], 16))
+                return fail(MX_ERR_ALIGNMENT, "%s must be 16-byte aligned", vnames[j]);
+        if (L->post_norm && !(L->post_eps >= 0.0f))
+            return fail(MX_ERR_INVALID_ARG, "post_eps must be >= 0");
+    }
     return MX_OK;
 }
+
+// The optional parts of a layout (none for a version-1 layout).
+LayerExt ext_of(const mx_moe_layout *L)
+{
+    LayerExt x{};
+    x.n_slots = L->n_experts;
+    x.rcoef = 1.0f / sqrtf((float)L->d_model);
+    if (L->version >= 2u) {
+        x.slot = L->expert_slot;
+        if (x.slot)
+            x.n_slots = L->n_slots;
+        x.router_scale = L->router_scale;
+        x.post_norm = L->post_norm;
+        x.post_eps = L->post_eps;
+        x.shared_gate = L->shared_expert_gate;
+    }
+    return x;
+}
+
+// The parts only the single-launch and grouped-GEMM paths implement.
+bool ext_needs_new_paths(const LayerExt &x) { return x.router_scale || x.post_norm || x.shared_gate; }
 
 bool overlap(const void *a, size_t na, const void *b, size_t nb)
 {
@@ -289,11 +327,14 @@ mx_status run_pd(const PdIn *in, int n, int T, int pre_norm, float eps, const Pd
         const PdIn &c = in[l];
         const mx_moe_layout *L = c.L;
         PdLayer &d = P.L[l];
+        const LayerExt x = ext_of(L);
         FfnArgs f{};
         f.D = L->d_model;
         f.I = L->d_expert;
         f.S = L->d_shared;
         f.E = L->n_experts;
+        f.slot = x.slot;
+        f.n_slots = x.n_slots;
         f.blob = static_cast<const uint8_t *>(c.blob);
         f.stride = L->record_stride;
         const mx_sub *subs[3] = {&L->gate, &L->up, &L->down};
@@ -329,6 +370,13 @@ mx_status run_pd(const PdIn *in, int n, int T, int pre_norm, float eps, const Pd
         d.residual = c.residual;
         d.res_mode = c.res_mode;
         d.lam = L->layer_scalar;
+        d.slot = x.slot;
+        d.n_slots = x.n_slots;
+        d.router_scale = x.router_scale;
+        d.post_norm = x.post_norm;
+        d.shared_gate = x.shared_gate;
+        d.post_eps = x.post_eps;
+        d.rcoef = x.rcoef;
     }
     prof_begin(kStageGateUp, s);
     cudaError_t e = launch_pd(P, s);
@@ -448,6 +496,9 @@ mx_status run_pass(const void *x, int T, const mx_qlinear *router, const mx_ffn 
     f.S = L->d_shared;
     f.E = L->n_experts;
     f.K = L->top_k;
+    const LayerExt ext = ext_of(L);
+    f.slot = ext.slot;
+    f.n_slots = ext.n_slots;
     f.blob = static_cast<const uint8_t *>(blob);
     f.stride = L->record_stride;
     const mx_sub *subs[3] = {&L->gate, &L->up, &L->down};
@@ -529,6 +580,9 @@ mx_status run_prefill(const Call &c, const Plan &p, uint8_t *ws, cudaStream_t s)
     f.err = ra.err;
     f.ws = ws + p.pf;
     f.n_cta = num_sms();
+    f.ext = ext_of(L);
+    ra.router_scale = f.ext.router_scale;
+    ra.rcoef = f.ext.rcoef;
     PfPrepared pp;
     prof_begin(kStageRoute, s);
     cudaError_t e = launch_prefill_prepare(f, &pp, s);
@@ -573,6 +627,11 @@ mx_status forward_impl(const Call &c, cudaStream_t s, void *ws, size_t ws_bytes)
         const int pre = (c.opt && c.opt->pre_rmsnorm) ? 1 : 0;
         return run_pd(&in, 1, c.T, pre, c.opt ? c.opt->rms_eps : 0.0f, sm, n_cta, p, w, s);
     }
+    if (ext_needs_new_paths(ext_of(c.L)))
+        return fail(MX_ERR_UNSUPPORTED, "router_scale, post_norm and shared_expert_gate need the single-launch "
+                                        "decode path (T <= %d) or the grouped GEMMs (BF16, T > %d); this call "
+                                        "(T=%d, %s) would run the multi-launch decode kernels",
+                    kPdMaxT, kPrefillAbove, c.T, c.L->act_dtype == MX_BF16 ? "bf16" : "fp32");
     for (int t0 = 0; t0 < c.T; t0 += kDecodeChunk) {
         const int n = c.T - t0 < kDecodeChunk ? c.T - t0 : kDecodeChunk;
         mx_moe_options o{};
@@ -619,6 +678,7 @@ const char *mx_status_string(mx_status s)
     case MX_ERR_CUDA: return "MX_ERR_CUDA";
     case MX_ERR_DEVICE_TIMEOUT: return "MX_ERR_DEVICE_TIMEOUT";
     case MX_ERR_RANGE: return "MX_ERR_RANGE";
+    case MX_ERR_NOT_RESIDENT: return "MX_ERR_NOT_RESIDENT";
     }
     return "MX_ERR_UNKNOWN";
 }
@@ -665,6 +725,8 @@ mx_status mx_moe_workspace_check(const void *ws, void *stream)
         return cuda_fail(e, "reading the workspace error word");
     if (word & 1u)
         return fail(MX_ERR_DEVICE_TIMEOUT, "a device-side wait gave up (error word 0x%x)", word);
+    if (word & 4u)
+        return fail(MX_ERR_NOT_RESIDENT, "a selected expert has no record in the blob (error word 0x%x)", word);
     if (word != 0)
         return fail(MX_ERR_RANGE, "a partial sum fell outside the fixed-point range of the decode path "
                                   "(error word 0x%x)", word);
@@ -781,6 +843,8 @@ mx_status mx_moe_route(const void *x, int T, const mx_qlinear *router, const mx_
         return fail(MX_ERR_INVALID_ARG, "T=%d is negative", T);
     if ((st = check_qlinear(router, "router", layout->n_experts, layout->d_model, 8)) != MX_OK)
         return st;
+    if (ext_of(layout).router_scale)
+        return fail(MX_ERR_UNSUPPORTED, "mx_moe_route does not take a layout with router_scale");
     if (T == 0)
         return MX_OK;
     if (!x || !topk_idx || !topk_w || !counts || !offsets || !perm)

@@ -103,6 +103,21 @@ __device__ __forceinline__ float byte_f(uint32_t w)
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr unsigned kErrTimeout = 1u;  // a bounded wait gave up
 constexpr unsigned kErrRange = 2u;    // a value outside a fixed-point range (left out)
+constexpr unsigned kErrAbsent = 4u;   // a selected expert has no record in the blob
+
+// Record of expert e in the blob: through the resident-set table when there
+// is one, else e.  An expert with no record sets kErrAbsent in *err and reads
+// record 0 (the call's outputs are then not the block's; the error word says so).
+__device__ __forceinline__ int expert_record(const int16_t *slot, int n_slots, int e, unsigned *err)
+{
+    if (!slot)
+        return e;
+    const int r = __ldg(slot + e);
+    if (r >= 0 && r < n_slots)
+        return r;
+    atomicOr(err, kErrAbsent);
+    return 0;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 

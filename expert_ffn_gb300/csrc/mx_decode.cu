@@ -172,6 +172,7 @@ struct Rt {  // routing of the current layer (computed by the consumer warps)
     float *slot_w;    // [T*K] (first the selected logits, then the weights)
     int *emap;        // [E] expert -> active index
     uint32_t *emask;  // [16]
+    int *act_r;       // [amax] blob record of each active expert
 };
 
 struct Smem {
@@ -191,6 +192,8 @@ struct Smem {
     float *rn, *xsc;       // [T] rmsnorm factors, x plane scales
     int *vmax;             // [T] plane maxima (float bits)
     float *yfx;            // [2] fixed-point factor of the layer's y and its inverse
+    float *gv;             // [T] shared-branch gate of each token (with a gate vector)
+    float *pnr;            // [T] post-FFN norm factors (with a post-norm weight)
     int *flag;             // [4]
     uint8_t *zero;         // 16 zero bytes
     Rt rt;
@@ -223,6 +226,8 @@ __device__ __forceinline__ Smem carve(uint8_t *sm, const PdParams &p)
     s.ufo = m + 20;
     s.vmax = reinterpret_cast<int *>(m + 24);  // [T]
     s.yfx = m + 28;
+    s.gv = m + 32;
+    s.pnr = m + 36;
     int *r = reinterpret_cast<int *>(sm + o.rt);
     const int amax = TK < p.E ? TK : p.E;
     s.rt.n_act = r;
@@ -233,6 +238,7 @@ __device__ __forceinline__ Smem carve(uint8_t *sm, const PdParams &p)
     s.rt.slot_e = s.rt.act_slot + 4 * amax;
     s.rt.slot_w = reinterpret_cast<float *>(s.rt.slot_e + TK);
     s.rt.emap = reinterpret_cast<int *>(s.rt.slot_w + TK);
+    s.rt.act_r = s.rt.emap + p.E;
     s.zero = sm + o.zero;
     return s;
 }
@@ -534,7 +540,7 @@ __device__ __forceinline__ void store_planes(uint8_t *dst, bool per_slot, int nv
 // x_l (xraw) -> xq (optionally rmsnorm'd, rounded to the act dtype), its group
 // sums in the canonical order (the router's X), and its e4m3 planes.
 template <int NB>
-__device__ void prologue(const PdParams &p, const Smem &s)
+__device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
 {
     constexpr int es = NB == 1 ? 2 : 4;
     const int tid = threadIdx.x, lane = tid & 31, T = p.T, D = p.D, GD = D / 64;
@@ -695,6 +701,35 @@ __device__ void prologue(const PdParams &p, const Smem &s)
             *reinterpret_cast<uint2 *>(s.xpl + off) = pl[q];
         }
     }
+    if (L.shared_gate) {
+        // shared-branch gate sigmoid(g . x): per group an fma chain, then the
+        // groups in order
+        for (int i = tid; i < T * GD; i += kCT) {
+            const int t = i / GD, g = i - t * GD;
+            float v[64];
+            ld64(s.xq, t, g, v);
+            const uint4 *gp = reinterpret_cast<const uint4 *>(L.shared_gate + g * 64);
+            float q = 0.f;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const uint4 w = __ldg(gp + ch);
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    q = fmaf(__uint_as_float(u[j] << 16), v[8 * ch + 2 * j], q);
+                    q = fmaf(__uint_as_float(u[j] & 0xFFFF0000u), v[8 * ch + 2 * j + 1], q);
+                }
+            }
+            s.pr[i] = q;
+        }
+        csync();
+        if (tid < T) {
+            float z = 0.f;
+            for (int g = 0; g < GD; ++g)
+                z = z + s.pr[tid * GD + g];
+            s.gv[tid] = 1.0f / (1.0f + expf(-z));
+        }
+    }
     csync();
 }
 
@@ -709,6 +744,9 @@ __device__ void router_rows(const PdParams &p, const PdLayer &L, const Smem &s, 
     float *P = s.pr;            // [GD][T]
     float *sv = s.pr + GD * T;  // [GD]
     float *bv = sv + GD;        // [GD]
+    float *xx = bv + GD;        // [GD][T] group sums of the scaled input (with router_scale)
+    // With router_scale the router reads (x_i * rs_i) * rcoef in fp32.
+    const bool scaled = L.router_scale != nullptr;
     for (int r = C; r < p.E; r += NC) {
         if (r != C && tid < GD) {
             const uint4 *q = reinterpret_cast<const uint4 *>(L.rw + (size_t)r * (D / 4) + (size_t)tid * 16);
@@ -722,7 +760,52 @@ __device__ void router_rows(const PdParams &p, const PdLayer &L, const Smem &s, 
             const int g = tid;
             sv[g] = rsv;
             bv[g] = rbv;
-            for (int t = 0; t < T; ++t) {
+            for (int t = 0; t < T && scaled; ++t) {
+                // 8 columns at a time: the scaled values (x_i * rs_i) * rcoef,
+                // their sum and the dot product, both in column order
+                const uint8_t *xr = s.xq + ((size_t)t * D + g * 64) * es;
+                const uint4 *rp = reinterpret_cast<const uint4 *>(L.router_scale + g * 64);
+                float X = 0.f, acc = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    float xv[8];
+                    if constexpr (es == 2) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(xr + 16 * ch);
+                        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            xv[2 * q] = __uint_as_float(u[q] << 16);
+                            xv[2 * q + 1] = __uint_as_float(u[q] & 0xFFFF0000u);
+                        }
+                    } else {
+                        const float4 a = *reinterpret_cast<const float4 *>(xr + 32 * ch);
+                        const float4 b = *reinterpret_cast<const float4 *>(xr + 32 * ch + 16);
+                        xv[0] = a.x; xv[1] = a.y; xv[2] = a.z; xv[3] = a.w;
+                        xv[4] = b.x; xv[5] = b.y; xv[6] = b.z; xv[7] = b.w;
+                    }
+                    const uint4 s4 = __ldg(rp + ch);
+                    const uint32_t su[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float sc = __uint_as_float((j & 1) ? (su[j >> 1] & 0xFFFF0000u) : (su[j >> 1] << 16));
+                        xv[j] = __fmul_rn(__fmul_rn(xv[j], sc), L.rcoef);
+                        X = X + xv[j];
+                    }
+                    const uint4 r4 = rq[ch >> 1];
+                    const uint32_t w0 = (ch & 1) ? r4.z : r4.x, w1 = (ch & 1) ? r4.w : r4.y;
+                    acc = fmaf(byte_f<0>(w0), xv[0], acc);
+                    acc = fmaf(byte_f<1>(w0), xv[1], acc);
+                    acc = fmaf(byte_f<2>(w0), xv[2], acc);
+                    acc = fmaf(byte_f<3>(w0), xv[3], acc);
+                    acc = fmaf(byte_f<0>(w1), xv[4], acc);
+                    acc = fmaf(byte_f<1>(w1), xv[5], acc);
+                    acc = fmaf(byte_f<2>(w1), xv[6], acc);
+                    acc = fmaf(byte_f<3>(w1), xv[7], acc);
+                }
+                xx[g * T + t] = X;
+                P[g * T + t] = acc;
+            }
+            for (int t = 0; t < T && !scaled; ++t) {
                 float xv[64];
                 const uint8_t *xr = s.xq + ((size_t)t * D + g * 64) * es;
 #pragma unroll
@@ -766,7 +849,7 @@ __device__ void router_rows(const PdParams &p, const PdLayer &L, const Smem &s, 
                     a[j] = sv[g];
                     b[j] = P[g * T + tid];
                     c[j] = bv[g];
-                    d[j] = s.xg[tid * GD + g];
+                    d[j] = scaled ? xx[g * T + tid] : s.xg[tid * GD + g];
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
@@ -861,6 +944,7 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
         for (uint32_t b = bits; b; b &= b - 1u, ++j) {
             const int e = 32 * lane + __ffs(b) - 1;
             rt.act_e[j] = e;
+            rt.act_r[j] = expert_record(L.slot, L.n_slots, e, p.err);
             rt.act_n[j] = 0;
             rt.emap[e] = j;
         }
@@ -959,7 +1043,7 @@ __device__ void producer(const PdParams &p, const Smem &s)
             break;
         const int nr = *s.rt.n_act * GI;
         for (int r = first_routed(C, NC, GS); r < nr && ok; r += NC)
-            ok = issue_unit(L, false, s.rt.act_e[r / GI], r % GI);
+            ok = issue_unit(L, false, s.rt.act_r[r / GI], r % GI);
     }
     // Leave no copy in flight: wait (bounded) for the last item of every slot.
     __syncwarp();
@@ -1034,7 +1118,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 dst[i] = __ldg(src + i);
             csync();
         }
-        prologue<NB>(p, s);
+        prologue<NB>(p, L, s);
         PD_STAMP(l, 1);
         router_rows<NB>(p, L, s, rq, rsv, rbv);  // ends with a consumer barrier
         PD_STAMP(l, 2);
@@ -1068,7 +1152,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                     sp = L.ss[2] + u;
                     bq = L.sb[2] + u;
                 } else {
-                    const uint8_t *rec = L.blob + (uint64_t)s.rt.act_e[j] * L.stride;
+                    const uint8_t *rec = L.blob + (uint64_t)s.rt.act_r[j] * L.stride;
                     sp = reinterpret_cast<const uint16_t *>(rec + L.off_s[2]) + u;
                     bq = reinterpret_cast<const uint16_t *>(rec + L.off_b[2]) + u;
                 }
@@ -1114,6 +1198,8 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                         float h = gelu_tanh(ag) * au;
                         if (!shared)
                             h *= s.rt.slot_w[oslot];
+                        else if (L.shared_gate)
+                            h *= s.gv[ot];
                         s.uh[(8 * warp + gid) * 4 + c] = h;
                     }
                 }
@@ -1249,6 +1335,28 @@ __device__ void consumers(const PdParams &p, const Smem &s)
         // d_model <= 3072, T = 1)
         constexpr int kYB = NB == 1 ? 12 : 6;
         const float yinv = s.yfx[1];
+        if (L.post_norm) {
+            // post-FFN norm factor of each token: per group of 64 an fma chain
+            // of squares, then the groups in order
+            for (int i = tid; i < T * GD; i += kCT) {
+                const long long *yp = y + (size_t)i * 64;  // token i / GD, group i % GD
+                float q = 0.f;
+#pragma unroll 16
+                for (int k2 = 0; k2 < 64; ++k2) {
+                    const float v = from_fix(__ldcg(yp + k2)) * yinv;
+                    q = fmaf(v, v, q);
+                }
+                s.pr[i] = q;
+            }
+            csync();
+            if (tid < T) {
+                float ss = 0.f;
+                for (int g = 0; g < GD; ++g)
+                    ss = ss + s.pr[tid * GD + g];
+                s.pnr[tid] = 1.0f / sqrtf(ss / (float)D + L.post_eps);
+            }
+            csync();
+        }
         for (int i0 = 0; i0 < T * D; i0 += kYB * kCT) {
             long long yq[kYB];
 #pragma unroll
@@ -1261,7 +1369,11 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             const int i = i0 + tid + j * kCT;
             if (i >= T * D)
                 break;
-            const float yv = from_fix(yq[j]) * yinv;
+            float yv = from_fix(yq[j]) * yinv;
+            if (L.post_norm) {
+                const int t = i / D;
+                yv = __fmul_rn(__fmul_rn(yv, s.pnr[t]), bf2f(__ldg(L.post_norm + (i - t * D))));
+            }
             float res = 0.f;
             if (L.res_mode == 1)
                 res = es == 2 ? bf2f(reinterpret_cast<const uint16_t *>(s.xraw)[i])
@@ -1349,7 +1461,7 @@ bool pd_plan(int T, int D, int I, int S, int E, int K, int act, int n_cta, int s
     const int NB = act == 0 ? 2 : 1;
     const int GD = D / 64, TK = T * K, amax = TK < E ? TK : E;
     const int es = act == 1 ? 2 : 4;
-    const size_t scratch = (size_t)4 * std::max((size_t)T * GD, (size_t)GD * (T + 2));
+    const size_t scratch = (size_t)4 * std::max((size_t)T * GD, (size_t)GD * (2 * T + 2));
     for (int nr = 8; nr >= 3; --nr) {
         PdSmem o{};
         o.NR = nr;
@@ -1369,9 +1481,9 @@ bool pd_plan(int T, int D, int I, int S, int E, int K, int act, int n_cta, int s
         o.upl = take((size_t)4 * 256);
         o.dss = take((size_t)2 * 2 * (D / 4) * 2);
         o.lg = take((size_t)T * E * 4);
-        o.rt = take((size_t)4 * (20 + 6 * amax + 2 * TK + E));
+        o.rt = take((size_t)4 * (20 + 7 * amax + 2 * TK + E));
         o.pr = take(scratch);
-        o.misc = take((size_t)4 * (24 + 4 + 4));
+        o.misc = take((size_t)4 * 48);
         o.zero = take(16);
         o.total = (int)off;
         if ((long long)off <= smem_max) {

@@ -176,7 +176,7 @@ __device__ __forceinline__ GuItem gu_item(const FfnArgs &a, const GuLaunch &L, c
     } else {
         const int j = item - L.n_shared, ti = j / (a.I / 8), rb = j % (a.I / 8);
         it.routed = 1;
-        it.e = m.tiles[3 * ti];
+        it.e = expert_record(a.slot, a.n_slots, m.tiles[3 * ti], a.err);
         it.p0 = m.tiles[3 * ti + 1];
         it.ntok = m.tiles[3 * ti + 2] - it.p0;
         it.j0 = rb * 8;
@@ -394,7 +394,7 @@ __device__ __forceinline__ DnUnit dn_unit(const FfnArgs &a, const Meta &m, int u
     } else {
         const int ti = u - 1;
         d.shared_unit = 0;
-        d.e = m.tiles[3 * ti];
+        d.e = expert_record(a.slot, a.n_slots, m.tiles[3 * ti], a.err);
         d.p0 = m.tiles[3 * ti + 1];
         d.ntok = m.tiles[3 * ti + 2] - d.p0;
         d.cols = a.I;

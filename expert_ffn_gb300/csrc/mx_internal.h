@@ -46,10 +46,25 @@ struct RouteArgs {
     int logits_only;        // 1: stop after the logits
     int cluster;            // 1: one thread-block cluster; CTA 0 gathers the logits and routes
     unsigned *err;          // device error word (bounded waits that gave up)
+    // large router only: its input is x * router_scale * rcoef (XG then holds
+    // the group sums of that product); nullable
+    const uint16_t *router_scale;
+    float rcoef;            // 1 / sqrtf(D), computed on the host
+};
+
+// Optional parts of a layer (layout version 2; all absent for version 1).
+struct LayerExt {
+    const int16_t *slot;         // resident-set table [E], nullable
+    int n_slots;                 // records in the blob (E without a table)
+    const uint16_t *router_scale, *post_norm, *shared_gate;  // BF16 [D], nullable
+    float post_eps;
+    float rcoef;                 // 1 / sqrtf(D) (host-rounded, as the oracle's)
 };
 
 struct FfnArgs {
     int T, D, I, S, E, K;
+    const int16_t *slot;                    // resident-set table, nullable
+    int n_slots;                            // records in the blob
     const uint8_t *blob;
     uint64_t stride;
     uint64_t off_w[3], off_s[3], off_b[3];  // gate, up, down inside a record
@@ -144,6 +159,12 @@ struct PdLayer {
     const void *residual;  // res_mode 2
     float lam;
     int res_mode;          // 0 none, 1 the layer's input x, 2 `residual`
+    // optional parts (LayerExt): resident-set table, router input scale,
+    // post-FFN norm weight, shared-branch gate
+    const int16_t *slot;
+    int n_slots;
+    const uint16_t *router_scale, *post_norm, *shared_gate;
+    float post_eps, rcoef;
 };
 
 struct PdParams {
@@ -182,6 +203,8 @@ struct PfArgs {
     const float *xsc;       // [T] 2^-k of each token's FP16 scale
     const uint8_t *blob;
     uint64_t stride;
+    const int16_t *slot;    // resident-set table, nullable
+    int n_slots;            // records in the blob
     uint64_t off_s[3], off_b[3];
     const uint16_t *ss[3], *sb[3];
     void *H, *Hs;           // FP16 [T*K][I], [T][S] (operand column order)
@@ -211,6 +234,7 @@ struct PfCall {
     unsigned *err;
     uint8_t *ws;            // pf_workspace_bytes(...)
     int n_cta;
+    LayerExt ext;           // optional parts of the layer
 };
 
 // Buffers the router reads on the prefill path: FP16 activations in operand

@@ -176,6 +176,7 @@ __device__ __forceinline__ void tma_4d(void *dst, const CUtensorMap *map, int c0
 struct Unit {
     int shared;  // 1: the shared expert
     int e;       // routed expert
+    int r;       // its record in the blob
     int row0;    // first weight row of the tile
     int slot0;   // first token row of the tile (slot position or token)
     int n;       // tokens in the tile
@@ -198,6 +199,7 @@ __device__ __forceinline__ Unit unit_of(const PfArgs &a, int u, int nR)
         const int tt = tile - __ldg(a.tt_off + lo);
         U.shared = 0;
         U.e = lo;
+        U.r = expert_record(a.slot, a.n_slots, lo, a.err);
         U.row0 = kMT * f;
         U.slot0 = __ldg(a.offsets + lo) + kNT * tt;
         U.n = min(kNT, __ldg(a.offsets + lo) + __ldg(a.counts + lo) - U.slot0);
@@ -206,6 +208,7 @@ __device__ __forceinline__ Unit unit_of(const PfArgs &a, int u, int nR)
         const int v = u - nR * a.FT, tt = v / a.FTs, f = v - tt * a.FTs;
         U.shared = 1;
         U.e = 0;
+        U.r = 0;
         U.row0 = kMT * f;
         U.slot0 = kNT * tt;
         U.n = min(kNT, a.T - U.slot0);
@@ -355,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                         for (int at = 0; at < nat; ++at)
                             for (int m = 0; m < NMAT; ++m) {
                                 const CUtensorMap *map = U.shared ? (m ? &a.swb : &a.swa) : (m ? &a.wb : &a.wa);
-                                tma_4d(pk + (at * NMAT + m) * kPacked, map, 0, U.row0, kt0 + at, U.shared ? 0 : U.e,
+                                tma_4d(pk + (at * NMAT + m) * kPacked, map, 0, U.row0, kt0 + at, U.shared ? 0 : U.r,
                                        &full[sp]);
                             }
                     } else {
@@ -473,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 sv = a.ss[j] + (size_t)row * G;
                 bv = a.sb[j] + (size_t)row * G;
             } else {
-                const uint8_t *rec = a.blob + (uint64_t)U.e * a.stride;
+                const uint8_t *rec = a.blob + (uint64_t)U.r * a.stride;
                 sv = reinterpret_cast<const uint16_t *>(rec + a.off_s[j]) + (size_t)row * G;
                 bv = reinterpret_cast<const uint16_t *>(rec + a.off_b[j]) + (size_t)row * G;
             }
@@ -662,9 +665,12 @@ __global__ void pf_index(const int32_t *perm, int n, const int32_t *counts, int 
 
 // One CTA per token: optional rmsnorm (canonical order, rounded to BF16), the
 // token's power-of-two scale, its FP16 row in operand order, and its per-group
-// sums in the fixed add order (the router's X).
+// sums in the fixed add order (the router's X: of (x_i * rsc_i) * rcoef when
+// the router input is scaled).  With a gate vector, gv[t] = sigmoid(gvec . x)
+// (per group an fma chain, groups in order).
 __global__ void __launch_bounds__(256) pf_norm(const uint16_t *x, int D, int pre_norm, float eps, __half *X16,
-                                               float *xsc, float *XG)
+                                               float *xsc, float *XG, const uint16_t *rsc, float rcoef,
+                                               const uint16_t *gvec, float *gv)
 {
     extern __shared__ float gs[];  // D floats, then 64 + D/64 scratch
     float *xv = gs, *scr = gs + D;
@@ -695,9 +701,29 @@ __global__ void __launch_bounds__(256) pf_norm(const uint16_t *x, int D, int pre
     }
     for (int g = tid; g < G; g += 256) {
         float X = 0.f;
-        for (int k = 0; k < 64; ++k)
-            X = X + xv[64 * g + k];
+        if (rsc) {
+            for (int k = 0; k < 64; ++k)
+                X = X + __fmul_rn(__fmul_rn(xv[64 * g + k], bf2f(__ldg(rsc + 64 * g + k))), rcoef);
+        } else {
+            for (int k = 0; k < 64; ++k)
+                X = X + xv[64 * g + k];
+        }
         XG[(size_t)t * G + g] = X;
+        if (gvec) {
+            float q = 0.f;
+            for (int k = 0; k < 64; ++k)
+                q = fmaf(bf2f(__ldg(gvec + 64 * g + k)), xv[64 * g + k], q);
+            scr[64 + g] = q;
+        }
+    }
+    if (gvec) {
+        __syncthreads();
+        if (tid == 0) {
+            float z = 0.f;
+            for (int g = 0; g < G; ++g)
+                z = z + scr[64 + g];
+            gv[t] = 1.0f / (1.0f + expf(-z));
+        }
     }
     float mx = 0.f;
     for (int i = tid; i < D; i += 256)
@@ -739,15 +765,19 @@ __global__ void __launch_bounds__(256) pf_scatter(const __half *X16, int D, int 
     }
 }
 
-// out[t] = residual[t] + lambda * (shared[t] + sum_k w[t,k] * y[slot(t,k)]), k ascending.
-__global__ void __launch_bounds__(256) pf_combine(const float *Y, const float *Ys, const int32_t *inv,
-                                                  const float *topk_w, int T, int D, int K, float lam,
-                                                  const uint16_t *residual, uint16_t *out)
+// The combined FFN output of token t at columns d..d+3: the shared branch (times
+// its gate gv[t] when there is one), then the K routed outputs, k ascending.
+__device__ __forceinline__ float4 combined(const float *Y, const float *Ys, const int32_t *inv,
+                                           const float *topk_w, const float *gv, int t, int D, int K, int d)
 {
-    const int t = blockIdx.y, d = 4 * (blockIdx.x * 256 + threadIdx.x);
-    if (t >= T || d >= D)
-        return;
     float4 acc = *reinterpret_cast<const float4 *>(Ys + (size_t)t * D + d);
+    if (gv) {
+        const float g = __ldg(gv + t);
+        acc.x = g * acc.x;
+        acc.y = g * acc.y;
+        acc.z = g * acc.z;
+        acc.w = g * acc.w;
+    }
     for (int k = 0; k < K; ++k) {
         const float w = __ldg(topk_w + (size_t)t * K + k);
         const float4 y = *reinterpret_cast<const float4 *>(Y + (size_t)__ldg(inv + (size_t)t * K + k) * D + d);
@@ -756,6 +786,13 @@ __global__ void __launch_bounds__(256) pf_combine(const float *Y, const float *Y
         acc.z = acc.z + w * y.z;
         acc.w = acc.w + w * y.w;
     }
+    return acc;
+}
+
+// out[t] at columns d..d+3 = residual[t] + lambda * v, rounded to BF16.
+__device__ __forceinline__ void store_out(const uint16_t *residual, uint16_t *out, int t, int D, int d, float lam,
+                                          const float (&v)[4])
+{
     float r[4] = {0.f, 0.f, 0.f, 0.f};
     if (residual) {
         const uint2 rv = *reinterpret_cast<const uint2 *>(residual + (size_t)t * D + d);
@@ -764,11 +801,62 @@ __global__ void __launch_bounds__(256) pf_combine(const float *Y, const float *Y
         r[2] = __uint_as_float(rv.y << 16);
         r[3] = __uint_as_float(rv.y & 0xFFFF0000u);
     }
-    const float o[4] = {r[0] + lam * acc.x, r[1] + lam * acc.y, r[2] + lam * acc.z, r[3] + lam * acc.w};
+    const float o[4] = {r[0] + lam * v[0], r[1] + lam * v[1], r[2] + lam * v[2], r[3] + lam * v[3]};
     uint2 ov;
     ov.x = (uint32_t)f2bf(o[0]) | ((uint32_t)f2bf(o[1]) << 16);
     ov.y = (uint32_t)f2bf(o[2]) | ((uint32_t)f2bf(o[3]) << 16);
     *reinterpret_cast<uint2 *>(out + (size_t)t * D + d) = ov;
+}
+
+// With a post-FFN norm weight: one CTA per token holds the combined output in
+// shared memory, takes its RMS factor (per group of 64 an fma chain of squares,
+// groups in order) and writes residual + lambda * (y * r) * weight.
+__global__ void __launch_bounds__(256) pf_combine_norm(const float *Y, const float *Ys, const int32_t *inv,
+                                                       const float *topk_w, const float *gv, int T, int D, int K,
+                                                       float lam, const uint16_t *pnw, float peps,
+                                                       const uint16_t *residual, uint16_t *out)
+{
+    extern __shared__ float ys[];  // D floats, then D/64 group sums and the factor
+    const int t = blockIdx.x, tid = threadIdx.x, G = D / 64;
+    float *q = ys + D;
+    for (int d = 4 * tid; d < D; d += 1024)
+        *reinterpret_cast<float4 *>(ys + d) = combined(Y, Ys, inv, topk_w, gv, t, D, K, d);
+    __syncthreads();
+    for (int g = tid; g < G; g += 256) {
+        float a = 0.f;
+        for (int k = 0; k < 64; ++k)
+            a = fmaf(ys[64 * g + k], ys[64 * g + k], a);
+        q[g] = a;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float ss = 0.f;
+        for (int g = 0; g < G; ++g)
+            ss = ss + q[g];
+        q[G] = 1.0f / sqrtf(ss / (float)D + peps);
+    }
+    __syncthreads();
+    const float r = q[G];
+    for (int d = 4 * tid; d < D; d += 1024) {
+        float v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[j] = __fmul_rn(__fmul_rn(ys[d + j], r), bf2f(__ldg(pnw + d + j)));
+        store_out(residual, out, t, D, d, lam, v);
+    }
+}
+
+// out[t] = residual[t] + lambda * (shared[t] + sum_k w[t,k] * y[slot(t,k)]), k ascending.
+__global__ void __launch_bounds__(256) pf_combine(const float *Y, const float *Ys, const int32_t *inv,
+                                                  const float *topk_w, const float *gv, int T, int D, int K,
+                                                  float lam, const uint16_t *residual, uint16_t *out)
+{
+    const int t = blockIdx.y, d = 4 * (blockIdx.x * 256 + threadIdx.x);
+    if (t >= T || d >= D)
+        return;
+    const float4 acc = combined(Y, Ys, inv, topk_w, gv, t, D, K, d);
+    const float v[4] = {acc.x, acc.y, acc.z, acc.w};
+    store_out(residual, out, t, D, d, lam, v);
 }
 
 // ------------------------------------------------------------------- host
@@ -851,7 +939,7 @@ namespace {
 
 struct PfBufs {
     int32_t *inv, *tt_off;
-    float *xsc, *XG;
+    float *xsc, *XG, *gv;
     __half *X16, *Xr, *H, *Hs;
     float *Y, *Ys;
     float *QF;
@@ -873,6 +961,7 @@ PfBufs pf_carve(uint8_t *w, int T, int D, int I, int S, int E, int K)
     b.tt_off = reinterpret_cast<int32_t *>(take((size_t)(E + 1) * 4));
     b.xsc = reinterpret_cast<float *>(take((size_t)T * 4));
     b.XG = reinterpret_cast<float *>(take((size_t)T * (D / 64) * 4));
+    b.gv = reinterpret_cast<float *>(take((size_t)T * 4));
     b.X16 = reinterpret_cast<__half *>(take((size_t)T * D * 2));
     b.Xr = reinterpret_cast<__half *>(take(TK * D * 2));
     b.H = reinterpret_cast<__half *>(take(TK * I * 2));
@@ -898,7 +987,8 @@ cudaError_t launch_prefill_prepare(const PfCall &c, PfPrepared *out, cudaStream_
     cudaError_t e = smem_optin(reinterpret_cast<const void *>(pf_norm), gsm);
     if (e != cudaSuccess)
         return e;
-    pf_norm<<<c.T, 256, gsm, s>>>(static_cast<const uint16_t *>(c.x), c.D, c.pre_norm, c.eps, b.X16, b.xsc, b.XG);
+    pf_norm<<<c.T, 256, gsm, s>>>(static_cast<const uint16_t *>(c.x), c.D, c.pre_norm, c.eps, b.X16, b.xsc, b.XG,
+                                  c.ext.router_scale, c.ext.rcoef, c.ext.shared_gate, b.gv);
     out->X16 = b.X16;
     out->xsc = b.xsc;
     out->XG = b.XG;
@@ -936,6 +1026,8 @@ cudaError_t launch_prefill(const PfCall &c, cudaStream_t s)
     a.xsc = xsc;
     a.blob = c.blob;
     a.stride = c.stride;
+    a.slot = c.ext.slot;
+    a.n_slots = c.ext.slot ? c.ext.n_slots : E;
     for (int j = 0; j < 3; ++j) {
         a.off_s[j] = c.off_s[j];
         a.off_b[j] = c.off_b[j];
@@ -957,8 +1049,8 @@ cudaError_t launch_prefill(const PfCall &c, cudaStream_t s)
     a.GK_s = D / 64;
     a.rows = I;
     a.rows_s = S;
-    if ((e = encode_packed(&a.wa, c.blob + c.off_w[0], I, D, E, c.stride)) != cudaSuccess ||
-        (e = encode_packed(&a.wb, c.blob + c.off_w[1], I, D, E, c.stride)) != cudaSuccess ||
+    if ((e = encode_packed(&a.wa, c.blob + c.off_w[0], I, D, a.n_slots, c.stride)) != cudaSuccess ||
+        (e = encode_packed(&a.wb, c.blob + c.off_w[1], I, D, a.n_slots, c.stride)) != cudaSuccess ||
         (e = encode_packed(&a.swa, c.sw[0], S, D, 1, 0)) != cudaSuccess ||
         (e = encode_packed(&a.swb, c.sw[1], S, D, 1, 0)) != cudaSuccess ||
         (e = encode_rows(&a.xr, Xr, TK, D)) != cudaSuccess || (e = encode_rows(&a.xs, X16, T, D)) != cudaSuccess)
@@ -978,14 +1070,23 @@ cudaError_t launch_prefill(const PfCall &c, cudaStream_t s)
     a.GK_s = S / 64;
     a.rows = D;
     a.rows_s = D;
-    if ((e = encode_packed(&a.wa, c.blob + c.off_w[2], D, I, E, c.stride)) != cudaSuccess ||
+    if ((e = encode_packed(&a.wa, c.blob + c.off_w[2], D, I, a.n_slots, c.stride)) != cudaSuccess ||
         (e = encode_packed(&a.swa, c.sw[2], D, S, 1, 0)) != cudaSuccess ||
         (e = encode_rows(&a.xr, H, TK, I)) != cudaSuccess || (e = encode_rows(&a.xs, Hs, T, S)) != cudaSuccess)
         return e;
     prof_begin(kStageDown, s);
     e = launch_gemm<1>(a, c.n_cta, s);
-    if (e == cudaSuccess) {
-        pf_combine<<<dim3((D / 4 + 255) / 256, T), 256, 0, s>>>(Y, Ys, inv, c.topk_w, T, D, K, c.lam,
+    const float *gv = c.ext.shared_gate ? bf.gv : nullptr;
+    if (e == cudaSuccess && c.ext.post_norm) {
+        const size_t nsm = ((size_t)D + D / 64 + 1) * 4;
+        if ((e = smem_optin(reinterpret_cast<const void *>(pf_combine_norm), nsm)) == cudaSuccess) {
+            pf_combine_norm<<<T, 256, nsm, s>>>(Y, Ys, inv, c.topk_w, gv, T, D, K, c.lam, c.ext.post_norm,
+                                                c.ext.post_eps, static_cast<const uint16_t *>(c.residual),
+                                                static_cast<uint16_t *>(c.out));
+            e = cudaGetLastError();
+        }
+    } else if (e == cudaSuccess) {
+        pf_combine<<<dim3((D / 4 + 255) / 256, T), 256, 0, s>>>(Y, Ys, inv, c.topk_w, gv, T, D, K, c.lam,
                                                                static_cast<const uint16_t *>(c.residual),
                                                                static_cast<uint16_t *>(c.out));
         e = cudaGetLastError();

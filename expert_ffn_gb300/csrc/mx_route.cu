@@ -589,7 +589,8 @@ template <int TT>
 __global__ void __launch_bounds__(TT * 4) logits_gemm(const __half *__restrict__ X16, const float *__restrict__ xsc,
                                                        const float *__restrict__ XG, const float *__restrict__ QF,
                                                        const uint16_t *__restrict__ rs, const uint16_t *__restrict__ rb,
-                                                       int T, int D, int E, int Ep, float *__restrict__ logits)
+                                                       int T, int D, int E, int Ep, float *__restrict__ logits,
+                                                       const uint16_t *__restrict__ rsc, float rcoef)
 {
     constexpr int NT = TT * 4;               // threads
     constexpr int XV = TT * 8 / NT;          // 16-byte activation vectors per thread per group (= 2)
@@ -636,8 +637,13 @@ __global__ void __launch_bounds__(TT * 4) logits_gemm(const __half *__restrict__
             for (int j = 0; j < 4; ++j) {
                 const __half2 h = *reinterpret_cast<const __half2 *>(&u[j]);
                 const float2 f = __half22float2(h);
-                xs[8 * ch + j][t] = f.x * xscale[v];      // operand position 2j   -> column j
-                xs[8 * ch + j + 4][t] = f.y * xscale[v];  // operand position 2j+1 -> column j+4
+                float a0 = f.x * xscale[v], a1 = f.y * xscale[v];
+                if (rsc) {  // the router's input (x_i * rsc_i) * rcoef
+                    a0 = __fmul_rn(__fmul_rn(a0, bf2f(__ldg(rsc + 64 * g + 8 * ch + j))), rcoef);
+                    a1 = __fmul_rn(__fmul_rn(a1, bf2f(__ldg(rsc + 64 * g + 8 * ch + j + 4))), rcoef);
+                }
+                xs[8 * ch + j][t] = a0;      // operand position 2j   -> column j
+                xs[8 * ch + j + 4][t] = a1;  // operand position 2j+1 -> column j+4
             }
         }
 #pragma unroll
@@ -797,10 +803,12 @@ cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float 
     // 64-token blocks when they fill the GPU twice over, else 32-token blocks
     if ((long long)ne * ((a.T + 63) / 64) >= 2 * 152) {
         logits_gemm<64><<<dim3(ne, (a.T + 63) / 64), 256, 0, s>>>(static_cast<const __half *>(X16), xsc, XG, QF,
-                                                                    a.rs, a.rb, a.T, a.D, a.E, Ep, a.logits);
+                                                                    a.rs, a.rb, a.T, a.D, a.E, Ep, a.logits,
+                                                                    a.router_scale, a.rcoef);
     } else {
         logits_gemm<32><<<dim3(ne, (a.T + 31) / 32), 128, 0, s>>>(static_cast<const __half *>(X16), xsc, XG, QF,
-                                                                    a.rs, a.rb, a.T, a.D, a.E, Ep, a.logits);
+                                                                    a.rs, a.rb, a.T, a.D, a.E, Ep, a.logits,
+                                                                    a.router_scale, a.rcoef);
     }
     e = cudaGetLastError();
     if (e != cudaSuccess)

@@ -63,7 +63,7 @@ cudaError_t encode_qmat(CUtensorMap *m, const void *base, int rows, int cols, in
 struct Key {
     const void *blob, *sw0, *sw1, *sw2;
     uint64_t stride, off[3];
-    int D, I, S, E;
+    int D, I, S, E, records;
     bool operator==(const Key &o) const { return std::memcmp(this, &o, sizeof(Key)) == 0; }
 };
 
@@ -121,6 +121,7 @@ cudaError_t get_ffn_maps(const FfnArgs &a, FfnMaps *out)
     k.I = a.I;
     k.S = a.S;
     k.E = a.E;
+    k.records = a.slot ? a.n_slots : a.E;
     {
         std::lock_guard<std::mutex> g(g_mu);
         for (int i = 0; i < g_n; ++i)
@@ -131,13 +132,13 @@ cudaError_t get_ffn_maps(const FfnArgs &a, FfnMaps *out)
     }
     FfnMaps m;
     cudaError_t e;
-    if ((e = encode_qmat(&m.gate, a.blob + a.off_w[0], a.I, a.D, a.E, a.stride, 8)) != cudaSuccess ||
-        (e = encode_qmat(&m.up, a.blob + a.off_w[1], a.I, a.D, a.E, a.stride, 8)) != cudaSuccess ||
-        (e = encode_qmat(&m.down, a.blob + a.off_w[2], a.D, a.I, a.E, a.stride, 16)) != cudaSuccess ||
+    if ((e = encode_qmat(&m.gate, a.blob + a.off_w[0], a.I, a.D, k.records, a.stride, 8)) != cudaSuccess ||
+        (e = encode_qmat(&m.up, a.blob + a.off_w[1], a.I, a.D, k.records, a.stride, 8)) != cudaSuccess ||
+        (e = encode_qmat(&m.down, a.blob + a.off_w[2], a.D, a.I, k.records, a.stride, 16)) != cudaSuccess ||
         (e = encode_qmat(&m.sgate, a.sw[0], a.S, a.D, 1, 0, 8)) != cudaSuccess ||
         (e = encode_qmat(&m.sup, a.sw[1], a.S, a.D, 1, 0, 8)) != cudaSuccess ||
         (e = encode_qmat(&m.sdown, a.sw[2], a.D, a.S, 1, 0, 16)) != cudaSuccess ||
-        (e = encode_qmat(&m.down1, a.blob + a.off_w[2], a.D, a.I, a.E, a.stride, a.D / 16 < 256 ? a.D / 16 : 256, 1)) !=
+        (e = encode_qmat(&m.down1, a.blob + a.off_w[2], a.D, a.I, k.records, a.stride, a.D / 16 < 256 ? a.D / 16 : 256, 1)) !=
             cudaSuccess ||
         (e = encode_qmat(&m.sdown1, a.sw[2], a.D, a.S, 1, 0, a.D / 16 < 256 ? a.D / 16 : 256, 1)) != cudaSuccess)
         return e;

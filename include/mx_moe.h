@@ -67,7 +67,8 @@ typedef enum {
     MX_ERR_WORKSPACE = -4,      /* workspace too small or could not be allocated       */
     MX_ERR_CUDA = -5,           /* a CUDA runtime call failed                          */
     MX_ERR_DEVICE_TIMEOUT = -6, /* a device-side bounded wait gave up                  */
-    MX_ERR_RANGE = -7           /* a device-side range check failed (see below)        */
+    MX_ERR_RANGE = -7,          /* a device-side range check failed (see below)        */
+    MX_ERR_NOT_RESIDENT = -8    /* a selected expert has no record in the blob          */
 } mx_status;
 
 typedef enum { MX_F32 = 0, MX_BF16 = 1 } mx_dtype;
@@ -92,12 +93,39 @@ typedef struct {
 } mx_sub;
 
 #define MX_MOE_LAYOUT_MAGIC 0x4D584D45u /* "EMXM" little-endian */
-#define MX_MOE_LAYOUT_VERSION 1u
+#define MX_MOE_LAYOUT_VERSION 2u /* version 1 layouts (ending at per_expert_scale) are accepted too */
 
-/* Layout of one layer's expert blob: n_experts records of record_stride bytes.
- * Record e holds gate [d_expert, d_model], up [d_expert, d_model] and down
- * [d_model, d_expert] matrices (4-bit) at the offsets given.  d_shared is the
- * intermediate width of the layer's shared expert (mx_ffn). */
+/* Layout of one layer's expert blob: n_experts records of record_stride bytes
+ * (n_slots records when expert_slot is given).  Record r holds gate [d_expert,
+ * d_model], up [d_expert, d_model] and down [d_model, d_expert] matrices
+ * (4-bit) at the offsets given.  d_shared is the intermediate width of the
+ * layer's shared expert (mx_ffn).
+ *
+ * Version 2 adds optional parts of the layer, each absent when NULL:
+ *   expert_slot   a resident-set table ("Mference System design", section
+ *                 "Load and ownership": a GPU-visible expert-to-slot table,
+ *                 Int16 per expert, -1 for absent): device int16 [E]; expert
+ *                 e's weights are record expert_slot[e] of a blob of n_slots
+ *                 records.  A selected expert with no record (-1, or outside
+ *                 [0, n_slots)) contributes nothing and the call's error word
+ *                 reports it (mx_moe_workspace_check: MX_ERR_NOT_RESIDENT);
+ *                 the call's outputs are then not the block's.
+ *   router_scale  device BF16 [D]: the router reads x * router_scale / sqrt(D)
+ *                 (section "Decode", router formula), each element
+ *                 (x_i * router_scale_i) * (1/sqrtf(D)) in fp32; the experts
+ *                 still read x.
+ *   post_norm     device BF16 [D]: the combined output y = shared + sum_k w_k
+ *                 y_k becomes rmsnorm(y) * post_norm before the layer scalar
+ *                 and the residual (section "Decode", cb2 row: the post-FFN
+ *                 norms), eps post_eps; canonical order as pre_rmsnorm.
+ *   shared_expert_gate  device BF16 [D]: the shared branch is scaled per token
+ *                 by sigmoid(shared_expert_gate . x) (the page's gated shared
+ *                 expert of the Qwen family).
+ * router_scale, post_norm and shared_expert_gate are supported by the
+ * single-launch decode path (T <= 4) and the grouped-GEMM path (BF16, T > 4);
+ * calls that would run the multi-launch decode kernels (fp32 with T > 4, or
+ * those paths forced by MX_MOE_SINGLE_LAUNCH=0 / MX_MOE_PREFILL_GEMM=0)
+ * return MX_ERR_UNSUPPORTED for them.  expert_slot works on every path. */
 typedef struct {
     uint32_t magic;              /* MX_MOE_LAYOUT_MAGIC                          */
     uint32_t version;            /* MX_MOE_LAYOUT_VERSION                        */
@@ -113,6 +141,13 @@ typedef struct {
     int32_t act_dtype;           /* mx_dtype of x, out and residual              */
     float layer_scalar;          /* lambda                                       */
     const float *per_expert_scale; /* device [E], nullable = all ones            */
+    /* version 2 and later */
+    const int16_t *expert_slot;  /* device [E], nullable (see above)             */
+    int32_t n_slots;             /* records in the blob when expert_slot is set  */
+    const uint16_t *router_scale;  /* device BF16 [D], 16-byte aligned, nullable */
+    const uint16_t *post_norm;     /* device BF16 [D], 16-byte aligned, nullable */
+    float post_eps;                /* eps of post_norm                           */
+    const uint16_t *shared_expert_gate; /* device BF16 [D], 16-byte aligned, nullable */
 } mx_moe_layout;
 
 /* Per-call options (all optional; pass NULL for the plain block). */
@@ -168,8 +203,9 @@ MX_API mx_status mx_moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  * Device-side error word of a workspace.  Kernels that wait on asynchronous
  * copies give up after a bounded time, record it in the workspace's first word
  * and skip their math; this call synchronises on `stream`, reads the word, and
- * returns MX_ERR_DEVICE_TIMEOUT if a wait gave up, MX_ERR_RANGE if a range
- * check failed, MX_OK otherwise.  The word stays set until the workspace is
+ * returns MX_ERR_DEVICE_TIMEOUT if a wait gave up, MX_ERR_NOT_RESIDENT if a
+ * selected expert had no record in the blob (layout expert_slot),
+ * MX_ERR_RANGE if a range check failed, MX_OK otherwise.  The word stays set until the workspace is
  * re-initialised (mx_moe_workspace_init).
  *
  * Range of the single-launch decode path (T <= 4): its down projections are
@@ -233,6 +269,8 @@ MX_API mx_status mx_moe_layer_forward_static(const void *x, int T, const mx_qlin
  *   logits    device fp32 [T][E], nullable: the router logits
  * Grouping follows the "Prefill" section ("groups token/expert pairs into
  * bounded routed-MoE work").  opt may request pre_rmsnorm; residual is ignored.
+ * A layout with router_scale returns MX_ERR_UNSUPPORTED here (the block entry
+ * points apply it).
  */
 MX_API mx_status mx_moe_route(const void *x, int T, const mx_qlinear *router, const mx_moe_layout *layout,
                        int32_t *topk_idx, float *topk_w, int32_t *counts, int32_t *offsets,

@@ -85,7 +85,8 @@ def test_valid_call_with_zero_tokens_is_a_noop(L):
 
 @pytest.mark.parametrize("field,value,status", [
     ("magic", 0x12345678, INVALID),
-    ("version", 2, INVALID),
+    ("version", 3, INVALID),
+    ("version", 0, INVALID),
     ("group", 32, UNSUP),
     ("bits", 8, UNSUP),
     ("d_model", 250, UNSUP),
@@ -189,3 +190,77 @@ def test_stack_rejections(L):
     assert rc == WS
     rc = L.mx_moe_stack_forward(FAKE, 0, n, routers, shareds, blobs, layouts, FAKE, FAKE, 1e-6, None, FAKE, need)
     assert rc == OK
+
+
+# ------------------------------------------------ layout version 2 (optional parts)
+
+LAYOUT_FIELDS = ("magic", "version", "d_model", "d_expert", "n_experts", "top_k", "d_shared", "group", "bits",
+                 "record_stride", "gate", "up", "down", "act_dtype", "layer_scalar", "per_expert_scale",
+                 "expert_slot", "n_slots", "router_scale", "post_norm", "post_eps", "shared_expert_gate")
+
+
+def test_layout_struct_matches_the_header(tmp_path):
+    """The binding's Layout has the C struct's field offsets and size (a C
+    program built against include/mx_moe.h prints them)."""
+    src = tmp_path / "off.c"
+    body = "".join(f'    printf("%s %zu\\n", "{f}", offsetof(mx_moe_layout, {f}));\n' for f in LAYOUT_FIELDS)
+    src.write_text("#include <stddef.h>\n#include <stdio.h>\n#include \"mx_moe.h\"\n"
+                   "int main(void) {\n" + body + '    printf("size %zu\\n", sizeof(mx_moe_layout));\n'
+                   "    return 0;\n}\n")
+    exe = tmp_path / "off"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    for f in LAYOUT_FIELDS:
+        assert int(got[f]) == getattr(mx.Layout, f).offset, f
+    assert int(got["size"]) == C.sizeof(mx.Layout)
+
+
+def test_version_one_layout_is_accepted(L):
+    lay = layout(version=1)
+    assert call(L, lay, T=0) == OK
+    # a version-1 caller's struct ends at per_expert_scale: the fields after it are not read
+    lay.expert_slot, lay.n_slots = FAKE + 1, -5
+    assert call(L, lay, T=0) == OK
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("expert_slot", FAKE + 1, ALIGN),
+    ("router_scale", FAKE + 8, ALIGN),
+    ("post_norm", FAKE + 2, ALIGN),
+    ("shared_expert_gate", FAKE + 4, ALIGN),
+])
+def test_optional_part_alignment(L, field, value, status):
+    lay = layout(**{field: value})
+    if field == "expert_slot":
+        lay.n_slots = E
+    assert call(L, lay) == status
+
+
+@pytest.mark.parametrize("n_slots", [0, -1, 32768])
+def test_slot_table_needs_a_record_count(L, n_slots):
+    assert call(L, layout(expert_slot=FAKE, n_slots=n_slots)) == INVALID
+
+
+def test_post_norm_eps_must_be_nonnegative(L):
+    assert call(L, layout(post_norm=FAKE, post_eps=-1e-6)) == INVALID
+    assert call(L, layout(post_norm=FAKE, post_eps=float("nan"))) == INVALID
+
+
+@pytest.mark.parametrize("field", ["router_scale", "post_norm", "shared_expert_gate"])
+def test_multi_launch_path_rejects_the_new_parts(L, field):
+    """FP32 activations with more than four tokens run the multi-launch decode
+    kernels, which do not implement these parts: the call says so before any
+    launch."""
+    lay = layout(**{field: FAKE}, act_dtype=mx.MX_F32)
+    need = L.mx_moe_workspace_bytes(C.byref(lay), 8)
+    assert call(L, lay, T=8, ws=FAKE, ws_bytes=need) == UNSUP
+    assert b"multi-launch" in L.mx_last_error_string()
+
+
+def test_route_entry_rejects_router_scale(L):
+    lay = layout(router_scale=FAKE)
+    r = q(E, D, 8)
+    rc = L.mx_moe_route(FAKE, 4, C.byref(r), C.byref(lay), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE,
+                        1 << 30)
+    assert rc == UNSUP

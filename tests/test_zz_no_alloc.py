@@ -5,6 +5,7 @@ rejections (CPU), and on the GPU the same results as mx_moe_layer_forward_ex
 Collected last (file name) so that it also runs after every other test of the
 session has used the library."""
 import ctypes as C
+import gc
 
 import numpy as np
 import pytest
@@ -79,12 +80,19 @@ def test_static_matches_workspace_call(case):
     ref = run(False)
     mx.workspace_check(ws.t, s)
     run(True)  # warm-up: the first static call on the device resolves the scratch address
-    free0 = torch.cuda.mem_get_info()[0]
-    stats0 = torch.cuda.memory_stats().get("num_alloc_retries", 0), torch.cuda.memory_allocated()
-    for _ in range(2):  # two calls in a row: each leaves the scratch ready for the next
-        got = run(True)
-        for g, r in zip(got, ref):
-            assert np.array_equal(g, r)
-    assert torch.cuda.mem_get_info()[0] == free0
-    assert (torch.cuda.memory_stats().get("num_alloc_retries", 0), torch.cuda.memory_allocated()) == stats0
+    # tensors of earlier tests that only the cycle collector frees would
+    # otherwise be released in the middle of the measurement
+    gc.collect()
+    gc.disable()
+    try:
+        free0 = torch.cuda.mem_get_info()[0]
+        stats0 = torch.cuda.memory_stats().get("num_alloc_retries", 0), torch.cuda.memory_allocated()
+        for _ in range(2):  # two calls in a row: each leaves the scratch ready for the next
+            got = run(True)
+            for g, r in zip(got, ref):
+                assert np.array_equal(g, r)
+        assert torch.cuda.mem_get_info()[0] == free0
+        assert (torch.cuda.memory_stats().get("num_alloc_retries", 0), torch.cuda.memory_allocated()) == stats0
+    finally:
+        gc.enable()
     assert np.all(ref[1] >= 0)
