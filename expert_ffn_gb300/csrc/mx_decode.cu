@@ -60,6 +60,7 @@
 #include <climits>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 namespace mx {
 
@@ -170,10 +171,14 @@ struct Rt {  // routing of the current layer (computed by the consumer warps)
     int *act_slot;    // [amax][4] slot ids s = t*K + k, ascending
     int *slot_e;      // [T*K]
     float *slot_w;    // [T*K] (first the selected logits, then the weights)
-    int *emap;        // [E] expert -> active index
+    int *emap;        // [E] expert -> active index (then act_r, [amax]: the blob
+                      // record of each active expert; act_r(rt, E) gives it)
     uint32_t *emask;  // [16]
-    int *act_r;       // [amax] blob record of each active expert
 };
+
+// The record array follows emap: no pointer of its own, so that the hot loops
+// keep the registers they had.
+__device__ __forceinline__ int *act_r(const Rt &rt, int E) { return rt.emap + E; }
 
 struct Smem {
     uint64_t *full, *empty, *route_bar;
@@ -191,9 +196,8 @@ struct Smem {
     float *fx;             // [T] x plane back factors 2^(9-k)
     float *rn, *xsc;       // [T] rmsnorm factors, x plane scales
     int *vmax;             // [T] plane maxima (float bits)
-    float *yfx;            // [2] fixed-point factor of the layer's y and its inverse
-    float *gv;             // [T] shared-branch gate of each token (with a gate vector)
-    float *pnr;            // [T] post-FFN norm factors (with a post-norm weight)
+    float *yfx;            // [2] fixed-point factor of the layer's y and its inverse, then
+                           // yfx + 4: [T] shared-branch gates, yfx + 8: [T] post-norm factors
     int *flag;             // [4]
     uint8_t *zero;         // 16 zero bytes
     Rt rt;
@@ -226,8 +230,6 @@ __device__ __forceinline__ Smem carve(uint8_t *sm, const PdParams &p)
     s.ufo = m + 20;
     s.vmax = reinterpret_cast<int *>(m + 24);  // [T]
     s.yfx = m + 28;
-    s.gv = m + 32;
-    s.pnr = m + 36;
     int *r = reinterpret_cast<int *>(sm + o.rt);
     const int amax = TK < p.E ? TK : p.E;
     s.rt.n_act = r;
@@ -238,7 +240,6 @@ __device__ __forceinline__ Smem carve(uint8_t *sm, const PdParams &p)
     s.rt.slot_e = s.rt.act_slot + 4 * amax;
     s.rt.slot_w = reinterpret_cast<float *>(s.rt.slot_e + TK);
     s.rt.emap = reinterpret_cast<int *>(s.rt.slot_w + TK);
-    s.rt.act_r = s.rt.emap + p.E;
     s.zero = sm + o.zero;
     return s;
 }
@@ -539,7 +540,7 @@ __device__ __forceinline__ void store_planes(uint8_t *dst, bool per_slot, int nv
 
 // x_l (xraw) -> xq (optionally rmsnorm'd, rounded to the act dtype), its group
 // sums in the canonical order (the router's X), and its e4m3 planes.
-template <int NB>
+template <int NB, bool EXT>
 __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
 {
     constexpr int es = NB == 1 ? 2 : 4;
@@ -701,7 +702,7 @@ __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
             *reinterpret_cast<uint2 *>(s.xpl + off) = pl[q];
         }
     }
-    if (L.shared_gate) {
+    if (EXT && L.shared_gate) {
         // shared-branch gate sigmoid(g . x): per group an fma chain, then the
         // groups in order
         for (int i = tid; i < T * GD; i += kCT) {
@@ -727,7 +728,7 @@ __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
             float z = 0.f;
             for (int g = 0; g < GD; ++g)
                 z = z + s.pr[tid * GD + g];
-            s.gv[tid] = 1.0f / (1.0f + expf(-z));
+            s.yfx[4 + tid] = 1.0f / (1.0f + expf(-z));
         }
     }
     csync();
@@ -735,7 +736,7 @@ __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
 
 // Router rows r = blockIdx.x, + gridDim.x, ...: logits in the fixed order of
 // the header.  rq/rsv/rbv: the first row's bytes and affine terms, prefetched.
-template <int NB>
+template <int NB, bool EXT>
 __device__ void router_rows(const PdParams &p, const PdLayer &L, const Smem &s, uint4 (&rq)[4], float rsv,
                             float rbv)
 {
@@ -746,7 +747,7 @@ __device__ void router_rows(const PdParams &p, const PdLayer &L, const Smem &s, 
     float *bv = sv + GD;        // [GD]
     float *xx = bv + GD;        // [GD][T] group sums of the scaled input (with router_scale)
     // With router_scale the router reads (x_i * rs_i) * rcoef in fp32.
-    const bool scaled = L.router_scale != nullptr;
+    const bool scaled = EXT && L.router_scale != nullptr;
     for (int r = C; r < p.E; r += NC) {
         if (r != C && tid < GD) {
             const uint4 *q = reinterpret_cast<const uint4 *>(L.rw + (size_t)r * (D / 4) + (size_t)tid * 16);
@@ -868,6 +869,7 @@ __device__ void router_rows(const PdParams &p, const PdLayer &L, const Smem &s, 
 // Top-k (descending, ties to the lower expert, NaN as -inf), softmax of the
 // selected logits times the per-expert scale, and the grouping of slots by
 // expert (ascending expert, ascending slot).  All consumer threads.
+template <bool EXT>
 __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = p.T, E = p.E, K = p.K;
@@ -944,7 +946,8 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
         for (uint32_t b = bits; b; b &= b - 1u, ++j) {
             const int e = 32 * lane + __ffs(b) - 1;
             rt.act_e[j] = e;
-            rt.act_r[j] = expert_record(L.slot, L.n_slots, e, p.err);
+            if constexpr (EXT)
+                act_r(rt, E)[j] = expert_record(L.slot, L.n_slots, e, p.err);
             rt.act_n[j] = 0;
             rt.emap[e] = j;
         }
@@ -969,7 +972,7 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
 // expert j, block u) as r = j * GI + u; unit id i goes to CTA i mod NC.
 __device__ __forceinline__ int first_routed(int C, int NC, int GS) { return ((C - GS) % NC + NC) % NC; }
 
-template <int NB>
+template <int NB, bool EXT>
 __device__ void producer(const PdParams &p, const Smem &s)
 {
     const int lane = threadIdx.x & 31, C = blockIdx.x, NC = gridDim.x;
@@ -1043,7 +1046,7 @@ __device__ void producer(const PdParams &p, const Smem &s)
             break;
         const int nr = *s.rt.n_act * GI;
         for (int r = first_routed(C, NC, GS); r < nr && ok; r += NC)
-            ok = issue_unit(L, false, s.rt.act_r[r / GI], r % GI);
+            ok = issue_unit(L, false, EXT ? act_r(s.rt, p.E)[r / GI] : s.rt.act_e[r / GI], r % GI);
     }
     // Leave no copy in flight: wait (bounded) for the last item of every slot.
     __syncwarp();
@@ -1084,7 +1087,7 @@ __device__ void unit_planes(const float *uh, int ne, uint8_t *upl, float *ux, fl
     }
 }
 
-template <int NB>
+template <int NB, bool EXT>
 __device__ void consumers(const PdParams &p, const Smem &s)
 {
     constexpr int es = NB == 1 ? 2 : 4;
@@ -1118,9 +1121,9 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 dst[i] = __ldg(src + i);
             csync();
         }
-        prologue<NB>(p, L, s);
+        prologue<NB, EXT>(p, L, s);
         PD_STAMP(l, 1);
-        router_rows<NB>(p, L, s, rq, rsv, rbv);  // ends with a consumer barrier
+        router_rows<NB, EXT>(p, L, s, rq, rsv, rbv);  // ends with a consumer barrier
         PD_STAMP(l, 2);
         // (hold_cta: a CTA told by the host not to arrive at the first logit
         // exchange, so that every other CTA's bounded wait runs out)
@@ -1152,7 +1155,8 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                     sp = L.ss[2] + u;
                     bq = L.sb[2] + u;
                 } else {
-                    const uint8_t *rec = L.blob + (uint64_t)s.rt.act_r[j] * L.stride;
+                    const int rj = EXT ? act_r(s.rt, p.E)[j] : s.rt.act_e[j];
+                    const uint8_t *rec = L.blob + (uint64_t)rj * L.stride;
                     sp = reinterpret_cast<const uint16_t *>(rec + L.off_s[2]) + u;
                     bq = reinterpret_cast<const uint16_t *>(rec + L.off_b[2]) + u;
                 }
@@ -1198,8 +1202,8 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                         float h = gelu_tanh(ag) * au;
                         if (!shared)
                             h *= s.rt.slot_w[oslot];
-                        else if (L.shared_gate)
-                            h *= s.gv[ot];
+                        else if (EXT && L.shared_gate)
+                            h *= s.yfx[4 + ot];
                         s.uh[(8 * warp + gid) * 4 + c] = h;
                     }
                 }
@@ -1312,7 +1316,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 yp[i] = 0;
         }
         PD_STAMP(l, 4);
-        route_tables(p, L, s);
+        route_tables<EXT>(p, L, s);
         if (tid == 0)
             mbar_arrive(s.route_bar);
         PD_STAMP(l, 5);
@@ -1335,7 +1339,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
         // d_model <= 3072, T = 1)
         constexpr int kYB = NB == 1 ? 12 : 6;
         const float yinv = s.yfx[1];
-        if (L.post_norm) {
+        if (EXT && L.post_norm) {
             // post-FFN norm factor of each token: per group of 64 an fma chain
             // of squares, then the groups in order
             for (int i = tid; i < T * GD; i += kCT) {
@@ -1353,10 +1357,13 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 float ss = 0.f;
                 for (int g = 0; g < GD; ++g)
                     ss = ss + s.pr[tid * GD + g];
-                s.pnr[tid] = 1.0f / sqrtf(ss / (float)D + L.post_eps);
+                s.yfx[8 + tid] = 1.0f / sqrtf(ss / (float)D + L.post_eps);
             }
             csync();
         }
+        // (two instances of the loop, so that the plain one keeps its code)
+        auto rebuild = [&](auto pn_tag) {
+        constexpr bool PN = decltype(pn_tag)::value;
         for (int i0 = 0; i0 < T * D; i0 += kYB * kCT) {
             long long yq[kYB];
 #pragma unroll
@@ -1370,9 +1377,9 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             if (i >= T * D)
                 break;
             float yv = from_fix(yq[j]) * yinv;
-            if (L.post_norm) {
+            if constexpr (PN) {
                 const int t = i / D;
-                yv = __fmul_rn(__fmul_rn(yv, s.pnr[t]), bf2f(__ldg(L.post_norm + (i - t * D))));
+                yv = __fmul_rn(__fmul_rn(yv, s.yfx[8 + t]), bf2f(__ldg(L.post_norm + (i - t * D))));
             }
             float res = 0.f;
             if (L.res_mode == 1)
@@ -1394,13 +1401,21 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             }
             }
         }
+        };
+        if (EXT && L.post_norm)
+            rebuild(std::bool_constant<EXT>{});
+        else
+            rebuild(std::false_type{});
         csync();
         PD_STAMP(l, 11);
     }
     (void)lane;
 }
 
-template <int NB>
+// EXT: the variant with the layer's optional parts (resident-set table,
+// router input scale, shared-branch gate, post-FFN norm); plain layers run the
+// variant without their code.
+template <int NB, bool EXT>
 __global__ void __launch_bounds__(kPT, 1) pd_kernel(const __grid_constant__ PdParams p)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -1421,9 +1436,9 @@ __global__ void __launch_bounds__(kPT, 1) pd_kernel(const __grid_constant__ PdPa
     // shared-expert unit may add into y before any exchange of this call.
     __syncthreads();
     if (threadIdx.x >= kCT)
-        producer<NB>(p, s);
+        producer<NB, EXT>(p, s);
     else
-        consumers<NB>(p, s);
+        consumers<NB, EXT>(p, s);
     __syncthreads();
     // The last CTA to finish clears the counters for the next call (unless a
     // wait gave up: then the workspace must be re-initialised).
@@ -1506,10 +1521,10 @@ extern "C" __attribute__((visibility("default"))) int mx_pd_trace_read(unsigned 
 
 namespace {
 
-template <int NB>
+template <int NB, bool EXT>
 cudaError_t launch_nb(const PdParams &p, cudaStream_t st)
 {
-    auto k = pd_kernel<NB>;
+    auto k = pd_kernel<NB, EXT>;
     cudaError_t e = smem_optin(reinterpret_cast<const void *>(k), (size_t)p.sm.total);
     if (e != cudaSuccess)
         return e;
@@ -1536,7 +1551,14 @@ cudaError_t launch_nb(const PdParams &p, cudaStream_t st)
 
 cudaError_t launch_pd(const PdParams &p, cudaStream_t st)
 {
-    return p.act == 0 ? launch_nb<2>(p, st) : launch_nb<1>(p, st);
+    bool ext = false;
+    for (int l = 0; l < p.n_layers; ++l) {
+        const PdLayer &L = p.L[l];
+        ext = ext || L.slot || L.router_scale || L.post_norm || L.shared_gate;
+    }
+    if (ext)
+        return p.act == 0 ? launch_nb<2, true>(p, st) : launch_nb<1, true>(p, st);
+    return p.act == 0 ? launch_nb<2, false>(p, st) : launch_nb<1, false>(p, st);
 }
 
 } // namespace mx
