@@ -251,8 +251,9 @@ cudaError_t launch_prefill_prepare(const PfCall &c, PfPrepared *out, cudaStream_
 // After routing: scatter, gate/up GEMM, down GEMM, combine.
 cudaError_t launch_prefill(const PfCall &c, cudaStream_t s);
 // Routing of many tokens from the prepared activations (same logits, bit for bit).
-// QF: route_f32_bytes(D, E) of workspace for the router's bytes as floats.
-size_t route_f32_bytes(int D, int E);
+// QF: route_f32_bytes(T, D, E, K) of workspace: the router's bytes as floats,
+// then (reused) the per-block counts of the grouping.
+size_t route_f32_bytes(int T, int D, int E, int K);
 cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float *xsc, const float *XG, float *QF,
                                cudaStream_t s);
 

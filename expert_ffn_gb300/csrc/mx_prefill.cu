@@ -70,8 +70,12 @@ static_assert(__builtin_popcount(kDqMask) == kDqWarps, "dequantizing warps");
 // packed ring runs ahead.
 constexpr uint32_t kTmemCols = 512, kACols = 256;
 template <int MODE> struct Cfg;
-template <> struct Cfg<0> { static constexpr int NMAT = 2, NACC = 1, AT = 1, NA = 4, NB = 8, NP = 8; };
-template <> struct Cfg<1> { static constexpr int NMAT = 1, NACC = 2, AT = 2, NA = 4, NB = 4, NP = 8; };
+// TAB: the per-expert unit tables in shared memory (down: short units, the
+// lookups recur often); gate/up keeps them out, so that its shared memory
+// stays within the 196 KB carve-out and its L1 keeps room for the scale and
+// bias loads (gate/up ran 14% slower with 4 KB more shared memory).
+template <> struct Cfg<0> { static constexpr int NMAT = 2, NACC = 1, AT = 1, NA = 4, NB = 8, NP = 8; static constexpr bool TAB = false; };
+template <> struct Cfg<1> { static constexpr int NMAT = 1, NACC = 2, AT = 2, NA = 4, NB = 4, NP = 8; static constexpr bool TAB = true; };
 constexpr int kBTile = kNT * 128;  // bytes of one operand tile (128 tokens x 64 FP16)
 
 // ------------------------------------------------------------- tcgen05 glue
@@ -183,26 +187,42 @@ struct Unit {
     int kt_n;    // K tiles
 };
 
-__device__ __forceinline__ Unit unit_of(const PfArgs &a, int u, int nR)
+// Per-expert tables of the launch in shared memory (every role looks units up
+// at every unit start), at a fixed offset of the dynamic shared memory:
+// token-tile offsets [E+1], then slot offsets, slot counts and blob records [E].
+struct UnitTab {
+    const int *tt, *off, *cnt, *rec;
+    __device__ __forceinline__ explicit UnitTab(const int *base, int E)
+        : tt(base), off(base + E + 1), cnt(base + 2 * E + 1), rec(base + 3 * E + 1)
+    {
+    }
+};
+
+// Unit u of the launch: from the shared-memory tables (TAB) or from global memory.
+template <bool TAB>
+__device__ __forceinline__ Unit unit_of(const PfArgs &a, int u, int nR, const int *tab)
 {
+    const UnitTab tb(tab, a.E);
+    auto ld = [&](const int *smem_p, const int32_t *gmem_p) { return TAB ? *smem_p : __ldg(gmem_p); };
     Unit U;
     if (u < nR * a.FT) {
         const int tile = u / a.FT, f = u - tile * a.FT;
         int lo = 0, hi = a.E;
         while (lo + 1 < hi) {
             const int mid = (lo + hi) >> 1;
-            if (__ldg(a.tt_off + mid) <= tile)
+            if (ld(tb.tt + mid, a.tt_off + mid) <= tile)
                 lo = mid;
             else
                 hi = mid;
         }
-        const int tt = tile - __ldg(a.tt_off + lo);
+        const int tt = tile - ld(tb.tt + lo, a.tt_off + lo);
+        const int off = ld(tb.off + lo, a.offsets + lo), cnt = ld(tb.cnt + lo, a.counts + lo);
         U.shared = 0;
         U.e = lo;
-        U.r = expert_record(a.slot, a.n_slots, lo, a.err);
+        U.r = TAB ? tb.rec[lo] : expert_record(a.slot, a.n_slots, lo, a.err);
         U.row0 = kMT * f;
-        U.slot0 = __ldg(a.offsets + lo) + kNT * tt;
-        U.n = min(kNT, __ldg(a.offsets + lo) + __ldg(a.counts + lo) - U.slot0);
+        U.slot0 = off + kNT * tt;
+        U.n = min(kNT, off + cnt - U.slot0);
         U.kt_n = a.KT;
     } else {
         const int v = u - nR * a.FT, tt = v / a.FTs, f = v - tt * a.FTs;
@@ -295,6 +315,17 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
     uint32_t *tslot = reinterpret_cast<uint32_t *>(mma_done + 1);
     volatile int *abort = reinterpret_cast<volatile int *>(tslot + 1);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int *tab = reinterpret_cast<int *>(bars + 64);  // past the barriers, tslot and abort (512 bytes)
+    for (int i = tid; Cfg<MODE>::TAB && i <= a.E; i += kThreads) {
+        tab[i] = __ldg(a.tt_off + i);
+        if (i < a.E) {
+            const int c = __ldg(a.counts + i);
+            tab[a.E + 1 + i] = __ldg(a.offsets + i);
+            tab[2 * a.E + 1 + i] = c;
+            // (only a selected expert must have a record)
+            tab[3 * a.E + 1 + i] = c > 0 ? expert_record(a.slot, a.n_slots, i, a.err) : 0;
+        }
+    }
 
     if (tid == 0) {
         for (int i = 0; i < kNP; ++i) {
@@ -343,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
         uint32_t ph = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const Unit U = unit_of(a, u, nR);
+            const Unit U = unit_of<Cfg<MODE>::TAB>(a, u, nR, tab);
             for (int kt0 = 0; kt0 < U.kt_n; kt0 += kAt) {
                 const int nat = min(kAt, U.kt_n - kt0);
                 if (kp >= depth) {
@@ -395,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
         bool ok = true;
         const uint32_t bring_s = smem_u32(bring);
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++ai) {
-            const Unit U = unit_of(a, u, nR);
+            const Unit U = unit_of<Cfg<MODE>::TAB>(a, u, nR, tab);
             const int b = NACC == 1 ? 0 : (ai & 1);
             if (ai >= NACC) {
                 ok = __all_sync(0xffffffffu, bwait(&acc_empty[b], ((ai / NACC) - 1) & 1, a.err, abort));
@@ -465,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
         uint32_t php = 0, pha = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-            const Unit U = unit_of(a, u, nR);
+            const Unit U = unit_of<Cfg<MODE>::TAB>(a, u, nR, tab);
             const int rows = U.shared ? a.rows_s : a.rows;
             const int row = U.row0 + r;
             const bool valid = row < rows;
@@ -576,8 +607,22 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
         const int q = warp & 3;  // TMEM lane quadrant of this warp
         int ai = 0;
         for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++ai) {
-            const Unit U = unit_of(a, u, nR);
+            const Unit U = unit_of<Cfg<MODE>::TAB>(a, u, nR, tab);
             const int b = NACC == 1 ? 0 : (ai & 1);
+            // gate/up: the token scales of the unit's columns (lane j holds
+            // columns j, j + 32, ...), fetched while the unit's MMAs run
+            float my_sc[kNT / 32];
+            if (MODE == 0) {
+#pragma unroll
+                for (int i = 0; i < kNT / 32; ++i) {
+                    const int col = 32 * i + lane;
+                    my_sc[i] = 0.f;
+                    if (col < U.n) {
+                        const int p = U.slot0 + col;
+                        my_sc[i] = __ldg(a.xsc + (U.shared ? p : __ldg(a.perm + p) / a.K));
+                    }
+                }
+            }
             if (!__all_sync(0xffffffffu, bwait(&acc_full[b], (ai / NACC) & 1, a.err, abort)))
                 break;
             tc_fence_after();
@@ -591,22 +636,21 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 if (MODE == 0) {
                     uint32_t v[32];
                     tmem_ld32(d0 + kNT + c0, v);
+                    float sc_c = my_sc[0];
+#pragma unroll
+                    for (int i = 1; i < kNT / 32; ++i)
+                        if (c0 == 32 * i)
+                            sc_c = my_sc[i];
                     __half *H = static_cast<__half *>(U.shared ? a.Hs : a.H);
                     const int ld = U.shared ? a.S : a.I;
-                    // lane j fetches the token scale of column c0 + j once
-                    float my_sc = 0.f;
-                    if (c0 + lane < U.n) {
-                        const int p = U.slot0 + c0 + lane;
-                        my_sc = __ldg(a.xsc + (U.shared ? p : __ldg(a.perm + p) / a.K));
-                    }
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int col = c0 + j;
-                        const float sc = __shfl_sync(0xffffffffu, my_sc, j);
+                        const float sc = __shfl_sync(0xffffffffu, sc_c, j);
                         if (col < U.n && valid) {
                             const int p = U.slot0 + col;
                             const float gg = __uint_as_float(g[j]) * sc, uu = __uint_as_float(v[j]) * sc;
-                            float h = gelu_tanh(gg) * uu;
+                            float h = gelu_fast(gg) * uu;
                             h = fminf(fmaxf(h, -65504.f), 65504.f);
                             H[(size_t)p * ld + opos(row)] = __float2half_rn(h);
                         }
@@ -915,17 +959,18 @@ cudaError_t encode_packed(CUtensorMap *m, const void *base, int rows, int cols, 
 }
 
 template <int MODE>
-size_t gemm_smem()
+size_t gemm_smem(int E)
 {
     using C = Cfg<MODE>;
-    return 1024 + (size_t)C::NB * C::AT * kBTile + (size_t)C::NP * C::AT * C::NMAT * 128 * 32 + 512;
+    return 1024 + (size_t)C::NB * C::AT * kBTile + (size_t)C::NP * C::AT * C::NMAT * 128 * 32 + 512 +
+           (C::TAB ? (size_t)(4 * E + 1) * sizeof(int) : 0);
 }
 
 template <int MODE>
 cudaError_t launch_gemm(const PfArgs &a, int n_cta, cudaStream_t s)
 {
     auto k = pf_gemm<MODE>;
-    const size_t smem = gemm_smem<MODE>();
+    const size_t smem = gemm_smem<MODE>(a.E);
     cudaError_t e = smem_optin(reinterpret_cast<const void *>(k), smem);
     if (e != cudaSuccess)
         return e;
@@ -968,7 +1013,7 @@ PfBufs pf_carve(uint8_t *w, int T, int D, int I, int S, int E, int K)
     b.Hs = reinterpret_cast<__half *>(take((size_t)T * S * 2));
     b.Y = reinterpret_cast<float *>(take(TK * D * 4));
     b.Ys = reinterpret_cast<float *>(take((size_t)T * D * 4));
-    b.QF = reinterpret_cast<float *>(take(route_f32_bytes(D, E)));
+    b.QF = reinterpret_cast<float *>(take(route_f32_bytes(T, D, E, K)));
     b.total = (size_t)(p - w);
     return b;
 }

@@ -24,6 +24,7 @@
 
 #include <climits>
 #include <mutex>
+#include <type_traits>
 
 namespace mx {
 
@@ -582,23 +583,29 @@ __global__ void __launch_bounds__(256) router_to_f32(const uint32_t *__restrict_
         QF[(size_t)(4 * wi + b) * Ep + e] = (float)((w >> (8 * b)) & 0xFFu);
 }
 
-// Block of TT tokens x 64 experts; TT/4 x 16 threads, 4 x 4 accumulators each.
-// The next group's activations and router floats are loaded into registers
-// while the current group is multiplied.
+// Block of TT tokens x 64 experts, 256 threads: thread (ty, tx) of 16 x 16
+// holds tokens ty*TM .. ty*TM + TM - 1 (TM = TT/16) and experts 4tx .. 4tx+3,
+// TM x 4 accumulators.  Each group of 64 columns is staged in shared memory
+// (double-buffered; the next group's activations and router floats are loaded
+// into registers while the current one is multiplied), so one barrier per
+// group separates the buffers.
 template <int TT>
-__global__ void __launch_bounds__(TT * 4) logits_gemm(const __half *__restrict__ X16, const float *__restrict__ xsc,
-                                                       const float *__restrict__ XG, const float *__restrict__ QF,
-                                                       const uint16_t *__restrict__ rs, const uint16_t *__restrict__ rb,
-                                                       int T, int D, int E, int Ep, float *__restrict__ logits,
-                                                       const uint16_t *__restrict__ rsc, float rcoef)
+__global__ void __launch_bounds__(256, 1) logits_gemm(const __half *__restrict__ X16, const float *__restrict__ xsc,
+                                                    const float *__restrict__ XG, const float *__restrict__ QF,
+                                                    const uint16_t *__restrict__ rs, const uint16_t *__restrict__ rb,
+                                                    int T, int D, int E, int Ep, float *__restrict__ logits,
+                                                    const uint16_t *__restrict__ rsc, float rcoef)
 {
-    constexpr int NT = TT * 4;               // threads
-    constexpr int XV = TT * 8 / NT;          // 16-byte activation vectors per thread per group (= 2)
-    constexpr int QV = 64 * kLE / 4 / NT;    // 16-byte router vectors per thread per group
-    static_assert(XV * NT == TT * 8 && QV * NT * 4 == 64 * kLE, "tile shape");
-    __shared__ __align__(16) float xs[64][TT];   // [column][token]
-    __shared__ __align__(16) float qs[64][kLE];  // [column][expert]
-    __shared__ float sS[kLE], sB[kLE], sX[TT];
+    constexpr int NT = 256, TM = TT / 16;
+    constexpr int XV = TT * 8 / NT;             // 16-byte activation vectors per thread per group
+    constexpr int QV = 64 * kLE / 4 / NT;       // 16-byte router vectors per thread per group (= 4)
+    static_assert(XV >= 1 && XV * NT == TT * 8 && QV * NT * 4 == 64 * kLE && TM % 2 == 0, "tile shape");
+    extern __shared__ __align__(16) float lsm[];
+    float *xs0 = lsm;                           // [2][64][TT]   [column][token]
+    float *qs0 = xs0 + 2 * 64 * TT;             // [2][64][kLE]  [column][expert]
+    float *sS0 = qs0 + 2 * 64 * kLE;            // [2][kLE]
+    float *sB0 = sS0 + 2 * kLE;                 // [2][kLE]
+    float *sX0 = sB0 + 2 * kLE;                 // [2][TT]
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
     const int t0 = blockIdx.y * TT, e0 = blockIdx.x * kLE, G = D / 64;
     uint4 xr[XV], qr[QV];
@@ -619,16 +626,10 @@ __global__ void __launch_bounds__(TT * 4) logits_gemm(const __half *__restrict__
             qr[v] = __ldg(reinterpret_cast<const uint4 *>(QF + (size_t)(64 * g + c) * Ep + e0) + e4);
         }
     };
-    float acc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            acc[i][j] = 0.f;
-    fetch(0);
-    for (int g = 0; g < G; ++g) {
-        // registers -> shared: activations back in column order (operand
-        // position p of an 8-block holds column [0,4,1,5,2,6,3,7][p])
+    // registers -> shared buffer b: activations back in column order (operand
+    // position p of an 8-block holds column [0,4,1,5,2,6,3,7][p])
+    auto stage = [&](int g, int b) {
+        float *xs = xs0 + b * 64 * TT, *qs = qs0 + b * 64 * kLE;
 #pragma unroll
         for (int v = 0; v < XV; ++v) {
             const int i = tid + v * NT, t = i % TT, ch = i / TT;
@@ -642,65 +643,111 @@ __global__ void __launch_bounds__(TT * 4) logits_gemm(const __half *__restrict__
                     a0 = __fmul_rn(__fmul_rn(a0, bf2f(__ldg(rsc + 64 * g + 8 * ch + j))), rcoef);
                     a1 = __fmul_rn(__fmul_rn(a1, bf2f(__ldg(rsc + 64 * g + 8 * ch + j + 4))), rcoef);
                 }
-                xs[8 * ch + j][t] = a0;      // operand position 2j   -> column j
-                xs[8 * ch + j + 4][t] = a1;  // operand position 2j+1 -> column j+4
+                xs[(8 * ch + j) * TT + t] = a0;      // operand position 2j   -> column j
+                xs[(8 * ch + j + 4) * TT + t] = a1;  // operand position 2j+1 -> column j+4
             }
         }
 #pragma unroll
         for (int v = 0; v < QV; ++v) {
             const int i = tid + v * NT, c = i >> 4, e4 = i & 15;
-            *reinterpret_cast<uint4 *>(&qs[c][4 * e4]) = qr[v];
+            *reinterpret_cast<uint4 *>(qs + c * kLE + 4 * e4) = qr[v];
         }
         if (tid < kLE) {
             const int ee = e0 + tid;
-            sS[tid] = ee < E ? bf2f(__ldg(rs + (size_t)ee * G + g)) : 0.f;
-            sB[tid] = ee < E ? bf2f(__ldg(rb + (size_t)ee * G + g)) : 0.f;
+            sS0[b * kLE + tid] = ee < E ? bf2f(__ldg(rs + (size_t)ee * G + g)) : 0.f;
+            sB0[b * kLE + tid] = ee < E ? bf2f(__ldg(rb + (size_t)ee * G + g)) : 0.f;
         }
         if (tid < TT) {
             const int tt = t0 + tid;
-            sX[tid] = tt < T ? __ldg(XG + (size_t)tt * G + g) : 0.f;
+            sX0[b * TT + tid] = tt < T ? __ldg(XG + (size_t)tt * G + g) : 0.f;
         }
-        __syncthreads();
-        if (g + 1 < G)
-            fetch(g + 1);
-        float P[4][4];
+    };
+    float acc[TM][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            acc[i][j] = 0.f;
+    fetch(0);
+    stage(0, 0);
+    if (G > 1)
+        fetch(1);
+    __syncthreads();
+    for (int g = 0; g < G; ++g) {
+        const int b = g & 1;
+        const float *xs = xs0 + b * 64 * TT, *qs = qs0 + b * 64 * kLE;
+        float P[TM][4];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
                 P[i][j] = 0.f;
 #pragma unroll 8
         for (int c = 0; c < 64; ++c) {
-            const float4 xv = *reinterpret_cast<const float4 *>(&xs[c][4 * ty]);
-            const float4 qv = *reinterpret_cast<const float4 *>(&qs[c][4 * tx]);
-            const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, qa[4] = {qv.x, qv.y, qv.z, qv.w};
+            float xa[TM];
+            if constexpr (TM % 4 == 0) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+                for (int i = 0; i < TM; i += 4) {
+                    const float4 x4 = *reinterpret_cast<const float4 *>(xs + c * TT + ty * TM + i);
+                    xa[i] = x4.x;
+                    xa[i + 1] = x4.y;
+                    xa[i + 2] = x4.z;
+                    xa[i + 3] = x4.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < TM; i += 2) {
+                    const float2 x2 = *reinterpret_cast<const float2 *>(xs + c * TT + ty * TM + i);
+                    xa[i] = x2.x;
+                    xa[i + 1] = x2.y;
+                }
+            }
+            const float4 qv = *reinterpret_cast<const float4 *>(qs + c * kLE + 4 * tx);
+            const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
                     P[i][j] = fmaf(qa[j], xa[i], P[i][j]);
         }
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < TM; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                acc[i][j] = fmaf(sS[4 * tx + j], P[i][j], acc[i][j]);
-                acc[i][j] = fmaf(sB[4 * tx + j], sX[4 * ty + i], acc[i][j]);
+                acc[i][j] = fmaf(sS0[b * kLE + 4 * tx + j], P[i][j], acc[i][j]);
+                acc[i][j] = fmaf(sB0[b * kLE + 4 * tx + j], sX0[b * TT + ty * TM + i], acc[i][j]);
             }
+        // the other buffer was last read in group g - 1, before the barrier
+        // that ended it: stage group g + 1 there, then fetch group g + 2
+        if (g + 1 < G) {
+            stage(g + 1, b ^ 1);
+            if (g + 2 < G)
+                fetch(g + 2);
+        }
         __syncthreads();
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int tt = t0 + 4 * ty + i;
+    for (int i = 0; i < TM; ++i) {
+        const int tt = t0 + ty * TM + i;
         if (tt >= T)
             continue;
+        const int ee = e0 + 4 * tx;
+        if ((E & 3) == 0 && ee + 3 < E) {
+            *reinterpret_cast<float4 *>(logits + (size_t)tt * E + ee) =
+                make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+        } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int ee = e0 + 4 * tx + j;
-            if (ee < E)
-                logits[(size_t)tt * E + ee] = acc[i][j];
+            for (int j = 0; j < 4; ++j)
+                if (ee + j < E)
+                    logits[(size_t)tt * E + ee + j] = acc[i][j];
         }
     }
+}
+
+template <int TT>
+constexpr size_t logits_smem()
+{
+    return (size_t)(2 * 64 * TT + 2 * 64 * kLE + 4 * kLE + 2 * TT) * sizeof(float);
 }
 
 // Top-k + softmax of 8 tokens per block (one warp per token), from the logits.
@@ -711,13 +758,123 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const RouteArgs a)
     topk_tokens(a, t0, min(kWarps, a.T - t0), sm);
 }
 
-// Grouping of all slots by expert, one block of 32 warps.
-constexpr int kGroupWarps = 32;
-__global__ void __launch_bounds__(32 * kGroupWarps) group_kernel(const RouteArgs a)
+// Grouping of many slots by expert over several blocks (the order of
+// group_slots: ascending expert, ascending slot within an expert).  Block b
+// takes slots [b kGrpSlots, (b + 1) kGrpSlots); its warp w the w-th quarter.
+//   group_count    per-block expert counts bc[b][e]
+//   group_scan     counts, offsets, and each block's base bb[b][e] within
+//                  its expert (exclusive over blocks)
+//   group_scatter  each warp ranks its slots (32 at a time, in order) and
+//                  writes perm[offsets[e] + bb[b][e] + (earlier warps' and
+//                  rows' count) + rank]
+constexpr int kGrpSlots = 1024, kGrpWarps = 4;
+
+__global__ void __launch_bounds__(32 * kGrpWarps) group_count(const int32_t *__restrict__ idx, int n, int E,
+                                                              int32_t *__restrict__ bc)
 {
-    extern __shared__ __align__(16) float sm[];
-    group_slots_nw<kGroupWarps>(a, sm);
+    extern __shared__ int h[];  // [E]
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        h[e] = 0;
+    __syncthreads();
+    const int lo = blockIdx.x * kGrpSlots, hi = min(n, lo + kGrpSlots);
+    for (int s = lo + threadIdx.x; s < hi; s += blockDim.x)
+        atomicAdd(&h[__ldg(idx + s)], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x)
+        bc[(size_t)blockIdx.x * E + e] = h[e];
 }
+
+__global__ void __launch_bounds__(1024) group_scan(const int32_t *__restrict__ bc, int nb, int E,
+                                                   int32_t *__restrict__ bb, int32_t *__restrict__ counts,
+                                                   int32_t *__restrict__ offsets)
+{
+    __shared__ int cnt[kMaxExperts + 1];
+    __shared__ int wsum[32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int b = 0; b < nb; ++b) {
+            bb[(size_t)b * E + e] = run;
+            run += bc[(size_t)b * E + e];
+        }
+        cnt[e] = run;
+        counts[e] = run;
+    }
+    __syncthreads();
+    // exclusive scan of cnt over the experts (E <= 1024: one value per thread)
+    const int v = tid < E ? cnt[tid] : 0;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        int w = lane < nw ? wsum[lane] : 0, wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o)
+                wi += y;
+        }
+        wsum[lane] = wi - w;
+    }
+    __syncthreads();
+    const int ex = incl - v + wsum[warp];
+    if (tid < E)
+        offsets[tid] = ex;
+    if (tid == E - 1)
+        offsets[E] = ex + v;
+}
+
+__global__ void __launch_bounds__(32 * kGrpWarps) group_scatter(const int32_t *__restrict__ idx, int n, int E,
+                                                                const int32_t *__restrict__ bb,
+                                                                const int32_t *__restrict__ offsets,
+                                                                int32_t *__restrict__ perm)
+{
+    extern __shared__ int wb[];  // [kGrpWarps][E]: counts, then running positions
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int per = kGrpSlots / kGrpWarps;
+    const int lo = min(n, blockIdx.x * kGrpSlots + warp * per), hi = min(n, lo + per);
+    for (int i = threadIdx.x; i < kGrpWarps * E; i += blockDim.x)
+        wb[i] = 0;
+    __syncthreads();
+    int *mine = wb + warp * E;
+    for (int s0 = lo; s0 < hi; s0 += 32) {
+        const int s = s0 + lane, e = s < hi ? __ldg(idx + s) : -1;
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(m) - 1)
+            mine[e] += __popc(m);
+        __syncwarp();
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = __ldg(offsets + e) + __ldg(bb + (size_t)blockIdx.x * E + e);
+        for (int w = 0; w < kGrpWarps; ++w) {
+            const int c = wb[w * E + e];
+            wb[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int s0 = lo; s0 < hi; s0 += 32) {
+        const int s = s0 + lane, e = s < hi ? __ldg(idx + s) : -1;
+        const unsigned m = __match_any_sync(0xffffffffu, e);
+        if (e >= 0)
+            perm[mine[e] + __popc(m & lt)] = s;
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(m) - 1)
+            mine[e] += __popc(m);
+        __syncwarp();
+    }
+}
+
 
 } // namespace
 
@@ -790,7 +947,13 @@ cudaError_t launch_route(const RouteArgs &a, const RouteLaunch &L, cudaStream_t 
     }
 }
 
-size_t route_f32_bytes(int D, int E) { return (size_t)D * ((E + kLE - 1) / kLE * kLE) * sizeof(float); }
+size_t route_f32_bytes(int T, int D, int E, int K)
+{
+    const size_t qf = (size_t)D * ((E + kLE - 1) / kLE * kLE);
+    const size_t nb = ((size_t)T * K + kGrpSlots - 1) / kGrpSlots;
+    const size_t grp = 2 * nb * (size_t)E;
+    return (qf > grp ? qf : grp) * sizeof(float);
+}
 
 cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float *xsc, const float *XG, float *QF,
                                cudaStream_t s)
@@ -800,27 +963,47 @@ cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    // 64-token blocks when they fill the GPU twice over, else 32-token blocks
-    if ((long long)ne * ((a.T + 63) / 64) >= 2 * 152) {
-        logits_gemm<64><<<dim3(ne, (a.T + 63) / 64), 256, 0, s>>>(static_cast<const __half *>(X16), xsc, XG, QF,
-                                                                    a.rs, a.rb, a.T, a.D, a.E, Ep, a.logits,
-                                                                    a.router_scale, a.rcoef);
-    } else {
-        logits_gemm<32><<<dim3(ne, (a.T + 31) / 32), 128, 0, s>>>(static_cast<const __half *>(X16), xsc, XG, QF,
-                                                                    a.rs, a.rb, a.T, a.D, a.E, Ep, a.logits,
-                                                                    a.router_scale, a.rcoef);
-    }
-    e = cudaGetLastError();
+    // the largest token block that still gives most SMs a block
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess)
+        sms = 148;
+    auto run = [&](auto tt_tag) -> cudaError_t {
+        constexpr int TT = decltype(tt_tag)::value;
+        auto k = logits_gemm<TT>;
+        const size_t smem = logits_smem<TT>();
+        cudaError_t r = smem_optin(reinterpret_cast<const void *>(k), smem);
+        if (r != cudaSuccess)
+            return r;
+        k<<<dim3(ne, (a.T + TT - 1) / TT), 256, smem, s>>>(static_cast<const __half *>(X16), xsc, XG, QF, a.rs,
+                                                            a.rb, a.T, a.D, a.E, Ep, a.logits, a.router_scale,
+                                                            a.rcoef);
+        return cudaGetLastError();
+    };
+    const long long need = (long long)sms * 4 / 5;
+    if ((long long)ne * ((a.T + 127) / 128) >= need)
+        e = run(std::integral_constant<int, 128>{});
+    else if ((long long)ne * ((a.T + 63) / 64) >= need)
+        e = run(std::integral_constant<int, 64>{});
+    else
+        e = run(std::integral_constant<int, 32>{});
     if (e != cudaSuccess)
         return e;
     const size_t topk_smem = ((size_t)kWarps * a.E + (size_t)kWarps * ((a.E + 31) / 32)) * sizeof(float);
     topk_kernel<<<(a.T + kWarps - 1) / kWarps, kThreads, topk_smem, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
-    const size_t group_smem = (2 * (size_t)kGroupWarps * a.E + 3 * (size_t)a.E) * sizeof(float);
-    if ((e = smem_optin(reinterpret_cast<const void *>(group_kernel), group_smem)) != cudaSuccess)
+    // grouping over several blocks; its block counts reuse QF (the logits are done)
+    const int n = a.T * a.K, nb = (n + kGrpSlots - 1) / kGrpSlots;
+    int32_t *bc = reinterpret_cast<int32_t *>(QF), *bb = bc + (size_t)nb * a.E;
+    group_count<<<nb, 32 * kGrpWarps, a.E * sizeof(int), s>>>(a.topk_idx, n, a.E, bc);
+    if ((e = cudaGetLastError()) != cudaSuccess)
         return e;
-    group_kernel<<<1, 32 * kGroupWarps, group_smem, s>>>(a);
+    group_scan<<<1, 1024, 0, s>>>(bc, nb, a.E, bb, a.counts, a.offsets);
+    if ((e = cudaGetLastError()) != cudaSuccess)
+        return e;
+    group_scatter<<<nb, 32 * kGrpWarps, kGrpWarps * a.E * sizeof(int), s>>>(a.topk_idx, n, a.E, bb, a.offsets,
+                                                                            a.perm);
     return cudaGetLastError();
 }
 
