@@ -511,21 +511,40 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 sv = reinterpret_cast<const uint16_t *>(rec + a.off_s[j]) + (size_t)row * G;
                 bv = reinterpret_cast<const uint16_t *>(rec + a.off_b[j]) + (size_t)row * G;
             }
-            // scale and bias of the row's groups, kPf stages ahead in a register
-            // ring (the loads are L2/DRAM latency; a stage takes well under that)
-            constexpr int kPf = 4;
-            uint32_t s_r[kPf][kAt], b_r[kPf][kAt];
+            // scale and bias of the row's groups in blocks of 8 atoms (one
+            // 16-byte load each when the row pitch allows), one block ahead
+            // in registers (the loads are L2/DRAM latency; a block of stages
+            // takes well over that)
+            constexpr int kSB = 8, kSt = kSB / kAt;  // atoms, stages per block
+            const bool vec = (G % kSB) == 0;
+            auto load_blk = [&](int k0, uint4 &s4, uint4 &b4) {
+                s4 = b4 = make_uint4(0, 0, 0, 0);
+                if (!valid || k0 >= U.kt_n)
+                    return;
+                if (vec) {
+                    s4 = __ldg(reinterpret_cast<const uint4 *>(sv + k0));
+                    b4 = __ldg(reinterpret_cast<const uint4 *>(bv + k0));
+                } else {
+                    uint32_t sw[kSB], bw[kSB];
 #pragma unroll
-            for (int j = 0; j < kPf; ++j)
-#pragma unroll
-                for (int at = 0; at < kAt; ++at) {
-                    const int kn = j * kAt + at;
-                    s_r[j][at] = (valid && kn < U.kt_n) ? __ldg(sv + kn) : 0u;
-                    b_r[j][at] = (valid && kn < U.kt_n) ? __ldg(bv + kn) : 0u;
+                    for (int i = 0; i < kSB; ++i) {
+                        sw[i] = k0 + i < U.kt_n ? __ldg(sv + k0 + i) : 0u;
+                        bw[i] = k0 + i < U.kt_n ? __ldg(bv + k0 + i) : 0u;
+                    }
+                    s4 = make_uint4(sw[0] | sw[1] << 16, sw[2] | sw[3] << 16, sw[4] | sw[5] << 16, sw[6] | sw[7] << 16);
+                    b4 = make_uint4(bw[0] | bw[1] << 16, bw[2] | bw[3] << 16, bw[4] | bw[5] << 16, bw[6] | bw[7] << 16);
                 }
-            for (int kb = 0; kb < U.kt_n && ok; kb += kPf * kAt)
+            };
+            auto half_of = [](const uint4 &v, int h) -> uint16_t {
+                const uint32_t w = h < 2 ? v.x : h < 4 ? v.y : h < 6 ? v.z : v.w;
+                return (uint16_t)((h & 1) ? (w >> 16) : (w & 0xFFFFu));
+            };
+            uint4 s_c, b_c, s_n, b_n;
+            load_blk(0, s_c, b_c);
+            load_blk(kSB, s_n, b_n);
+            for (int kb = 0; kb < U.kt_n && ok; kb += kSB) {
 #pragma unroll
-            for (int jj = 0; jj < kPf; ++jj) {
+            for (int jj = 0; jj < kSt; ++jj) {
                 const int kt0 = kb + jj * kAt;
                 if (kt0 >= U.kt_n)
                     break;
@@ -533,11 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                 __half2 s2[kAt], b2[kAt];
 #pragma unroll
                 for (int at = 0; at < kAt; ++at) {
-                    s2[at] = __float2half2_rn(bf2f((uint16_t)s_r[jj][at]));
-                    b2[at] = __float2half2_rn(bf2f((uint16_t)b_r[jj][at]));
-                    const int kn = kt0 + kPf * kAt + at;
-                    s_r[jj][at] = (valid && kn < U.kt_n) ? __ldg(sv + kn) : 0u;
-                    b_r[jj][at] = (valid && kn < U.kt_n) ? __ldg(bv + kn) : 0u;
+                    s2[at] = __float2half2_rn(bf2f(half_of(s_c, jj * kAt + at)));
+                    b2[at] = __float2half2_rn(bf2f(half_of(b_c, jj * kAt + at)));
                 }
                 ok = bwait(&p_full[sp], php, a.err, abort) && (kf < kNA || bwait(&a_empty[sa], pha ^ 1u, a.err, abort));
                 if (!__all_sync(0xffffffffu, ok)) {
@@ -593,6 +609,10 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                     sp = 0;
                     php ^= 1u;
                 }
+            }
+            s_c = s_n;
+            b_c = b_n;
+            load_blk(kb + 2 * kSB, s_n, b_n);
             }
         }
         tmem_st_wait();
