@@ -50,7 +50,11 @@ namespace mx {
 namespace {
 
 constexpr int kMT = 128;  // weight rows per tile (MMA M)
-constexpr int kNT = 128;  // tokens per tile (MMA N, at most)
+// Tokens per tile (MMA N, at most).  An expert's tokens at T = 4096, 256
+// experts top-8 average 128 with a spread of ~11: 160 keeps nearly every
+// expert in one tile, so its weights are dequantized once per row tile
+// instead of once more for a tail of a few tokens.
+constexpr int kNT = 160;
 // Warp roles.  A warp runs on scheduler (warp % 4): each scheduler gets two
 // dequantizing warps (8..15), one epilogue warp (4..7, TMEM lane quadrant =
 // warp % 4) and one of: the weight producer (0), the MMA warp (1), the
@@ -63,20 +67,20 @@ constexpr int kBWarp = 2;
 static_assert(__builtin_popcount(kDqMask) == kDqWarps, "dequantizing warps");
 // A stage covers AT 64-K atoms.  TMEM (512 columns): accumulators in
 // columns [0, kACols), the FP16 weight slots (one per stage) above.  Gate/up
-// needs 256 columns per accumulator (gate and up side by side), so it keeps
-// one accumulator and four one-atom weight slots; down double-buffers its
-// 128-column accumulator and has four two-atom slots.  The activation ring
+// needs 2 kNT columns per accumulator (gate and up side by side), so it keeps
+// one accumulator and three one-atom weight slots; down double-buffers its
+// kNT-column accumulator and has three two-atom slots.  The activation ring
 // (NB stages) and the packed ring (NP stages) live in shared memory; the
 // packed ring runs ahead.
-constexpr uint32_t kTmemCols = 512, kACols = 256;
+constexpr uint32_t kTmemCols = 512, kACols = 2 * kNT;
 template <int MODE> struct Cfg;
 // TAB: the per-expert unit tables in shared memory (down: short units, the
 // lookups recur often); gate/up keeps them out, so that its shared memory
 // stays within the 196 KB carve-out and its L1 keeps room for the scale and
 // bias loads (gate/up ran 14% slower with 4 KB more shared memory).
-template <> struct Cfg<0> { static constexpr int NMAT = 2, NACC = 1, AT = 1, NA = 4, NB = 8, NP = 8; static constexpr bool TAB = false; };
-template <> struct Cfg<1> { static constexpr int NMAT = 1, NACC = 2, AT = 2, NA = 4, NB = 4, NP = 8; static constexpr bool TAB = true; };
-constexpr int kBTile = kNT * 128;  // bytes of one operand tile (128 tokens x 64 FP16)
+template <> struct Cfg<0> { static constexpr int NMAT = 2, NACC = 1, AT = 1, NA = 3, NB = 6, NP = 8; static constexpr bool TAB = false; };
+template <> struct Cfg<1> { static constexpr int NMAT = 1, NACC = 2, AT = 2, NA = 3, NB = 3, NP = 8; static constexpr bool TAB = true; };
+constexpr int kBTile = kNT * 128;  // bytes of one operand tile (kNT tokens x 64 FP16)
 
 // ------------------------------------------------------------- tcgen05 glue
 
