@@ -583,6 +583,25 @@ __global__ void __launch_bounds__(256) router_to_f32(const uint32_t *__restrict_
         QF[(size_t)(4 * wi + b) * Ep + e] = (float)((w >> (8 * b)) & 0xFFu);
 }
 
+// Two fp32 values as one 64-bit register pair, and back.
+__device__ __forceinline__ uint64_t pair_f32(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpair_f32(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// d = a * b + d on both lanes of the pairs, each an IEEE fma (round to nearest).
+__device__ __forceinline__ void fma_f32x2(uint64_t &d, uint64_t a, uint64_t b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
 // Block of TT tokens x 64 experts, 256 threads: thread (ty, tx) of 16 x 16
 // holds tokens ty*TM .. ty*TM + TM - 1 (TM = TT/16) and experts 4tx .. 4tx+3,
 // TM x 4 accumulators.  Each group of 64 columns is staged in shared memory
@@ -676,40 +695,35 @@ __global__ void __launch_bounds__(256, 1) logits_gemm(const __half *__restrict__
     for (int g = 0; g < G; ++g) {
         const int b = g & 1;
         const float *xs = xs0 + b * 64 * TT, *qs = qs0 + b * 64 * kLE;
-        float P[TM][4];
+        // P[i][j] for token pairs (i, i + 1): one packed two-lane fma per
+        // pair and expert, each lane an IEEE fma like fmaf (the same chain)
+        uint64_t P2[TM / 2][4];
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
+        for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-                P[i][j] = 0.f;
+                P2[i][j] = 0ull;
 #pragma unroll 8
         for (int c = 0; c < 64; ++c) {
-            float xa[TM];
-            if constexpr (TM % 4 == 0) {
+            uint64_t xp[TM / 2];
 #pragma unroll
-                for (int i = 0; i < TM; i += 4) {
-                    const float4 x4 = *reinterpret_cast<const float4 *>(xs + c * TT + ty * TM + i);
-                    xa[i] = x4.x;
-                    xa[i + 1] = x4.y;
-                    xa[i + 2] = x4.z;
-                    xa[i + 3] = x4.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < TM; i += 2) {
-                    const float2 x2 = *reinterpret_cast<const float2 *>(xs + c * TT + ty * TM + i);
-                    xa[i] = x2.x;
-                    xa[i + 1] = x2.y;
-                }
-            }
+            for (int i = 0; i < TM / 2; ++i)
+                xp[i] = *reinterpret_cast<const uint64_t *>(xs + c * TT + ty * TM + 2 * i);
             const float4 qv = *reinterpret_cast<const float4 *>(qs + c * kLE + 4 * tx);
-            const float qa[4] = {qv.x, qv.y, qv.z, qv.w};
+            const uint64_t qd[4] = {pair_f32(qv.x, qv.x), pair_f32(qv.y, qv.y), pair_f32(qv.z, qv.z),
+                                    pair_f32(qv.w, qv.w)};
 #pragma unroll
-            for (int i = 0; i < TM; ++i)
+            for (int i = 0; i < TM / 2; ++i)
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    P[i][j] = fmaf(qa[j], xa[i], P[i][j]);
+                    fma_f32x2(P2[i][j], qd[j], xp[i]);
         }
+        float P[TM][4];
+#pragma unroll
+        for (int i = 0; i < TM / 2; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                unpair_f32(P2[i][j], P[2 * i][j], P[2 * i + 1][j]);
 #pragma unroll
         for (int i = 0; i < TM; ++i)
 #pragma unroll
