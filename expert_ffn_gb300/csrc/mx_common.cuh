@@ -88,6 +88,20 @@ __device__ __forceinline__ float gelu_tanh(float z)
     return 0.5f * z * (1.0f + tanhf(inner));
 }
 
+__device__ __forceinline__ float exp2f_fast(float x)
+{
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+__device__ __forceinline__ float rcp_fast(float x)
+{
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
 // The same GELU through the identity 0.5 (1 + tanh(u)) = 1 / (1 + e^(-2u)):
 // z / (1 + e^(-2u)) with the fast exponential and division intrinsics (a few
 // ulp; the limits z -> -inf and +inf give -0 and z).  For the bulk epilogue of
@@ -98,6 +112,59 @@ __device__ __forceinline__ float gelu_fast(float z)
     const float k1 = 0.044715f;
     const float inner = k0 * (z + k1 * z * z * z);
     return __fdividef(z, 1.0f + __expf(-2.0f * inner));
+}
+
+// Two fp32 values as one 64-bit register pair, and back; packed two-lane
+// arithmetic on such pairs (each lane an IEEE operation, round to nearest).
+__device__ __forceinline__ uint64_t pair_f32(float lo, float hi)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpair_f32(uint64_t v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// d = a * b + d
+__device__ __forceinline__ void fma_f32x2(uint64_t &d, uint64_t a, uint64_t b)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// GELU (tanh form) of two values through z / (1 + e^(-2u)), u = k0 z (1 +
+// k1 z^2): packed arithmetic, the fast base-2 exponential and reciprocal
+// (the same approximations as gelu_fast).
+__device__ __forceinline__ uint64_t gelu_fast_x2(uint64_t z)
+{
+    const float k0 = 0.7978845608028654f, k1 = 0.044715f;
+    const float c = -2.0f * k0 * 1.4426950408889634f;  // e^(-2 k0 w) = 2^(c w)
+    const uint64_t z2 = mul_f32x2(z, z);
+    uint64_t t = pair_f32(1.0f, 1.0f);
+    fma_f32x2(t, z2, pair_f32(k1, k1));        // 1 + k1 z^2
+    const uint64_t a = mul_f32x2(mul_f32x2(z, t), pair_f32(c, c));
+    float a0, a1;
+    unpair_f32(a, a0, a1);
+    const uint64_t d = add_f32x2(pair_f32(exp2f_fast(a0), exp2f_fast(a1)), pair_f32(1.0f, 1.0f));
+    float d0, d1;
+    unpair_f32(d, d0, d1);
+    return mul_f32x2(z, pair_f32(rcp_fast(d0), rcp_fast(d1)));
 }
 
 // One packed router byte as an exact float: 2^23 + q built in the mantissa, minus 2^23.

@@ -667,17 +667,23 @@ __global__ void __launch_bounds__(kThreads, 1) pf_gemm(const __grid_constant__ P
                             sc_c = my_sc[i];
                     __half *H = static_cast<__half *>(U.shared ? a.Hs : a.H);
                     const int ld = U.shared ? a.S : a.I;
+                    __half *hp = H + (size_t)(U.slot0 + c0) * ld + opos(row);
+                    // two columns at a time in packed arithmetic; h rounded to
+                    // FP16 with saturation at the largest finite value
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int col = c0 + j;
-                        const float sc = __shfl_sync(0xffffffffu, sc_c, j);
-                        if (col < U.n && valid) {
-                            const int p = U.slot0 + col;
-                            const float gg = __uint_as_float(g[j]) * sc, uu = __uint_as_float(v[j]) * sc;
-                            float h = gelu_fast(gg) * uu;
-                            h = fminf(fmaxf(h, -65504.f), 65504.f);
-                            H[(size_t)p * ld + opos(row)] = __float2half_rn(h);
-                        }
+                    for (int j = 0; j < 32; j += 2) {
+                        const float s0 = __shfl_sync(0xffffffffu, sc_c, j), s1 = __shfl_sync(0xffffffffu, sc_c, j + 1);
+                        const uint64_t sc2 = pair_f32(s0, s1);
+                        const uint64_t gg = mul_f32x2(pair_f32(__uint_as_float(g[j]), __uint_as_float(g[j + 1])), sc2);
+                        const uint64_t uu = mul_f32x2(pair_f32(__uint_as_float(v[j]), __uint_as_float(v[j + 1])), sc2);
+                        float h0, h1;
+                        unpair_f32(mul_f32x2(gelu_fast_x2(gg), uu), h0, h1);
+                        uint32_t hh;
+                        asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(hh) : "f"(h1), "f"(h0));
+                        if (valid && c0 + j < U.n)
+                            *reinterpret_cast<uint16_t *>(hp + (size_t)j * ld) = (uint16_t)(hh & 0xFFFFu);
+                        if (valid && c0 + j + 1 < U.n)
+                            *reinterpret_cast<uint16_t *>(hp + (size_t)(j + 1) * ld) = (uint16_t)(hh >> 16);
                     }
                 } else {
                     float *Y = U.shared ? a.Ys : a.Y;

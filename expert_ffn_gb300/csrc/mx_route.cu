@@ -583,25 +583,6 @@ __global__ void __launch_bounds__(256) router_to_f32(const uint32_t *__restrict_
         QF[(size_t)(4 * wi + b) * Ep + e] = (float)((w >> (8 * b)) & 0xFFu);
 }
 
-// Two fp32 values as one 64-bit register pair, and back.
-__device__ __forceinline__ uint64_t pair_f32(float lo, float hi)
-{
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-
-__device__ __forceinline__ void unpair_f32(uint64_t v, float &lo, float &hi)
-{
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-
-// d = a * b + d on both lanes of the pairs, each an IEEE fma (round to nearest).
-__device__ __forceinline__ void fma_f32x2(uint64_t &d, uint64_t a, uint64_t b)
-{
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
-}
-
 // Block of TT tokens x 64 experts, 256 threads: thread (ty, tx) of 16 x 16
 // holds tokens ty*TM .. ty*TM + TM - 1 (TM = TT/16) and experts 4tx .. 4tx+3,
 // TM x 4 accumulators.  Each group of 64 columns is staged in shared memory
