@@ -874,55 +874,119 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = p.T, E = p.E, K = p.K;
     const Rt &rt = s.rt;
-    for (int i = tid; i < T * E; i += kCT) {
-        const float v = __ldcg(p.logits + i);
-        s.lg[i] = isnan(v) ? -INFINITY : v;
-    }
-    csync();
-    for (int i = tid; i < T * E; i += kCT) {
-        const int t = i / E, e = i - t * E;
-        const float *row = s.lg + t * E;
-        const float v = row[e];
-        int rank = 0, j = 0;
-        if ((E & 3) == 0) {  // rows 16-byte aligned: four logits per load
-#pragma unroll 4
-            for (; j < E; j += 4) {
-                const float4 u = *reinterpret_cast<const float4 *>(row + j);
-                rank += ((u.x > v) || (u.x == v && j < e)) + ((u.y > v) || (u.y == v && j + 1 < e)) +
-                        ((u.z > v) || (u.z == v && j + 2 < e)) + ((u.w > v) || (u.w == v && j + 3 < e));
+    // top-K and softmax, one warp per token: lane l holds the logits of
+    // experts l, l + 32, ... as order-preserving keys (NaN as -inf); K rounds
+    // of a warp maximum, ties to the lower expert; lane k keeps round k
+    if (E <= 128 && warp < T) {
+        const int t = warp;
+        constexpr int kPer = 4;
+        uint32_t key[kPer];
+#pragma unroll
+        for (int j = 0; j < kPer; ++j) {
+            const int e = lane + 32 * j;
+            float v = e < E ? __ldcg(p.logits + (size_t)t * E + e) : -INFINITY;
+            if (isnan(v))
+                v = -INFINITY;
+            const uint32_t u = __float_as_uint(v);
+            // monotone in v; taken and absent entries get 0, below every key
+            key[j] = e < E ? (u & 0x80000000u ? ~u : u | 0x80000000u) : 0u;
+        }
+        int mye = 0;
+        float myv = 0.f;
+        for (int k = 0; k < K; ++k) {
+            uint32_t best = 0u;
+            int bj = 0;
+#pragma unroll
+            for (int j = 0; j < kPer; ++j)
+                if (key[j] > best) {
+                    best = key[j];
+                    bj = j;
+                }
+            const uint32_t mx = __reduce_max_sync(0xffffffffu, best);
+            const int win = __reduce_min_sync(0xffffffffu, best == mx ? lane + 32 * bj : INT_MAX);
+            if (lane == (win & 31)) {
+#pragma unroll
+                for (int j = 0; j < kPer; ++j)
+                    if (j == (win >> 5))
+                        key[j] = 0u;
+            }
+            if (lane == k) {
+                mye = win;
+                myv = __uint_as_float(mx & 0x80000000u ? mx & 0x7FFFFFFFu : ~mx);
             }
         }
-        for (; j < E; ++j) {
-            const float u = row[j];
-            rank += (u > v) || (u == v && j < e);
-        }
-        if (rank < K) {
-            rt.slot_e[t * K + rank] = e;
-            rt.slot_w[t * K + rank] = v;
-        }
-    }
-    csync();
-    // softmax on warp 1 (lane = token) while warp 0 groups the slots
-    if (warp == 1 && lane < T) {
-        const int t = lane;
-        float *w = rt.slot_w + t * K;
-        const float m = w[0];
+        // softmax of the selected logits shifted by the largest (round 0),
+        // the sum in ascending k, times the per-expert scale
+        const float m = __shfl_sync(0xffffffffu, myv, 0);
+        const float ex = lane < K ? expf(myv - m) : 0.f;
         float sum = 0.f;
-        for (int k = 0; k < K; ++k) {
-            w[k] = expf(w[k] - m);
-            sum += w[k];
-        }
-        for (int k = 0; k < K; ++k) {
-            float x = w[k] / sum;
+        for (int k = 0; k < K; ++k)
+            sum += __shfl_sync(0xffffffffu, ex, k);
+        if (lane < K) {
+            float x = ex / sum;
             if (L.pes)
-                x = x * __ldg(L.pes + rt.slot_e[t * K + k]);
-            w[k] = x;
+                x = x * __ldg(L.pes + mye);
+            rt.slot_e[t * K + lane] = mye;
+            rt.slot_w[t * K + lane] = x;
             if (blockIdx.x == 0) {
-                L.topk_idx[t * K + k] = rt.slot_e[t * K + k];
-                L.topk_w[t * K + k] = x;
+                L.topk_idx[t * K + lane] = mye;
+                L.topk_w[t * K + lane] = x;
             }
         }
     }
+    if (E > 128) {
+        // more than 128 experts: each logit's rank by a scan of its row
+        for (int i = tid; i < T * E; i += kCT) {
+            const float v = __ldcg(p.logits + i);
+            s.lg[i] = isnan(v) ? -INFINITY : v;
+        }
+        csync();
+        for (int i = tid; i < T * E; i += kCT) {
+            const int t = i / E, e = i - t * E;
+            const float *row = s.lg + t * E;
+            const float v = row[e];
+            int rank = 0, j = 0;
+            if ((E & 3) == 0) {  // rows 16-byte aligned: four logits per load
+#pragma unroll 4
+                for (; j < E; j += 4) {
+                    const float4 u = *reinterpret_cast<const float4 *>(row + j);
+                    rank += ((u.x > v) || (u.x == v && j < e)) + ((u.y > v) || (u.y == v && j + 1 < e)) +
+                            ((u.z > v) || (u.z == v && j + 2 < e)) + ((u.w > v) || (u.w == v && j + 3 < e));
+                }
+            }
+            for (; j < E; ++j) {
+                const float u = row[j];
+                rank += (u > v) || (u == v && j < e);
+            }
+            if (rank < K) {
+                rt.slot_e[t * K + rank] = e;
+                rt.slot_w[t * K + rank] = v;
+            }
+        }
+        csync();
+        // softmax on warp 1 (lane = token) while warp 0 groups the slots
+        if (warp == 1 && lane < T) {
+            const int t = lane;
+            float *w = rt.slot_w + t * K;
+            const float m = w[0];
+            float sum = 0.f;
+            for (int k = 0; k < K; ++k) {
+                w[k] = expf(w[k] - m);
+                sum += w[k];
+            }
+            for (int k = 0; k < K; ++k) {
+                float x = w[k] / sum;
+                if (L.pes)
+                    x = x * __ldg(L.pes + rt.slot_e[t * K + k]);
+                w[k] = x;
+                if (blockIdx.x == 0) {
+                    L.topk_idx[t * K + k] = rt.slot_e[t * K + k];
+                    L.topk_w[t * K + k] = x;
+                }
+            }
+        }
+    }
+    csync();
     if (warp == 0) {
         if (lane < 16)
             rt.emask[lane] = 0u;
