@@ -745,6 +745,93 @@ constexpr size_t logits_smem()
     return (size_t)(2 * 64 * TT + 2 * 64 * kLE + 4 * kLE + 2 * TT) * sizeof(float);
 }
 
+// Few tokens (up to kPartT): the per-group dot products P[g][t][e] of every
+// group in its own block (grid: expert tiles x token tiles x groups), then
+// logits_sum adds them in the fixed order.  Each P is the same chain as in
+// logits_gemm, so the logits are the same bit for bit; the grid has G times
+// more blocks.
+constexpr int kPartT = 512;
+
+__global__ void __launch_bounds__(256) logits_part(const __half *__restrict__ X16, const float *__restrict__ xsc,
+                                                   const float *__restrict__ QF, int T, int D, int E, int Ep,
+                                                   const uint16_t *__restrict__ rsc, float rcoef,
+                                                   float *__restrict__ P)
+{
+    constexpr int TT = 32, TM = 2, NT = 256;
+    __shared__ __align__(16) float xs[64 * TT];   // [column][token]
+    __shared__ __align__(16) float qs[64 * kLE];  // [column][expert]
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int t0 = blockIdx.y * TT, e0 = blockIdx.x * kLE, g = blockIdx.z;
+    {
+        // activations: thread tid = 8-column chunk ch of token t (one 16-byte load)
+        const int t = tid % TT, ch = tid / TT, tt = t0 + t;
+        const uint4 xr = tt < T ? __ldg(reinterpret_cast<const uint4 *>(X16 + (size_t)tt * D + 64 * g) + ch)
+                                : make_uint4(0, 0, 0, 0);
+        const float xscale = tt < T ? __ldg(xsc + tt) : 0.f;
+        const uint32_t u[4] = {xr.x, xr.y, xr.z, xr.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const __half2 h = *reinterpret_cast<const __half2 *>(&u[j]);
+            const float2 f = __half22float2(h);
+            float a0 = f.x * xscale, a1 = f.y * xscale;
+            if (rsc) {
+                a0 = __fmul_rn(__fmul_rn(a0, bf2f(__ldg(rsc + 64 * g + 8 * ch + j))), rcoef);
+                a1 = __fmul_rn(__fmul_rn(a1, bf2f(__ldg(rsc + 64 * g + 8 * ch + j + 4))), rcoef);
+            }
+            xs[(8 * ch + j) * TT + t] = a0;
+            xs[(8 * ch + j + 4) * TT + t] = a1;
+        }
+#pragma unroll
+        for (int v = 0; v < 64 * kLE / 4 / NT; ++v) {
+            const int i = tid + v * NT, c = i >> 4, e4 = i & 15;
+            *reinterpret_cast<uint4 *>(qs + c * kLE + 4 * e4) =
+                __ldg(reinterpret_cast<const uint4 *>(QF + (size_t)(64 * g + c) * Ep + e0) + e4);
+        }
+    }
+    __syncthreads();
+    uint64_t P2[TM / 2][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        P2[0][j] = 0ull;
+#pragma unroll 8
+    for (int c = 0; c < 64; ++c) {
+        const uint64_t xp = *reinterpret_cast<const uint64_t *>(xs + c * TT + ty * TM);
+        const float4 qv = *reinterpret_cast<const float4 *>(qs + c * kLE + 4 * tx);
+        fma_f32x2(P2[0][0], pair_f32(qv.x, qv.x), xp);
+        fma_f32x2(P2[0][1], pair_f32(qv.y, qv.y), xp);
+        fma_f32x2(P2[0][2], pair_f32(qv.z, qv.z), xp);
+        fma_f32x2(P2[0][3], pair_f32(qv.w, qv.w), xp);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float p0, p1;
+        unpair_f32(P2[0][j], p0, p1);
+        const int ee = e0 + 4 * tx + j, tt = t0 + ty * TM;
+        if (ee < E) {
+            if (tt < T)
+                P[((size_t)g * T + tt) * E + ee] = p0;
+            if (tt + 1 < T)
+                P[((size_t)g * T + tt + 1) * E + ee] = p1;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(256) logits_sum(const float *__restrict__ P, const uint16_t *__restrict__ rs,
+                                                  const uint16_t *__restrict__ rb, const float *__restrict__ XG,
+                                                  int T, int E, int G, float *__restrict__ logits)
+{
+    const int i = blockIdx.x * 256 + threadIdx.x;
+    if (i >= T * E)
+        return;
+    const int t = i / E, e = i - t * E;
+    float acc = 0.f;
+    for (int g = 0; g < G; ++g) {
+        acc = fmaf(bf2f(__ldg(rs + (size_t)e * G + g)), __ldg(P + ((size_t)g * T + t) * E + e), acc);
+        acc = fmaf(bf2f(__ldg(rb + (size_t)e * G + g)), __ldg(XG + (size_t)t * G + g), acc);
+    }
+    logits[i] = acc;
+}
+
 // Top-k + softmax of 8 tokens per block (one warp per token), from the logits.
 __global__ void __launch_bounds__(kThreads) topk_kernel(const RouteArgs a)
 {
@@ -944,7 +1031,9 @@ cudaError_t launch_route(const RouteArgs &a, const RouteLaunch &L, cudaStream_t 
 
 size_t route_f32_bytes(int T, int D, int E, int K)
 {
-    const size_t qf = (size_t)D * ((E + kLE - 1) / kLE * kLE);
+    // the router's bytes as floats, then the per-group products of up to
+    // kPartT tokens (reserved for every T, so that the size grows with T)
+    const size_t qf = (size_t)D * ((E + kLE - 1) / kLE * kLE) + (size_t)(D / 64) * (T < kPartT ? T : kPartT) * E;
     const size_t nb = ((size_t)T * K + kGrpSlots - 1) / kGrpSlots;
     const size_t grp = 2 * nb * (size_t)E;
     return (qf > grp ? qf : grp) * sizeof(float);
@@ -976,7 +1065,16 @@ cudaError_t launch_route_large(const RouteArgs &a, const void *X16, const float 
         return cudaGetLastError();
     };
     const long long need = (long long)sms * 4 / 5;
-    if ((long long)ne * ((a.T + 127) / 128) >= need)
+    if (a.T <= kPartT) {
+        const int G = a.D / 64;
+        float *P = QF + (size_t)a.D * Ep;
+        logits_part<<<dim3(ne, (a.T + 31) / 32, G), 256, 0, s>>>(static_cast<const __half *>(X16), xsc, QF, a.T,
+                                                                 a.D, a.E, Ep, a.router_scale, a.rcoef, P);
+        if ((e = cudaGetLastError()) == cudaSuccess) {
+            logits_sum<<<(a.T * a.E + 255) / 256, 256, 0, s>>>(P, a.rs, a.rb, XG, a.T, a.E, G, a.logits);
+            e = cudaGetLastError();
+        }
+    } else if ((long long)ne * ((a.T + 127) / 128) >= need)
         e = run(std::integral_constant<int, 128>{});
     else if ((long long)ne * ((a.T + 63) / 64) >= need)
         e = run(std::integral_constant<int, 64>{});
