@@ -382,15 +382,15 @@ __device__ __forceinline__ float from_fix(long long q)
     return (float)hi + __uint2float_rn(lo) * kUnfix;
 }
 
-// Adds v f into the fixed-point sum; a value outside the range is reported
-// (kErrRange) and left out.
-__device__ __forceinline__ void red_fix(long long *y, float v, float f, unsigned *err)
+// Adds v f into the fixed-point sum; a value outside the range adds 0 and
+// sets `bad` (the caller reports it once, kErrRange), so the hot loop has no
+// branch around the add.
+__device__ __forceinline__ void red_fix(long long *y, float v, float f, bool &bad)
 {
-    const float a = v * f;
-    if (!(fabsf(a) < kFixLimit)) {
-        atomicOr(err, kErrRange);
-        return;
-    }
+    float a = v * f;
+    const bool in = fabsf(a) < kFixLimit;
+    bad |= !in;
+    a = in ? a : 0.f;
     const long long q = to_fix(a);
     asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(y), "l"(q) : "memory");
 }
@@ -1310,6 +1310,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             }
             const int ot = shared ? oc : s.rt.act_slot[4 * j + oc] / K;  // this lane's token
             const float hfo = s.ufo[oc], hX = s.ux[oc], yf = s.yfx[0];
+            bool bad = false;  // a partial sum outside the fixed-point range
             long long *yv = y + (size_t)ot * D;
             for (int q = 0; q < 4; ++q) {
                 // this item's (scale | bias << 16) words into buffer q & 1 (the
@@ -1345,11 +1346,11 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                         dn_tile<false>(tile + rt2 * 512, hb, isb[r2], isb[r2 + 8], hfo, hX, b0, b8);
                     }
                     if (out) {
-                        red_fix(yv + q * R4 + r0, a0, yf, p.err);
-                        red_fix(yv + q * R4 + r0 + 8, a8, yf, p.err);
+                        red_fix(yv + q * R4 + r0, a0, yf, bad);
+                        red_fix(yv + q * R4 + r0 + 8, a8, yf, bad);
                         if (rt2 != rt) {
-                            red_fix(yv + q * R4 + r2, b0, yf, p.err);
-                            red_fix(yv + q * R4 + r2 + 8, b8, yf, p.err);
+                            red_fix(yv + q * R4 + r2, b0, yf, bad);
+                            red_fix(yv + q * R4 + r2 + 8, b8, yf, bad);
                         }
                     }
                 }
@@ -1359,6 +1360,8 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 if (tr_first)
                     PD_STAMP(l, 16 + q);
             }
+            if (bad)
+                atomicOr(p.err, kErrRange);
             k += 12;
             return csync_and(good);
         };
