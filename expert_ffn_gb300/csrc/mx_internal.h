@@ -14,7 +14,7 @@ constexpr int kTileTokens = 64;
 // Largest T one pass of the decode path handles; longer inputs run in chunks.
 constexpr int kDecodeChunk = 64;
 // BF16 calls with more tokens than this run the grouped tensor-core GEMMs
-// (each expert's weights dequantized once per tile of up to 128 of its tokens).
+// (each expert's weights dequantized once per tile of up to 160 of its tokens).
 constexpr int kPrefillAbove = 4;
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 32;

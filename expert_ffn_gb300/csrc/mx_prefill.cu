@@ -1,4 +1,4 @@
-// mx_prefill.cu -- prefill path (T > 64 tokens, BF16 activations): grouped
+// mx_prefill.cu -- grouped-GEMM path (T > 4 tokens, BF16 activations): grouped
 // GEMMs on the 5th-generation tensor cores (tcgen05, accumulators in TMEM).
 //
 // What it computes is the block of the "Mference System design" page: section
@@ -15,7 +15,7 @@
 //   gather   x -> FP16 rows (scaled per token by a power of two, operand column
 //            order), once in token order (shared expert) and once per slot in
 //            expert order (routed experts)
-//   gate/up  grouped GEMM, tiles of 128 weight rows x 128 tokens:
+//   gate/up  grouped GEMM, tiles of 128 weight rows x up to kNT tokens:
 //            h = gelu(W_gate x) * (W_up x), FP16 [slot][I] and [T][S]
 //   down     grouped GEMM: y = W_down h, fp32 [slot][D] and [T][D]
 //   combine  out = residual + lambda * (shared + sum_k w_k y_k), k ascending
@@ -29,7 +29,7 @@
 //               B = the activation tile in shared memory, M = 128, N = the
 //               tile's tokens rounded up to 16, K = 16, fp32 accumulators in
 //               TMEM) and commits to mbarriers;
-//   warp 2      TMA producer of the 128-token FP16 activation tiles
+//   warp 2      TMA producer of the FP16 activation tiles (up to kNT tokens)
 //               (SWIZZLE_128B);
 //   warps 4-7   epilogue: tcgen05.ld of the accumulators (TMEM lane quadrant
 //               = warp % 4), gelu(g) * u for gate/up, fp32 rows for down;

@@ -304,7 +304,7 @@ MX_API size_t mx_moe_stack_workspace_bytes(const mx_moe_layout *layout, int T);
  * records a CUDA event pair around each of its kernels on the call's own
  * stream.  Stages: 0 = routing (router GEMV + top-k + grouping), 1 = gate/up +
  * GeGLU, 2 = down + combine.  The single-launch decode path (T <= 4) records
- * its one launch as stage 1; the prefill path (T > 64, BF16) records its
+ * its one launch as stage 1; the grouped-GEMM path (T > 4, BF16) records its
  * gate/up GEMM as stage 1 and its down GEMM + combine as stage 2 (the token
  * gather between routing and gate/up is not timed).  mx_moe_profile_read synchronises on the recorded
  * events and returns, per stage, the summed milliseconds and the number of
