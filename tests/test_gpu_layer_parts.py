@@ -234,3 +234,42 @@ def test_decode_stack_with_parts(orc, gu):
         assert np.array_equal(li, idx.cpu().numpy()[l]) and np.array_equal(lw, w.cpu().numpy()[l])
         cur = out
     assert np.array_equal(gu.to_host(xd, np.uint16), cur)
+
+
+def test_decode_stack_T3_with_parts(orc, gu):
+    """Three tokens through a 3-layer stack whose layers carry every optional
+    part: the stack entry point equals the chain of single-layer calls bit for
+    bit, every layer's top-k equals the oracle's, and the final output is
+    within the BF16 bars of the oracle's stack."""
+    import expert_ffn_gb300 as mx
+    n, T = 3, 3
+    cfg = synth.small_config(T=T, D=384, E=32, K=4, I=192, S=128, act="bf16", seed=840)
+    layers = []
+    for l in range(n):
+        lay = synth.make_layer(cfg, l)
+        lay = _with_blob(lay, [int(e) for e in np.random.default_rng(40 + l).permutation(lay.E)])
+        lay.router_scale = _router_scale(cfg.D, 50 + l)
+        lay.post_norm, lay.post_eps = _post_norm(cfg.D, 60 + l), 1e-6
+        lay.shared_expert_gate = _gate(cfg.D, 70 + l)
+        layers.append(lay)
+    x = synth.make_x(cfg)
+    devs = [mx.DeviceLayer(l, mx.MX_BF16) for l in layers]
+    xs_ref, idx_ref, w_ref = orc.stack_forward(layers, x, 1e-6)
+    xd = gu.to_dev(x)
+    idx = torch.full((n, T, cfg.K), -1, dtype=torch.int32, device="cuda")
+    w = torch.zeros((n, T, cfg.K), dtype=torch.float32, device="cuda")
+    ws = gu.Workspace(mx.stack_workspace_bytes(devs[0].layout, T))
+    mx.stack_forward(xd, T, mx.Stack(devs), idx, w, ws.t, ws.nbytes, rms_eps=1e-6,
+                     stream=torch.cuda.current_stream())
+    mx.workspace_check(ws.t, torch.cuda.current_stream())
+    torch.cuda.synchronize()
+    ws1 = gu.Workspace(mx.workspace_bytes(devs[0].layout, T))
+    cur = x
+    for l in range(n):
+        out, li, lw = gu.run_block(devs[l], cur, residual=cur, pre_norm=True, eps=1e-6, ws=ws1)
+        assert np.array_equal(li, idx.cpu().numpy()[l]) and np.array_equal(lw, w.cpu().numpy()[l])
+        cur = out
+    assert np.array_equal(gu.to_host(xd, np.uint16), cur)
+    assert np.array_equal(idx.cpu().numpy(), idx_ref)
+    assert rel_l2(w.cpu().numpy(), w_ref) <= 5e-3
+    check_out(cur, xs_ref[-1], "bf16")

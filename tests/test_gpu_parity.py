@@ -441,6 +441,7 @@ PREFILL_SHAPES = [
     (200, 320, 8, 3, 192, 320),      # D, I, S not multiples of 128; T ragged; experts with >128 slots
     (300, 512, 4, 2, 704, 128),      # few experts: several token tiles each
     (129, 1024, 64, 8, 256, 384),
+    (700, 256, 4, 2, 128, 64),       # ~350 slots per expert: three token tiles; above the per-group router's 512
 ]
 
 
