@@ -473,6 +473,93 @@ __device__ __forceinline__ void gu_item(const uint8_t *st, int G, const uint8_t 
     accu = fo * ((pu[0] + pu[1]) + (pu[2] + pu[3])) + ((qu[0] + qu[1]) + (qu[2] + qu[3]));
 }
 
+// 4-way byte dot products: a's bytes unsigned, b's unsigned / signed.
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Gate/up item on one warp for a single token of BF16 activations: integer
+// dot products instead of MMAs (an MMA would carry data in 2 of its 8
+// columns).  x is a 16-bit fixed-point vector (x 2^k1, max |x| 2^k1 in
+// [2^14, 2^15)) split into two byte planes, lo (unsigned) and hi (signed);
+// xp: this lane's planes of group 0, [plane][16 B] per group at 128-byte
+// pitch, the bytes of its 16 columns in the nibble order of its two packed
+// words (even columns of a word, then odd).  Lane (gid, c) takes columns
+// 16c .. 16c + 15 of rows gid (gate) and gid (up): per group 16 byte dot
+// products, exact in int32 (|sum| < 2^23, so exact in fp32 too); then the
+// group's scale and bias terms in fp32, the bias term once per row (lane c =
+// 0), and the four lanes of a row added by shuffles.  fo = 2^-k1.  Lane
+// output: gate and up dot products of row gid (every lane of the row).
+__device__ __forceinline__ void gu_item_t1(const uint8_t *st, int G, const uint8_t *xp, float fo, const float *xg,
+                                           float &accg, float &accu)
+{
+    const int lane = threadIdx.x & 31, gid = lane >> 2, c = lane & 3;
+    const uint8_t *gt = st + gid * 32 + c * 8, *ut = gt + 256 * G;
+    const uint16_t *sc = reinterpret_cast<const uint16_t *>(st + 512 * G) + gid * G;
+    const uint16_t *sg = sc, *bg = sc + 8 * G, *su = sc + 16 * G, *bu = sc + 24 * G;
+    const float bsel = c == 0 ? 1.f : 0.f;
+    float pg[2] = {0.f, 0.f}, pu[2] = {0.f, 0.f}, qg[2] = {0.f, 0.f}, qu[2] = {0.f, 0.f};
+#pragma unroll 2
+    for (int g = 0; g < G; ++g) {
+        const int h = g & 1;
+        const uint2 wg = lds64(gt + 256 * g), wu = lds64(ut + 256 * g);
+        const uint4 x0 = *reinterpret_cast<const uint4 *>(xp + 128 * g);
+        const uint4 x1 = *reinterpret_cast<const uint4 *>(xp + 128 * g + 16);
+        int g0 = 0, g1 = 0, u0 = 0, u1 = 0;
+        {
+            const uint32_t lo = wg.x & kLo, hi = (wg.x >> 4) & kLo;
+            g0 = dp4a_uu(lo, x0.x, g0);
+            g0 = dp4a_uu(hi, x0.y, g0);
+            g1 = dp4a_us(lo, x1.x, g1);
+            g1 = dp4a_us(hi, x1.y, g1);
+        }
+        {
+            const uint32_t lo = wg.y & kLo, hi = (wg.y >> 4) & kLo;
+            g0 = dp4a_uu(lo, x0.z, g0);
+            g0 = dp4a_uu(hi, x0.w, g0);
+            g1 = dp4a_us(lo, x1.z, g1);
+            g1 = dp4a_us(hi, x1.w, g1);
+        }
+        {
+            const uint32_t lo = wu.x & kLo, hi = (wu.x >> 4) & kLo;
+            u0 = dp4a_uu(lo, x0.x, u0);
+            u0 = dp4a_uu(hi, x0.y, u0);
+            u1 = dp4a_us(lo, x1.x, u1);
+            u1 = dp4a_us(hi, x1.y, u1);
+        }
+        {
+            const uint32_t lo = wu.y & kLo, hi = (wu.y >> 4) & kLo;
+            u0 = dp4a_uu(lo, x0.z, u0);
+            u0 = dp4a_uu(hi, x0.w, u0);
+            u1 = dp4a_us(lo, x1.z, u1);
+            u1 = dp4a_us(hi, x1.w, u1);
+        }
+        const float X = xg[g] * bsel;
+        pg[h] = fmaf(bf2f(sg[g]), (float)(g1 * 256 + g0), pg[h]);
+        qg[h] = fmaf(bf2f(bg[g]), X, qg[h]);
+        pu[h] = fmaf(bf2f(su[g]), (float)(u1 * 256 + u0), pu[h]);
+        qu[h] = fmaf(bf2f(bu[g]), X, qu[h]);
+    }
+    float ag = fo * (pg[0] + pg[1]) + (qg[0] + qg[1]);
+    float au = fo * (pu[0] + pu[1]) + (qu[0] + qu[1]);
+    ag += __shfl_xor_sync(0xffffffffu, ag, 1);
+    au += __shfl_xor_sync(0xffffffffu, au, 1);
+    ag += __shfl_xor_sync(0xffffffffu, ag, 2);
+    au += __shfl_xor_sync(0xffffffffu, au, 2);
+    accg = ag;
+    accu = au;
+}
+
 // One 16-row x 64-column tile of a unit's down slice (one group), one warp;
 // t0: this lane's bytes of the tile (tile + gid * 32 + c * 8); sb0 / sb8: the
 // BF16 scale (low half) and bias (high half) of rows gid and gid + 8.  hb: the
@@ -539,8 +626,9 @@ __device__ __forceinline__ void store_planes(uint8_t *dst, bool per_slot, int nv
 }
 
 // x_l (xraw) -> xq (optionally rmsnorm'd, rounded to the act dtype), its group
-// sums in the canonical order (the router's X), and its e4m3 planes.
-template <int NB, bool EXT>
+// sums in the canonical order (the router's X), and its e4m3 planes (T1: the
+// byte planes of gu_item_t1).
+template <int NB, bool EXT, bool T1>
 __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
 {
     constexpr int es = NB == 1 ? 2 : 4;
@@ -687,6 +775,22 @@ __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
             const float4 a = *reinterpret_cast<const float4 *>(src), b = *reinterpret_cast<const float4 *>(src + 16);
             x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
             x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+        }
+        if constexpr (T1) {
+            // 16-bit fixed point: x 2^(k+7), max |x| 2^(k+7) in [2^14, 2^15)
+            const float sc = s.xsc[t] * 128.0f;
+            uint32_t lo[2] = {0u, 0u}, hi[2] = {0u, 0u};  // [even, odd columns]
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int v = __float2int_rn(x[j] * sc);
+                lo[j & 1] |= (uint32_t)(v & 0xFF) << (8 * (j >> 1));
+                hi[j & 1] |= (uint32_t)((v >> 8) & 0xFF) << (8 * (j >> 1));
+            }
+            // lane c = w / 2 holds words 2c, 2c + 1 of the group: word w & 1
+            uint8_t *dst = s.xpl + (size_t)g * 128 + (w >> 1) * 32 + (w & 1) * 8;
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(lo[0], lo[1]);
+            *reinterpret_cast<uint2 *>(dst + 16) = make_uint2(hi[0], hi[1]);
+            continue;
         }
         const float sc = s.xsc[t];
 #pragma unroll
@@ -1151,7 +1255,7 @@ __device__ void unit_planes(const float *uh, int ne, uint8_t *upl, float *ux, fl
     }
 }
 
-template <int NB, bool EXT>
+template <int NB, bool EXT, bool T1>
 __device__ void consumers(const PdParams &p, const Smem &s)
 {
     constexpr int es = NB == 1 ? 2 : 4;
@@ -1185,7 +1289,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 dst[i] = __ldg(src + i);
             csync();
         }
-        prologue<NB, EXT>(p, L, s);
+        prologue<NB, EXT, T1>(p, L, s);
         PD_STAMP(l, 1);
         router_rows<NB, EXT>(p, L, s, rq, rsv, rbv);  // ends with a consumer barrier
         PD_STAMP(l, 2);
@@ -1257,8 +1361,12 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                     good = false;
                 } else {
                     float ag = 0.f, au = 0.f;
-                    gu_item<NB>(s.ring + (size_t)sl * o.slot, GD, bp, bvalid ? xgs : 0, bvalid ? xms : 0,
-                                bvalid ? xnbs : 0, s.fx[ot], s.xg + ot * GD, ag, au);
+                    if constexpr (T1)
+                        gu_item_t1(s.ring + (size_t)sl * o.slot, GD, s.xpl + c * 32, s.fx[0] * (1.0f / 65536.0f),
+                                   s.xg, ag, au);
+                    else
+                        gu_item<NB>(s.ring + (size_t)sl * o.slot, GD, bp, bvalid ? xgs : 0, bvalid ? xms : 0,
+                                    bvalid ? xnbs : 0, s.fx[ot], s.xg + ot * GD, ag, au);
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive_n(&s.empty[sl], kCW);
@@ -1482,7 +1590,8 @@ __device__ void consumers(const PdParams &p, const Smem &s)
 // EXT: the variant with the layer's optional parts (resident-set table,
 // router input scale, shared-branch gate, post-FFN norm); plain layers run the
 // variant without their code.
-template <int NB, bool EXT>
+// T1: one token of BF16 activations, gate/up on integer dot products.
+template <int NB, bool EXT, bool T1>
 __global__ void __launch_bounds__(kPT, 1) pd_kernel(const __grid_constant__ PdParams p)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -1505,7 +1614,7 @@ __global__ void __launch_bounds__(kPT, 1) pd_kernel(const __grid_constant__ PdPa
     if (threadIdx.x >= kCT)
         producer<NB, EXT>(p, s);
     else
-        consumers<NB, EXT>(p, s);
+        consumers<NB, EXT, T1>(p, s);
     __syncthreads();
     // The last CTA to finish clears the counters for the next call (unless a
     // wait gave up: then the workspace must be re-initialised).
@@ -1588,10 +1697,10 @@ extern "C" __attribute__((visibility("default"))) int mx_pd_trace_read(unsigned 
 
 namespace {
 
-template <int NB, bool EXT>
+template <int NB, bool EXT, bool T1>
 cudaError_t launch_nb(const PdParams &p, cudaStream_t st)
 {
-    auto k = pd_kernel<NB, EXT>;
+    auto k = pd_kernel<NB, EXT, T1>;
     cudaError_t e = smem_optin(reinterpret_cast<const void *>(k), (size_t)p.sm.total);
     if (e != cudaSuccess)
         return e;
@@ -1623,9 +1732,11 @@ cudaError_t launch_pd(const PdParams &p, cudaStream_t st)
         const PdLayer &L = p.L[l];
         ext = ext || L.slot || L.router_scale || L.post_norm || L.shared_gate;
     }
-    if (ext)
-        return p.act == 0 ? launch_nb<2, true>(p, st) : launch_nb<1, true>(p, st);
-    return p.act == 0 ? launch_nb<2, false>(p, st) : launch_nb<1, false>(p, st);
+    if (p.act == 0)
+        return ext ? launch_nb<2, true, false>(p, st) : launch_nb<2, false, false>(p, st);
+    if (p.T == 1)
+        return ext ? launch_nb<1, true, true>(p, st) : launch_nb<1, false, true>(p, st);
+    return ext ? launch_nb<1, true, false>(p, st) : launch_nb<1, false, false>(p, st);
 }
 
 } // namespace mx
