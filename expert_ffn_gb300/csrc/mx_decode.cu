@@ -360,16 +360,24 @@ __device__ __forceinline__ void fix_factor(float m, float &f, float &inv)
     f = __uint_as_float((uint32_t)(127 + k) << 23);
     inv = __uint_as_float((uint32_t)(127 - k) << 23);
 }
-// round(v * 2^32) as a 64-bit integer with 32-bit conversions (64-bit ones are
-// slow here).  For a = |v|: a = h + f with h = floor(a) an integer and f in
-// [0, 1), both exact, and h * 2^32 even, so round(a 2^32) = h 2^32 +
-// round(f 2^32) (below 2^32); round to nearest even is odd-symmetric.  Exact
-// for |v| < 2^31.
+// round(v * 2^32) as a 64-bit integer, exact for |v| < 2^23, on the integer
+// and fp32 pipes only (no float-to-integer conversion).  A = |v| 2^32 is
+// exact (a power-of-two scaling).  Below 2^23, A + 2^23 is a float whose ulp
+// is 1, so the addition rounds A to nearest even and the sum's bits minus
+// those of 2^23 are round(A) (a carry into the exponent yields 2^23 as well).
+// From 2^23 up A is an integer: its significand with the hidden bit, shifted
+// left by (biased exponent - 150) <= 31.  Round to nearest even is
+// odd-symmetric, so the sign is applied last.
 __device__ __forceinline__ long long to_fix(float v)
 {
-    const float a = fabsf(v), h = floorf(a);
-    const long long m = (long long)(((unsigned long long)__float2uint_rn(h) << 32) |
-                                    (unsigned long long)__float2uint_rn((a - h) * kFix));
+    const float A = fabsf(v) * kFix;
+    const uint32_t b = __float_as_uint(A);
+    const bool small = A < 8388608.0f;
+    const uint32_t rs = __float_as_uint(A + 8388608.0f) - 0x4B000000u;
+    const uint32_t mant = (b & 0x7FFFFFu) | 0x800000u, sh = (b >> 23) - 150u;
+    const uint32_t lo = small ? rs : __funnelshift_l(0u, mant, sh);
+    const uint32_t hi = small ? 0u : __funnelshift_l(mant, 0u, sh);
+    const long long m = (long long)(((unsigned long long)hi << 32) | lo);
     return v < 0.f ? -m : m;
 }
 
