@@ -112,6 +112,20 @@ __device__ __forceinline__ void plane_scale(float m, float &sc, float &back)
     back = __uint_as_float((uint32_t)(127 + 9 - k) << 23);
 }
 
+// Power-of-two scale 2^k putting the largest magnitude m in [2^(B-2),
+// 2^(B-1)) for a B-bit fixed-point copy, and 2^-k; k is clamped to
+// [-126, 126] so that both are normal floats (a vector below 2^(B-128) keeps
+// fewer bits).
+template <int B>
+__device__ __forceinline__ void fixb_scale(float m, float &sc, float &inv)
+{
+    const int E = (int)((__float_as_uint(m) >> 23) & 0xFF) - 127;
+    int k = B - 2 - E;
+    k = k > 126 ? 126 : (k < -126 ? -126 : k);
+    sc = __uint_as_float((uint32_t)(127 + k) << 23);
+    inv = __uint_as_float((uint32_t)(127 - k) << 23);
+}
+
 // Split 8 scaled values into NP e4m3 planes; plane p -> (even elements, odd
 // elements) as the b0/b1 register pair of one MMA k-step.
 template <int NP>
@@ -568,6 +582,47 @@ __device__ __forceinline__ void gu_item_t1(const uint8_t *st, int G, const uint8
     accu = au;
 }
 
+// Down slice, one token of BF16 activations: the 16 nibbles of one row that a
+// lane holds (columns 16c .. 16c + 15, two packed words) against the same
+// columns of the unit's hidden vector as 24-bit fixed point in three byte
+// planes (h0, h1 unsigned low and middle bytes, h2 signed high bytes, each in
+// the nibble order of the two words).  Each plane's sum is exact in int32 and
+// the total |sum| < 16 * 15 * 2^23 < 2^31 too; returned as a float (rounded
+// once, to 24 bits).
+__device__ __forceinline__ float dn_row_t1(uint2 q, const uint4 &h0, const uint4 &h1, const uint4 &h2)
+{
+    int g0 = 0, g1 = 0, g2 = 0;
+    uint32_t lo = q.x & kLo, hi = (q.x >> 4) & kLo;
+    g0 = dp4a_uu(lo, h0.x, g0);
+    g0 = dp4a_uu(hi, h0.y, g0);
+    g1 = dp4a_uu(lo, h1.x, g1);
+    g1 = dp4a_uu(hi, h1.y, g1);
+    g2 = dp4a_us(lo, h2.x, g2);
+    g2 = dp4a_us(hi, h2.y, g2);
+    lo = q.y & kLo;
+    hi = (q.y >> 4) & kLo;
+    g0 = dp4a_uu(lo, h0.z, g0);
+    g0 = dp4a_uu(hi, h0.w, g0);
+    g1 = dp4a_uu(lo, h1.z, g1);
+    g1 = dp4a_uu(hi, h1.w, g1);
+    g2 = dp4a_us(lo, h2.z, g2);
+    g2 = dp4a_us(hi, h2.w, g2);
+    return (float)(g2 * 65536 + g1 * 256 + g0);
+}
+
+// The four lanes c of a row group hold partial sums of 4 rows (a0, a8: rows
+// gid, gid + 8 of one tile; b0, b8: the same rows of a second tile); two
+// shuffle stages leave each lane one complete row sum, the other partials
+// having moved to the lanes that keep them: lane c = 0 -> a0, 1 -> b0,
+// 2 -> a8, 3 -> b8.  The additions run in the same order on every call.
+__device__ __forceinline__ float transpose_sum4(float a0, float a8, float b0, float b8, int c)
+{
+    const bool sb = c & 1, s8 = c & 2;
+    const float k0 = (sb ? b0 : a0) + __shfl_xor_sync(0xffffffffu, sb ? a0 : b0, 1);
+    const float k8 = (sb ? b8 : a8) + __shfl_xor_sync(0xffffffffu, sb ? a8 : b8, 1);
+    return (s8 ? k8 : k0) + __shfl_xor_sync(0xffffffffu, s8 ? k0 : k8, 2);
+}
+
 // One 16-row x 64-column tile of a unit's down slice (one group), one warp;
 // t0: this lane's bytes of the tile (tile + gid * 32 + c * 8); sb0 / sb8: the
 // BF16 scale (low half) and bias (high half) of rows gid and gid + 8.  hb: the
@@ -745,7 +800,10 @@ __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
     csync();
     if (tid < T) {
         float sc, bk;
-        plane_scale(__int_as_float(s.vmax[tid]), sc, bk);
+        if constexpr (T1)
+            fixb_scale<16>(__int_as_float(s.vmax[tid]), sc, bk);
+        else
+            plane_scale(__int_as_float(s.vmax[tid]), sc, bk);
         s.xsc[tid] = sc;
         s.fx[tid] = bk;
     }
@@ -785,8 +843,9 @@ __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
             x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
         }
         if constexpr (T1) {
-            // 16-bit fixed point: x 2^(k+7), max |x| 2^(k+7) in [2^14, 2^15)
-            const float sc = s.xsc[t] * 128.0f;
+            // 16-bit fixed point: x 2^k, max |x| 2^k in [2^14, 2^15) (a BF16
+            // value there is an integer of at most 32640)
+            const float sc = s.xsc[t];
             uint32_t lo[2] = {0u, 0u}, hi[2] = {0u, 0u};  // [even, odd columns]
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -1263,6 +1322,48 @@ __device__ void unit_planes(const float *uh, int ne, uint8_t *upl, float *ux, fl
     }
 }
 
+// One token: the unit's hidden vector (64 values, uh[4 i]) as 24-bit fixed
+// point in the byte planes of dn_row_t1, lane c's 48 bytes at upl + 64 c (low,
+// middle, high plane, 16 bytes each); ux = its sum, ufo = 2^-k (h 2^k
+// rounded, the largest magnitude in [2^22, 2^23), 2^23 clamped to 2^23 - 1).
+// Warp 0.
+__device__ void unit_planes_t1(const float *uh, uint8_t *upl, float *ux, float *ufo)
+{
+    const int lane = threadIdx.x & 31, w = lane & 7;
+    float x[8], sm = 0.f, mx = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        x[j] = uh[(8 * w + j) * 4];
+        sm += x[j];
+        mx = fmaxf(mx, fabsf(x[j]));
+    }
+#pragma unroll
+    for (int d = 1; d < 8; d <<= 1) {
+        sm += __shfl_xor_sync(0xffffffffu, sm, d);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, d));
+    }
+    float sc, inv;
+    fixb_scale<24>(mx, sc, inv);
+    if (lane < 8) {
+        uint32_t b[3][2] = {};  // [plane][even, odd columns]
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int v = min(__float2int_rn(x[j] * sc), 8388607);
+#pragma unroll
+            for (int pl = 0; pl < 3; ++pl)
+                b[pl][j & 1] |= (uint32_t)((v >> (8 * pl)) & 0xFF) << (8 * (j >> 1));
+        }
+        uint8_t *dst = upl + (w >> 1) * 64 + (w & 1) * 8;
+#pragma unroll
+        for (int pl = 0; pl < 3; ++pl)
+            *reinterpret_cast<uint2 *>(dst + 16 * pl) = make_uint2(b[pl][0], b[pl][1]);
+        if (w == 0) {
+            ux[0] = sm;
+            ufo[0] = inv;
+        }
+    }
+}
+
 template <int NB, bool EXT, bool T1>
 __device__ void consumers(const PdParams &p, const Smem &s)
 {
@@ -1370,7 +1471,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 } else {
                     float ag = 0.f, au = 0.f;
                     if constexpr (T1)
-                        gu_item_t1(s.ring + (size_t)sl * o.slot, GD, s.xpl + c * 32, s.fx[0] * (1.0f / 65536.0f),
+                        gu_item_t1(s.ring + (size_t)sl * o.slot, GD, s.xpl + c * 32, s.fx[0],
                                    s.xg, ag, au);
                     else
                         gu_item<NB>(s.ring + (size_t)sl * o.slot, GD, bp, bvalid ? xgs : 0, bvalid ? xms : 0,
@@ -1392,8 +1493,12 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 return false;
             if (tr_first)
                 PD_STAMP(l, 6);
-            if (warp == 0)
-                unit_planes(s.uh, ne, s.upl, s.ux, s.ufo);
+            if (warp == 0) {
+                if constexpr (T1)
+                    unit_planes_t1(s.uh, s.upl, s.ux, s.ufo);
+                else
+                    unit_planes(s.uh, ne, s.upl, s.ux, s.ufo);
+            }
             csync();
             if (tr_first)
                 PD_STAMP(l, 7);
@@ -1405,9 +1510,16 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             // one MMA: half the MMAs and B operands per tile.
             const bool one = ne <= 2;
             uint2 hb[4] = {};
+            uint4 h0 = {}, h1 = {}, h2 = {};  // one token: this lane's byte planes of h
             int oc;   // this lane's hidden vector
             bool out; // whether this lane adds its rows into y
-            if (one) {
+            if (T1) {
+                h0 = *reinterpret_cast<const uint4 *>(s.upl + c * 64);
+                h1 = *reinterpret_cast<const uint4 *>(s.upl + c * 64 + 16);
+                h2 = *reinterpret_cast<const uint4 *>(s.upl + c * 64 + 32);
+                oc = 0;
+                out = true;
+            } else if (one) {
                 const int v = gid >> 2, pl = gid & 3;
                 if (v < ne) {
                     const uint8_t *b1p = s.upl + v * 256 + (pl >> 1) * 64 + (pl & 1) * 32 + c * 8;
@@ -1453,6 +1565,20 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                     // two row tiles at a time (the second repeats the first past the end)
                     const int rt2 = rt + kCW < nrt ? rt + kCW : rt;
                     const int r0 = 16 * rt + gid, r2 = 16 * rt2 + gid;
+                    if constexpr (T1) {
+                        // every lane ends with one row of the two tiles (lane c:
+                        // tile rt or rt2 by bit 0, row gid or gid + 8 by bit 1)
+                        const uint8_t *ta = tile + rt * 512, *tb = tile + rt2 * 512;
+                        const float R = transpose_sum4(
+                            dn_row_t1(lds64(ta), h0, h1, h2), dn_row_t1(lds64(ta + 256), h0, h1, h2),
+                            dn_row_t1(lds64(tb), h0, h1, h2), dn_row_t1(lds64(tb + 256), h0, h1, h2), c);
+                        const int r = 16 * ((c & 1) ? rt2 : rt) + gid + 4 * (c & 2);
+                        const uint32_t sb = isb[r];
+                        const float a = fmaf(bf2f((uint16_t)(sb >> 16)), hX, bf2f((uint16_t)sb) * (R * hfo));
+                        if ((c & 1) == 0 || rt2 != rt)
+                            red_fix(yv + q * R4 + r, a, yf, bad);
+                        continue;
+                    }
                     float a0, a8, b0, b8;
                     if (one) {
                         dn_tile<true>(tile + rt * 512, hb, isb[r0], isb[r0 + 8], hfo, hX, a0, a8);
