@@ -170,9 +170,18 @@ __device__ unsigned long long g_pd_trace[kTraceCtas][kTracePts];
         if (threadIdx.x == 0 && (l) == kTraceLayer && blockIdx.x < kTraceCtas)                    \
             g_pd_trace[blockIdx.x][i] = global_ns();                                              \
     } while (0)
+// the same from whichever thread reaches it (the caller picks one)
+#define PD_STAMP_ANY(l, i)                                                                        \
+    do {                                                                                          \
+        if ((l) == kTraceLayer && blockIdx.x < kTraceCtas)                                        \
+            g_pd_trace[blockIdx.x][i] = global_ns();                                              \
+    } while (0)
 #else
 #define PD_STAMP(l, i) \
     do {               \
+    } while (0)
+#define PD_STAMP_ANY(l, i) \
+    do {                   \
     } while (0)
 #endif
 
@@ -1280,6 +1289,8 @@ __device__ void producer(const PdParams &p, const Smem &s)
         if (!(ok = __shfl_sync(0xffffffffu, good, 0) != 0))
             break;
         const int nr = *s.rt.n_act * GI;
+        if (lane == 0 && first_routed(C, NC, GS) < nr)
+            PD_STAMP_ANY(l, 23);
         for (int r = first_routed(C, NC, GS); r < nr && ok; r += NC)
             ok = issue_unit(L, false, EXT ? act_r(s.rt, p.E)[r / GI] : s.rt.act_e[r / GI], r % GI);
     }
@@ -1469,6 +1480,8 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 if (!__all_sync(0xffffffffu, w_ok && pwait(&s.full[sl], (kk / o.NR) & 1, p))) {
                     good = false;
                 } else {
+                    if (tr_first && lane == 0 && (warp == 0 || warp == kCW - 1))
+                        PD_STAMP_ANY(l, warp == 0 ? 20 : 21);
                     float ag = 0.f, au = 0.f;
                     if constexpr (T1)
                         gu_item_t1(s.ring + (size_t)sl * o.slot, GD, s.xpl + c * 32, s.fx[0],
@@ -1477,6 +1490,8 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                         gu_item<NB>(s.ring + (size_t)sl * o.slot, GD, bp, bvalid ? xgs : 0, bvalid ? xms : 0,
                                     bvalid ? xnbs : 0, s.fx[ot], s.xg + ot * GD, ag, au);
                     __syncwarp();
+                    if (tr_first && lane == 0 && warp == kCW - 1)
+                        PD_STAMP_ANY(l, 22);
                     if (lane == 0)
                         mbar_arrive_n(&s.empty[sl], kCW);
                     if (c < ne) {

@@ -14,9 +14,11 @@ router rows, the shared-expert units, the logit exchange, top-k / softmax /
 grouping, the routed units, the y exchange, the rebuild of x_{l+1}.  CTAs
 without shared units pass the shared-unit phase at once, and CTAs without
 routed units the routed one.  Indented rows time the inside of each CTA's
-first routed unit (over the CTAs that hold one): the end of its gate/up work,
-of the planes of h, and when each of its four down items had landed in shared
-memory and was done.
+first routed unit (over the CTAs that hold one): when the producer warp saw
+the routing, when the gate/up items of consumer warps 0 and 7 had landed
+(item 0 and item 7 of the unit) and when warp 7's was done, the end of its
+gate/up work, of the planes of h, and when each of its four down items had
+landed in shared memory and was done.
 """
 from __future__ import annotations
 
@@ -28,8 +30,9 @@ import sys
 PHASES = ["layer start", "prologue", "router rows", "shared units", "logit exchange", "top-k + grouping",
           "  unit gate/up", "  unit h planes", None, "routed units", "y exchange", "x rebuild",
           "  down 0 landed", "  down 1 landed", "  down 2 landed", "  down 3 landed",
-          "  down 0 done", "  down 1 done", "  down 2 done", "  down 3 done"]
-UNIT_PHASES = range(6, 20)  # inside the first routed unit of a CTA (CTAs that hold one)
+          "  down 0 done", "  down 1 done", "  down 2 done", "  down 3 done",
+          "  item 0 landed", "  item 7 landed", "  item 7 done", "  routing seen"]
+UNIT_PHASES = range(6, 24)  # inside the first routed unit of a CTA (CTAs that hold one)
 TRACE_LAYER, TRACE_CTAS, TRACE_PTS = 10, 160, 24
 
 
@@ -100,7 +103,7 @@ def main(argv=None) -> int:
     print(f"single-launch decode, d_model {cfg.D}, {cfg.E} experts top-{cfg.K}, T={T}, {cfg.layers} layers: "
           f"layer {TRACE_LAYER}, {ncta} CTAs, median of {args.runs} launches (us)")
     print(f"{'phase ends':18s} {'median CTA':>10s} {'fastest':>9s} {'slowest':>9s}")
-    order = [0, 1, 2, 3, 4, 5, 6, 7, 12, 16, 13, 17, 14, 18, 15, 19, 9, 10, 11]  # kernel order
+    order = [0, 1, 2, 3, 4, 5, 23, 20, 21, 22, 6, 7, 12, 16, 13, 17, 14, 18, 15, 19, 9, 10, 11]  # kernel order
     for i in order:
         a = np.median(np.array(rows[i]), axis=0)
         print(f"{PHASES[i]:18s} {a[0]:10.2f} {a[1]:9.2f} {a[2]:9.2f}")
