@@ -163,7 +163,7 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, i
 // Optional phase trace (built with -DMX_PD_TRACE): consumer thread 0 of every
 // CTA records %globaltimer at the phase edges of one layer.
 #ifdef MX_PD_TRACE
-constexpr int kTraceLayer = 10, kTraceCtas = 160, kTracePts = 24;
+constexpr int kTraceLayer = 10, kTraceCtas = 160, kTracePts = 32;
 __device__ unsigned long long g_pd_trace[kTraceCtas][kTracePts];
 #define PD_STAMP(l, i)                                                                            \
     do {                                                                                          \
@@ -529,10 +529,11 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
 // 16c .. 16c + 15 of rows gid (gate) and gid (up): per group 16 byte dot
 // products, exact in int32 (|sum| < 2^23, so exact in fp32 too); then the
 // group's scale and bias terms in fp32, the bias term once per row (lane c =
-// 0), and the four lanes of a row added by shuffles.  fo = 2^-k1.  Lane
-// output: gate and up dot products of row gid (every lane of the row).
-__device__ __forceinline__ void gu_item_t1(const uint8_t *st, int G, const uint8_t *xp, float fo, const float *xg,
-                                           float &accg, float &accu)
+// 0), and the four lanes of a row added by shuffles.  fo = 2^-k1.  The warp
+// takes groups [g0, g1) of the item.  Lane output: that part of the gate and
+// up dot products of row gid (every lane of the row).
+__device__ __forceinline__ void gu_item_t1(const uint8_t *st, int G, int g0, int g1, const uint8_t *xp, float fo,
+                                           const float *xg, float &accg, float &accu)
 {
     const int lane = threadIdx.x & 31, gid = lane >> 2, c = lane & 3;
     const uint8_t *gt = st + gid * 32 + c * 8, *ut = gt + 256 * G;
@@ -541,8 +542,8 @@ __device__ __forceinline__ void gu_item_t1(const uint8_t *st, int G, const uint8
     const float bsel = c == 0 ? 1.f : 0.f;
     float pg[2] = {0.f, 0.f}, pu[2] = {0.f, 0.f}, qg[2] = {0.f, 0.f}, qu[2] = {0.f, 0.f};
 #pragma unroll 2
-    for (int g = 0; g < G; ++g) {
-        const int h = g & 1;
+    for (int n = 0; n < g1 - g0; ++n) {
+        const int g = g0 + n, h = n & 1;
         const uint2 wg = lds64(gt + 256 * g), wu = lds64(ut + 256 * g);
         const uint4 x0 = *reinterpret_cast<const uint4 *>(xp + 128 * g);
         const uint4 x1 = *reinterpret_cast<const uint4 *>(xp + 128 * g + 16);
@@ -701,8 +702,9 @@ __device__ __forceinline__ void store_planes(uint8_t *dst, bool per_slot, int nv
 // sums in the canonical order (the router's X), and its e4m3 planes (T1: the
 // byte planes of gu_item_t1).
 template <int NB, bool EXT, bool T1>
-__device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
+__device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s, int l)
 {
+    (void)l;
     constexpr int es = NB == 1 ? 2 : 4;
     const int tid = threadIdx.x, lane = tid & 31, T = p.T, D = p.D, GD = D / 64;
     auto ld64 = [&](const uint8_t *base, int t, int g, float (&v)[64]) {
@@ -756,6 +758,7 @@ __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
         }
     }
     csync();
+    PD_STAMP(l, 24);
     // elementwise: xq = round(x * r), the magnitude maximum per token
     {
         const int n8 = T * D / 8;  // 8-value words
@@ -807,6 +810,7 @@ __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
         (void)lane;
     }
     csync();
+    PD_STAMP(l, 25);
     if (tid < T) {
         float sc, bk;
         if constexpr (T1)
@@ -823,6 +827,7 @@ __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
         fix_factor(__int_as_float(m), s.yfx[0], s.yfx[1]);
     }
     csync();
+    PD_STAMP(l, 26);
     // group sums in the canonical order (the router's X), and the planes
     for (int i = tid; i < T * GD; i += kCT) {
         const int t = i / GD, g = i - t * GD;
@@ -882,6 +887,7 @@ __device__ void prologue(const PdParams &p, const PdLayer &L, const Smem &s)
             *reinterpret_cast<uint2 *>(s.xpl + off) = pl[q];
         }
     }
+    PD_STAMP(l, 27);
     if (EXT && L.shared_gate) {
         // shared-branch gate sigmoid(g . x): per group an fma chain, then the
         // groups in order
@@ -1050,8 +1056,9 @@ __device__ void router_rows(const PdParams &p, const PdLayer &L, const Smem &s, 
 // selected logits times the per-expert scale, and the grouping of slots by
 // expert (ascending expert, ascending slot).  All consumer threads.
 template <bool EXT>
-__device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
+__device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s, int l)
 {
+    (void)l;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, T = p.T, E = p.E, K = p.K;
     const Rt &rt = s.rt;
     // top-K and softmax, one warp per token: lane l holds the logits of
@@ -1071,6 +1078,7 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
             // monotone in v; taken and absent entries get 0, below every key
             key[j] = e < E ? (u & 0x80000000u ? ~u : u | 0x80000000u) : 0u;
         }
+        PD_STAMP(l, 28);
         int mye = 0;
         float myv = 0.f;
         for (int k = 0; k < K; ++k) {
@@ -1113,6 +1121,7 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s)
                 L.topk_w[t * K + lane] = x;
             }
         }
+        PD_STAMP(l, 29);
     }
     if (E > 128) {
         // more than 128 experts: each logit's rank by a scan of its row
@@ -1409,7 +1418,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 dst[i] = __ldg(src + i);
             csync();
         }
-        prologue<NB, EXT, T1>(p, L, s);
+        prologue<NB, EXT, T1>(p, L, s, l);
         PD_STAMP(l, 1);
         router_rows<NB, EXT>(p, L, s, rq, rsv, rbv);  // ends with a consumer barrier
         PD_STAMP(l, 2);
@@ -1455,8 +1464,53 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                                    : 0u;
                 }
             }
-            // gate/up: warp w owns item k + w
-            {
+            if constexpr (T1) {
+                // gate/up, one token: the 8 items in halves of their groups;
+                // warp w < 4 takes half 0 of item w, then half 1 of item w + 4,
+                // warp w >= 4 half 1 of item w - 4, then half 0 of item w, so
+                // the last items to land are shared by two warps.  The halves'
+                // partial row sums (in x_q's buffer: the router has read it)
+                // are added in half order, the same on every call.
+                float2 *part = reinterpret_cast<float2 *>(s.xq);  // [item][half][row]
+                const int Gh = GD / 2;
+                for (int task = 0; task < 2 && good; ++task) {
+                    const int it = warp < 4 ? warp + 4 * task : warp - 4 + 4 * task;
+                    const int hf = warp < 4 ? task : 1 - task;
+                    const int kk = k + it, sl = kk % o.NR;
+                    // with fewer slots than items, wait for the release of the
+                    // slot's previous item first (see the general case below)
+                    const bool w_ok = it < o.NR || pwait(&s.empty[sl], ((kk / o.NR) - 1) & 1, p);
+                    if (!__all_sync(0xffffffffu, w_ok && pwait(&s.full[sl], (kk / o.NR) & 1, p))) {
+                        good = false;
+                        break;
+                    }
+                    if (tr_first && lane == 0 && ((warp == 0 && task == 0) || (warp == kCW - 1 && task == 1)))
+                        PD_STAMP_ANY(l, task == 0 ? 20 : 21);
+                    float ag, au;
+                    gu_item_t1(s.ring + (size_t)sl * o.slot, GD, hf ? Gh : 0, hf ? GD : Gh, s.xpl + c * 32, s.fx[0],
+                               s.xg, ag, au);
+                    if (c == 0)
+                        part[(it * 2 + hf) * 8 + gid] = make_float2(ag, au);
+                    __syncwarp();
+                    if (tr_first && lane == 0 && warp == kCW - 1 && task == 1)
+                        PD_STAMP_ANY(l, 22);
+                    if (lane == 0)
+                        mbar_arrive_n(&s.empty[sl], kCW / 2);
+                }
+                if (!(good = csync_and(good)))
+                    return false;
+                if (tid < 64) {  // hidden row tid = 8 item + row
+                    const float2 a = part[((tid >> 3) * 2) * 8 + (tid & 7)];
+                    const float2 b = part[((tid >> 3) * 2 + 1) * 8 + (tid & 7)];
+                    float h = gelu_tanh(a.x + b.x) * (a.y + b.y);
+                    if (!shared)
+                        h *= s.rt.slot_w[s.rt.act_slot[4 * j]];
+                    else if (EXT && L.shared_gate)
+                        h *= s.yfx[4];
+                    s.uh[tid * 4] = h;
+                }
+            } else {
+                // gate/up: warp w owns item k + w
                 const int kk = k + warp, sl = kk % o.NR;
                 int bt, ot, oslot = 0;
                 bool bvalid;
@@ -1480,18 +1534,10 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 if (!__all_sync(0xffffffffu, w_ok && pwait(&s.full[sl], (kk / o.NR) & 1, p))) {
                     good = false;
                 } else {
-                    if (tr_first && lane == 0 && (warp == 0 || warp == kCW - 1))
-                        PD_STAMP_ANY(l, warp == 0 ? 20 : 21);
                     float ag = 0.f, au = 0.f;
-                    if constexpr (T1)
-                        gu_item_t1(s.ring + (size_t)sl * o.slot, GD, s.xpl + c * 32, s.fx[0],
-                                   s.xg, ag, au);
-                    else
-                        gu_item<NB>(s.ring + (size_t)sl * o.slot, GD, bp, bvalid ? xgs : 0, bvalid ? xms : 0,
-                                    bvalid ? xnbs : 0, s.fx[ot], s.xg + ot * GD, ag, au);
+                    gu_item<NB>(s.ring + (size_t)sl * o.slot, GD, bp, bvalid ? xgs : 0, bvalid ? xms : 0,
+                                bvalid ? xnbs : 0, s.fx[ot], s.xg + ot * GD, ag, au);
                     __syncwarp();
-                    if (tr_first && lane == 0 && warp == kCW - 1)
-                        PD_STAMP_ANY(l, 22);
                     if (lane == 0)
                         mbar_arrive_n(&s.empty[sl], kCW);
                     if (c < ne) {
@@ -1629,8 +1675,10 @@ __device__ void consumers(const PdParams &p, const Smem &s)
         // the routing, once every CTA's logits are in
         if (!(ok = csync_and(ok)))
             break;
+        PD_STAMP(l, 30);
         if (!(ok = cwait(ctr + 0, NC, p, s)))
             break;
+        PD_STAMP(l, 31);
         if (l > 0) {
             // every CTA has rebuilt x_l from y_{l-1} before its logits of layer
             // l arrived: clear this CTA's share of y_{l-1} for the next call
@@ -1640,7 +1688,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
                 yp[i] = 0;
         }
         PD_STAMP(l, 4);
-        route_tables<EXT>(p, L, s);
+        route_tables<EXT>(p, L, s, l);
         if (tid == 0)
             mbar_arrive(s.route_bar);
         PD_STAMP(l, 5);
@@ -1814,7 +1862,9 @@ bool pd_plan(int T, int D, int I, int S, int E, int K, int act, int n_cta, int s
         };
         o.ring = take((size_t)o.NR * o.slot);
         o.xraw = take((size_t)T * D * es);
-        o.xq = take((size_t)T * D * es);
+        // (one BF16 token: also the 1 KB of gate/up partial sums once the
+        // router has read x_q)
+        o.xq = take(std::max((size_t)T * D * es, T == 1 && act == 1 ? (size_t)1024 : (size_t)0));
         o.xg = take((size_t)T * GD * 4);
         o.xpl = take((size_t)GD * 128 * NB * T);
         o.uh = take((size_t)64 * 4 * 4);

@@ -9,14 +9,17 @@ median, fastest and slowest CTA, each the median over several launches.
 
     python -m expert_ffn_gb300.phase_trace [--runs N]
 
-Phases, in kernel order: start of the layer, prologue (RMSNorm, planes of x),
-router rows, the shared-expert units, the logit exchange, top-k / softmax /
-grouping, the routed units, the y exchange, the rebuild of x_{l+1}.  CTAs
-without shared units pass the shared-unit phase at once, and CTAs without
-routed units the routed one.  Indented rows time the inside of each CTA's
+Phases, in kernel order: start of the layer, prologue (RMSNorm, planes of x;
+indented: its sum of squares, elementwise pass, plane scale, group sums and
+planes), router rows, the shared-expert units, the logit exchange (indented:
+the CTA's own barrier, the grid counter reached), top-k / softmax / grouping
+(indented: logit loads issued, top-k and softmax done), the routed units, the
+y exchange, the rebuild of x_{l+1}.  CTAs without shared units pass the
+shared-unit phase at once, and CTAs without routed units the routed one.
+Other indented rows time the inside of each CTA's
 first routed unit (over the CTAs that hold one): when the producer warp saw
-the routing, when the gate/up items of consumer warps 0 and 7 had landed
-(item 0 and item 7 of the unit) and when warp 7's was done, the end of its
+the routing, when item 0 and item 7 of its gate/up work had landed (as warp 0
+and warp 7 saw them) and when warp 7 was done with item 7, the end of its
 gate/up work, of the planes of h, and when each of its four down items had
 landed in shared memory and was done.
 """
@@ -31,9 +34,11 @@ PHASES = ["layer start", "prologue", "router rows", "shared units", "logit excha
           "  unit gate/up", "  unit h planes", None, "routed units", "y exchange", "x rebuild",
           "  down 0 landed", "  down 1 landed", "  down 2 landed", "  down 3 landed",
           "  down 0 done", "  down 1 done", "  down 2 done", "  down 3 done",
-          "  item 0 landed", "  item 7 landed", "  item 7 done", "  routing seen"]
+          "  item 0 landed", "  item 7 landed", "  item 7 done", "  routing seen",
+          "  sum of squares", "  elementwise", "  plane scale", "  group sums, planes",
+          "  logits loads issued", "  top-k, softmax", "  own barrier", "  counter reached"]
 UNIT_PHASES = range(6, 24)  # inside the first routed unit of a CTA (CTAs that hold one)
-TRACE_LAYER, TRACE_CTAS, TRACE_PTS = 10, 160, 24
+TRACE_LAYER, TRACE_CTAS, TRACE_PTS = 10, 160, 32
 
 
 def build_trace_lib() -> str:
@@ -103,7 +108,8 @@ def main(argv=None) -> int:
     print(f"single-launch decode, d_model {cfg.D}, {cfg.E} experts top-{cfg.K}, T={T}, {cfg.layers} layers: "
           f"layer {TRACE_LAYER}, {ncta} CTAs, median of {args.runs} launches (us)")
     print(f"{'phase ends':18s} {'median CTA':>10s} {'fastest':>9s} {'slowest':>9s}")
-    order = [0, 1, 2, 3, 4, 5, 23, 20, 21, 22, 6, 7, 12, 16, 13, 17, 14, 18, 15, 19, 9, 10, 11]  # kernel order
+    order = [0, 24, 25, 26, 27, 1, 2, 3, 30, 31, 4, 28, 29, 5, 23, 20, 21, 22, 6, 7, 12, 16, 13, 17, 14, 18, 15,
+             19, 9, 10, 11]  # kernel order
     for i in order:
         a = np.median(np.array(rows[i]), axis=0)
         print(f"{PHASES[i]:18s} {a[0]:10.2f} {a[1]:9.2f} {a[2]:9.2f}")
