@@ -15,17 +15,18 @@ from .build import LIB as LIB_PATH
 
 __all__ = ["MxError", "lib", "QLinear", "Ffn", "Sub", "Layout", "Options", "LAYOUT_MAGIC", "LAYOUT_VERSION",
            "MX_F32", "MX_BF16", "DeviceLayer", "layer_forward", "layer_forward_ex", "route", "stack_forward",
-           "workspace_bytes", "stack_workspace_bytes", "workspace_init", "layer_forward_static", "EXPORTED"]
+           "workspace_bytes", "stack_workspace_bytes", "workspace_init", "layer_forward_static", "EXPORTED",
+           "down_sb_bytes", "pack_down_sb"]
 
 LAYOUT_MAGIC = 0x4D584D45
-LAYOUT_VERSION = 2
+LAYOUT_VERSION = 3
 MX_F32, MX_BF16 = 0, 1
 
 # Every symbol include/mx_moe.h declares.
 EXPORTED = ("mx_moe_layer_forward", "mx_moe_layer_forward_ex", "mx_moe_workspace_bytes", "mx_moe_workspace_init",
             "mx_moe_route", "mx_moe_stack_forward", "mx_moe_stack_workspace_bytes", "mx_status_string",
             "mx_last_error_string", "mx_version", "mx_moe_profile_enable", "mx_moe_profile_read",
-            "mx_moe_workspace_check", "mx_moe_layer_forward_static")
+            "mx_moe_workspace_check", "mx_moe_layer_forward_static", "mx_moe_down_sb_bytes", "mx_moe_pack_down_sb")
 
 
 class MxError(RuntimeError):
@@ -54,7 +55,9 @@ class Layout(C.Structure):
                 ("act_dtype", C.c_int32), ("layer_scalar", C.c_float), ("per_expert_scale", C.c_void_p),
                 # version 2: optional parts of the layer (NULL = absent)
                 ("expert_slot", C.c_void_p), ("n_slots", C.c_int32), ("router_scale", C.c_void_p),
-                ("post_norm", C.c_void_p), ("post_eps", C.c_float), ("shared_expert_gate", C.c_void_p)]
+                ("post_norm", C.c_void_p), ("post_eps", C.c_float), ("shared_expert_gate", C.c_void_p),
+                # version 3: the packed down-projection scale / bias words (NULL = absent)
+                ("down_sb", C.c_void_p)]
 
 
 class Options(C.Structure):
@@ -83,6 +86,9 @@ def lib():
             L.mx_moe_stack_workspace_bytes.argtypes = [C.POINTER(Layout), I32]
             L.mx_moe_stack_workspace_bytes.restype = SZ
             L.mx_moe_workspace_init.argtypes = [P, SZ, P]
+            L.mx_moe_down_sb_bytes.argtypes = [C.POINTER(Layout)]
+            L.mx_moe_down_sb_bytes.restype = SZ
+            L.mx_moe_pack_down_sb.argtypes = [C.POINTER(Layout), P, C.POINTER(QLinear), P, P]
             L.mx_moe_route.argtypes = [P, I32, C.POINTER(QLinear), C.POINTER(Layout), P, P, P, P, P, P,
                                        C.POINTER(Options), P, P, SZ]
             L.mx_moe_stack_forward.argtypes = [P, I32, I32, C.POINTER(QLinear), C.POINTER(Ffn), C.POINTER(P),
@@ -95,7 +101,7 @@ def lib():
             L.mx_moe_workspace_check.argtypes = [P, P]
             L.mx_moe_profile_read.argtypes = [C.POINTER(C.c_double), C.POINTER(C.c_int), I32]
             for name in ("mx_moe_layer_forward", "mx_moe_layer_forward_ex", "mx_moe_layer_forward_static",
-                         "mx_moe_workspace_init",
+                         "mx_moe_workspace_init", "mx_moe_pack_down_sb",
                          "mx_moe_route", "mx_moe_stack_forward", "mx_moe_profile_enable", "mx_moe_profile_read",
                          "mx_moe_workspace_check"):
                 getattr(L, name).restype = C.c_int
@@ -133,7 +139,8 @@ def make_qlinear(w, s, b, rows: int, cols: int, bits: int) -> QLinear:
 
 
 def make_layout(D, I, E, K, S, stride, offsets, act_dtype, lam, per_expert_scale=None, expert_slot=None,
-                n_slots=0, router_scale=None, post_norm=None, post_eps=0.0, shared_expert_gate=None) -> Layout:
+                n_slots=0, router_scale=None, post_norm=None, post_eps=0.0, shared_expert_gate=None,
+                down_sb=None) -> Layout:
     L = Layout()
     L.magic, L.version = LAYOUT_MAGIC, LAYOUT_VERSION
     L.d_model, L.d_expert, L.n_experts, L.top_k, L.d_shared = D, I, E, K, S
@@ -151,6 +158,7 @@ def make_layout(D, I, E, K, S, stride, offsets, act_dtype, lam, per_expert_scale
     L.post_norm = _ptr(post_norm)
     L.post_eps = post_eps
     L.shared_expert_gate = _ptr(shared_expert_gate)
+    L.down_sb = _ptr(down_sb)
     return L
 
 
@@ -161,9 +169,12 @@ class DeviceLayer:
     shared_up, shared_down (each with .w .s .b .rows .cols .bits numpy arrays),
     blob, stride, offsets and optionally per_expert_scale and the layer's
     optional parts expert_slot (int16 [E]) with n_slots, router_scale,
-    post_norm (with post_eps) and shared_expert_gate (BF16 bits [D])."""
+    post_norm (with post_eps) and shared_expert_gate (BF16 bits [D]).
 
-    def __init__(self, host, act_dtype: int, device="cuda"):
+    ``pack_down_sb`` (default on) also builds the layout's packed
+    down-projection scale / bias table (mx_moe_pack_down_sb) on the device."""
+
+    def __init__(self, host, act_dtype: int, device="cuda", pack_down_sb: bool = True):
         import numpy as np
         import torch
         self.host = host
@@ -198,12 +209,38 @@ class DeviceLayer:
                                   host.lam, self.pes, self.expert_slot, int(getattr(host, "n_slots", 0) or 0),
                                   self.router_scale, self.post_norm, float(getattr(host, "post_eps", 0.0)),
                                   self.shared_expert_gate)
+        self.down_sb = None
+        if pack_down_sb:
+            self.down_sb = _pack_down_sb(self.layout, self.blob, self.shared.down, device=device)
+            self.layout.down_sb = self.down_sb.data_ptr()
 
     def set_layer_scalar(self, lam: float):
         self.layout.layer_scalar = lam
 
 
 # --------------------------------------------------------------- entry points
+
+def down_sb_bytes(layout: Layout) -> int:
+    return lib().mx_moe_down_sb_bytes(C.byref(layout))
+
+
+def _pack_down_sb(layout: Layout, blob, shared_down: QLinear, device="cuda", stream=None):
+    """The layout's packed down-projection (scale | bias << 16) words as a new
+    device uint8 tensor (mx_moe_pack_down_sb); the copy is done when this
+    returns."""
+    import torch
+    n = down_sb_bytes(layout)
+    if n == 0:
+        _check(-1)
+    out = torch.empty(n, dtype=torch.uint8, device=device)
+    _check(lib().mx_moe_pack_down_sb(C.byref(layout), _ptr(blob), C.byref(shared_down), _ptr(out),
+                                     _stream_handle(stream)))
+    torch.cuda.synchronize(out.device)
+    return out
+
+
+pack_down_sb = _pack_down_sb
+
 
 def workspace_bytes(layout: Layout, T: int) -> int:
     return lib().mx_moe_workspace_bytes(C.byref(layout), T)

@@ -9,6 +9,7 @@
 #include "mx_moe.h"
 #include "mx_internal.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -62,7 +63,7 @@ mx_status check_layout(const mx_moe_layout *L)
         return fail(MX_ERR_INVALID_ARG, "layout is NULL");
     if (L->magic != MX_MOE_LAYOUT_MAGIC)
         return fail(MX_ERR_INVALID_ARG, "layout magic 0x%08x is not 0x%08x", L->magic, MX_MOE_LAYOUT_MAGIC);
-    if (L->version != 1u && L->version != MX_MOE_LAYOUT_VERSION)
+    if (L->version < 1u || L->version > MX_MOE_LAYOUT_VERSION)
         return fail(MX_ERR_INVALID_ARG, "layout version %u is not supported", L->version);
     const int D = L->d_model, I = L->d_expert, E = L->n_experts, K = L->top_k, S = L->d_shared;
     if (L->group != 64)
@@ -119,6 +120,8 @@ mx_status check_layout(const mx_moe_layout *L)
         if (L->post_norm && !(L->post_eps >= 0.0f))
             return fail(MX_ERR_INVALID_ARG, "post_eps must be >= 0");
     }
+    if (L->version >= 3u && L->down_sb && !aligned(L->down_sb, 16))
+        return fail(MX_ERR_ALIGNMENT, "down_sb must be 16-byte aligned");
     return MX_OK;
 }
 
@@ -137,6 +140,8 @@ LayerExt ext_of(const mx_moe_layout *L)
         x.post_eps = L->post_eps;
         x.shared_gate = L->shared_expert_gate;
     }
+    if (L->version >= 3u)
+        x.down_sb = L->down_sb;
     return x;
 }
 
@@ -260,6 +265,11 @@ bool pd_usable(const mx_moe_layout *L, int T, PdSmem *sm, int *n_cta)
     const DevInfo d = dev_info();
     if (!d.sms)
         return false;
+    // the kernel keeps the scale / bias offsets inside an expert record in 32 bits
+    const mx_sub *subs[3] = {&L->gate, &L->up, &L->down};
+    for (int j = 0; j < 3; ++j)
+        if ((subs[j]->s | subs[j]->b) >> 32)
+            return false;
     const int act = L->act_dtype == MX_BF16 ? 1 : 0;
     // leave room for the kernel's static shared memory
     if (!pd_plan(T, L->d_model, L->d_expert, L->d_shared, L->n_experts, L->top_k, act, d.sms, d.smem_optin - 1280,
@@ -370,6 +380,8 @@ mx_status run_pd(const PdIn *in, int n, int T, int pre_norm, float eps, const Pd
         d.residual = c.residual;
         d.res_mode = c.res_mode;
         d.lam = L->layer_scalar;
+        d.dsb = x.down_sb;
+        d.dsb_s = x.down_sb ? x.down_sb + (size_t)x.n_slots * (L->d_expert / 64) * L->d_model : nullptr;
         d.slot = x.slot;
         d.n_slots = x.n_slots;
         d.router_scale = x.router_scale;
@@ -663,6 +675,30 @@ static __device__ __align__(256) unsigned char g_static_scratch[MX_STATIC_SCRATC
 static std::mutex g_static_mu;
 static void *g_static_ptr[64];  // per device ordinal, resolved on the first call
 
+// Column-major copy of the down projections' (scale | bias << 16) words: one
+// thread per output word (record words, then the shared expert's).  A one-off
+// rearrangement: the strided reads are not worth tiling.
+__global__ void pack_down_sb_kernel(const uint8_t *blob, uint64_t stride, uint64_t off_s, uint64_t off_b, int nrec,
+                                    int GI, int D, const uint16_t *ss, const uint16_t *sb, int GS, uint32_t *out)
+{
+    const size_t n_r = (size_t)nrec * GI * D, n = n_r + (size_t)GS * D;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        uint16_t sv, bv;
+        if (i < n_r) {
+            const size_t d = i % D, rg = i / D, r = rg / GI;
+            const int g = (int)(rg % GI);
+            const uint8_t *rec = blob + r * stride;
+            sv = reinterpret_cast<const uint16_t *>(rec + off_s)[d * GI + g];
+            bv = reinterpret_cast<const uint16_t *>(rec + off_b)[d * GI + g];
+        } else {
+            const size_t j = i - n_r, d = j % D, g = j / D;
+            sv = ss[d * GS + g];
+            bv = sb[d * GS + g];
+        }
+        out[i] = (uint32_t)sv | ((uint32_t)bv << 16);
+    }
+}
+
 extern "C" {
 
 const char *mx_version(void) { return "0.1.0"; }
@@ -700,6 +736,42 @@ size_t mx_moe_stack_workspace_bytes(const mx_moe_layout *layout, int T)
     const int t = T < 1 ? 1 : T;
     // the per-layer plan, then the ping-pong activation buffer
     return make_plan(layout, t, ffn_tokens(t)).total + up256((size_t)t * layout->d_model * 4);
+}
+
+size_t mx_moe_down_sb_bytes(const mx_moe_layout *layout)
+{
+    if (check_layout(layout) != MX_OK)
+        return 0;
+    const LayerExt x = ext_of(layout);
+    const size_t D = layout->d_model, GI = layout->d_expert / 64, GS = layout->d_shared / 64;
+    return ((size_t)x.n_slots * GI + GS) * D * 4;
+}
+
+mx_status mx_moe_pack_down_sb(const mx_moe_layout *layout, const void *blob, const mx_qlinear *shared_down,
+                              uint32_t *out, void *stream)
+{
+    mx_status st;
+    if ((st = check_layout(layout)) != MX_OK)
+        return st;
+    if (!blob || !shared_down || !out)
+        return fail(MX_ERR_INVALID_ARG, "mx_moe_pack_down_sb: blob, shared_down and out must not be NULL");
+    const int D = layout->d_model, I = layout->d_expert, S = layout->d_shared;
+    if ((st = check_qlinear(shared_down, "shared.down", D, S, 4)) != MX_OK)
+        return st;
+    if (!aligned(out, 16))
+        return fail(MX_ERR_ALIGNMENT, "mx_moe_pack_down_sb: out must be 16-byte aligned");
+    const LayerExt x = ext_of(layout);
+    const size_t bytes = mx_moe_down_sb_bytes(layout);
+    if (overlap(out, bytes, blob, (size_t)x.n_slots * layout->record_stride))
+        return fail(MX_ERR_INVALID_ARG, "mx_moe_pack_down_sb: out overlaps the blob");
+    const size_t n = bytes / 4;
+    const int blocks = (int)std::min<size_t>((n + 255) / 256, 8192);
+    pack_down_sb_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t *>(blob), layout->record_stride, layout->down.s, layout->down.b, x.n_slots, I / 64,
+        D, static_cast<const uint16_t *>(shared_down->scales), static_cast<const uint16_t *>(shared_down->biases),
+        S / 64, out);
+    const cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? MX_OK : cuda_fail(e, "mx_moe_pack_down_sb");
 }
 
 mx_status mx_moe_workspace_init(void *ws, size_t ws_bytes, void *stream)

@@ -1225,7 +1225,7 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s,
 // expert j, block u) as r = j * GI + u; unit id i goes to CTA i mod NC.
 __device__ __forceinline__ int first_routed(int C, int NC, int GS) { return ((C - GS) % NC + NC) % NC; }
 
-template <int NB, bool EXT>
+template <int NB, bool EXT, bool PK>
 __device__ void producer(const PdParams &p, const Smem &s)
 {
     const int lane = threadIdx.x & 31, C = blockIdx.x, NC = gridDim.x;
@@ -1274,13 +1274,18 @@ __device__ void producer(const PdParams &p, const Smem &s)
                 bulk_g2s(dst + 512 * GD + jj * 16 * GD, src, 16u * GD, bar);
             }
         }
+        // (with the packed down words, each down item also brings its D/4
+        // (scale | bias << 16) words, behind its weights)
         for (int q = 0; q < 4; ++q) {
             uint8_t *dst;
             uint64_t *bar;
-            if (!take(32u * R4, dst, bar))
+            if (!take(32u * R4 + (PK ? 4u * R4 : 0u), dst, bar))
                 return false;
             if (lane < 4)
                 tma_load_4d(dst + lane * 32 * R16, shared ? &L.sdown : &L.down, 0, q * R4 + lane * R16, u, e, bar);
+            else if (PK && lane == 4)
+                bulk_g2s(dst + 32 * R4, (shared ? L.dsb_s + (size_t)u * D : L.dsb + ((size_t)e * GI + u) * D) + q * R4,
+                         4u * R4, bar);
             __syncwarp();
         }
         return true;
@@ -1384,7 +1389,7 @@ __device__ void unit_planes_t1(const float *uh, uint8_t *upl, float *ux, float *
     }
 }
 
-template <int NB, bool EXT, bool T1>
+template <int NB, bool EXT, bool T1, bool PK>
 __device__ void consumers(const PdParams &p, const Smem &s)
 {
     constexpr int es = NB == 1 ? 2 : 4;
@@ -1445,7 +1450,7 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             csync();  // every warp is done with the previous unit
             constexpr int kR = kPdMaxD / kCT;
             uint32_t sbv[kR];  // (bias << 16) | scale of rows tid + i * kCT
-            {
+            if constexpr (!PK) {  // (with PK the down items bring their words)
                 const int G = shared ? GS : GI;
                 const uint16_t *sp, *bq;
                 if (shared) {
@@ -1602,18 +1607,25 @@ __device__ void consumers(const PdParams &p, const Smem &s)
             bool bad = false;  // a partial sum outside the fixed-point range
             long long *yv = y + (size_t)ot * D;
             for (int q = 0; q < 4; ++q) {
-                // this item's (scale | bias << 16) words into buffer q & 1 (the
-                // barrier also tells that every warp is done with item q - 1, so
-                // buffer q & 1, last read for item q - 2, is free)
-                uint32_t *isb = reinterpret_cast<uint32_t *>(s.dss) + (q & 1) * R4;
-#pragma unroll
-                for (int i = 0; i < kR; ++i) {
-                    const int r = tid + i * kCT - q * R4;
-                    if (r >= 0 && r < R4)
-                        isb[r] = sbv[i];
-                }
-                csync();
                 const int kk = k + 8 + q, sl = kk % o.NR;
+                // this item's (scale | bias << 16) words: behind its weights in
+                // the ring slot (packed table), else staged into buffer q & 1
+                // (the barrier also tells that every warp is done with item
+                // q - 1, so buffer q & 1, last read for item q - 2, is free)
+                const uint32_t *isb;
+                if constexpr (PK) {
+                    isb = reinterpret_cast<const uint32_t *>(s.ring + (size_t)sl * o.slot + 32 * R4);
+                } else {
+                    uint32_t *buf = reinterpret_cast<uint32_t *>(s.dss) + (q & 1) * R4;
+#pragma unroll
+                    for (int i = 0; i < kR; ++i) {
+                        const int r = tid + i * kCT - q * R4;
+                        if (r >= 0 && r < R4)
+                            buf[r] = sbv[i];
+                    }
+                    csync();
+                    isb = buf;
+                }
                 if (!__all_sync(0xffffffffu, good && pwait(&s.full[sl], (kk / o.NR) & 1, p))) {
                     good = false;
                     continue;
@@ -1788,7 +1800,8 @@ __device__ void consumers(const PdParams &p, const Smem &s)
 // router input scale, shared-branch gate, post-FFN norm); plain layers run the
 // variant without their code.
 // T1: one token of BF16 activations, gate/up on integer dot products.
-template <int NB, bool EXT, bool T1>
+// PK: every layer has the packed down (scale | bias) words (layout down_sb).
+template <int NB, bool EXT, bool T1, bool PK>
 __global__ void __launch_bounds__(kPT, 1) pd_kernel(const __grid_constant__ PdParams p)
 {
     extern __shared__ __align__(1024) uint8_t sm[];
@@ -1809,9 +1822,9 @@ __global__ void __launch_bounds__(kPT, 1) pd_kernel(const __grid_constant__ PdPa
     // shared-expert unit may add into y before any exchange of this call.
     __syncthreads();
     if (threadIdx.x >= kCT)
-        producer<NB, EXT>(p, s);
+        producer<NB, EXT, PK>(p, s);
     else
-        consumers<NB, EXT, T1>(p, s);
+        consumers<NB, EXT, T1, PK>(p, s);
     __syncthreads();
     // The last CTA to finish clears the counters for the next call (unless a
     // wait gave up: then the workspace must be re-initialised).
@@ -1896,10 +1909,10 @@ extern "C" __attribute__((visibility("default"))) int mx_pd_trace_read(unsigned 
 
 namespace {
 
-template <int NB, bool EXT, bool T1>
+template <int NB, bool EXT, bool T1, bool PK = false>
 cudaError_t launch_nb(const PdParams &p, cudaStream_t st)
 {
-    auto k = pd_kernel<NB, EXT, T1>;
+    auto k = pd_kernel<NB, EXT, T1, PK>;
     cudaError_t e = smem_optin(reinterpret_cast<const void *>(k), (size_t)p.sm.total);
     if (e != cudaSuccess)
         return e;
@@ -1926,13 +1939,16 @@ cudaError_t launch_nb(const PdParams &p, cudaStream_t st)
 
 cudaError_t launch_pd(const PdParams &p, cudaStream_t st)
 {
-    bool ext = false;
+    bool ext = false, pk = true;
     for (int l = 0; l < p.n_layers; ++l) {
         const PdLayer &L = p.L[l];
         ext = ext || L.slot || L.router_scale || L.post_norm || L.shared_gate;
+        pk = pk && L.dsb;
     }
     if (p.act == 0)
         return ext ? launch_nb<2, true, false>(p, st) : launch_nb<2, false, false>(p, st);
+    if (p.T == 1 && pk)
+        return ext ? launch_nb<1, true, true, true>(p, st) : launch_nb<1, false, true, true>(p, st);
     if (p.T == 1)
         return ext ? launch_nb<1, true, true>(p, st) : launch_nb<1, false, true>(p, st);
     return ext ? launch_nb<1, true, false>(p, st) : launch_nb<1, false, false>(p, st);

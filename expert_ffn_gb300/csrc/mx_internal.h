@@ -59,6 +59,7 @@ struct LayerExt {
     const uint16_t *router_scale, *post_norm, *shared_gate;  // BF16 [D], nullable
     float post_eps;
     float rcoef;                 // 1 / sqrtf(D) (host-rounded, as the oracle's)
+    const uint32_t *down_sb;     // packed down (scale | bias << 16) words, nullable
 };
 
 struct FfnArgs {
@@ -149,8 +150,9 @@ struct PdLayer {
     const uint16_t *rs, *rb;
     const uint8_t *blob;
     uint64_t stride;
-    uint64_t off_s[3], off_b[3];
+    uint32_t off_s[3], off_b[3];  // s / b offsets in a record (the path requires < 2^32)
     const uint16_t *ss[3], *sb[3];
+    const uint32_t *dsb, *dsb_s;  // packed down (scale | bias << 16) words: records, shared (nullable)
     const float *pes;
     int32_t *topk_idx;
     float *topk_w;

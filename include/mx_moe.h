@@ -93,7 +93,8 @@ typedef struct {
 } mx_sub;
 
 #define MX_MOE_LAYOUT_MAGIC 0x4D584D45u /* "EMXM" little-endian */
-#define MX_MOE_LAYOUT_VERSION 2u /* version 1 layouts (ending at per_expert_scale) are accepted too */
+#define MX_MOE_LAYOUT_VERSION 3u /* version 1 (ending at per_expert_scale) and 2 (ending at
+                                    shared_expert_gate) layouts are accepted too */
 
 /* Layout of one layer's expert blob: n_experts records of record_stride bytes
  * (n_slots records when expert_slot is given).  Record r holds gate [d_expert,
@@ -125,7 +126,23 @@ typedef struct {
  * single-launch decode path (T <= 4) and the grouped-GEMM path (BF16, T > 4);
  * calls that would run the multi-launch decode kernels (fp32 with T > 4, or
  * those paths forced by MX_MOE_SINGLE_LAUNCH=0 / MX_MOE_PREFILL_GEMM=0)
- * return MX_ERR_UNSUPPORTED for them.  expert_slot works on every path. */
+ * return MX_ERR_UNSUPPORTED for them.  expert_slot works on every path.
+ *
+ * Version 3 adds one optional field, a derived copy of weights already in the
+ * layer (so the results do not depend on it):
+ *   down_sb       device uint32, 16-byte aligned, nullable: the down
+ *                 projections' scale and bias pairs written by
+ *                 mx_moe_pack_down_sb for this layout, blob and shared expert,
+ *                 one word per (row, group) = scale bits | bias bits << 16,
+ *                 column-major: record r, group g, row d at (r * (I/64) + g) *
+ *                 D + d for the n records of the blob (n_slots with an
+ *                 expert_slot table, else n_experts), then the shared expert's
+ *                 group g, row d at n * (I/64) * D + g * D + d.  The group of
+ *                 one 64-wide slice of a down projection is then D contiguous
+ *                 words, which the single-launch decode path copies in blocks
+ *                 instead of gathering 2 D strided 2-byte values per slice;
+ *                 the other paths do not read it.  It must be re-packed
+ *                 whenever the down scales or biases it was made from change. */
 typedef struct {
     uint32_t magic;              /* MX_MOE_LAYOUT_MAGIC                          */
     uint32_t version;            /* MX_MOE_LAYOUT_VERSION                        */
@@ -148,6 +165,8 @@ typedef struct {
     const uint16_t *post_norm;     /* device BF16 [D], 16-byte aligned, nullable */
     float post_eps;                /* eps of post_norm                           */
     const uint16_t *shared_expert_gate; /* device BF16 [D], 16-byte aligned, nullable */
+    /* version 3 and later */
+    const uint32_t *down_sb;     /* device, 16-byte aligned, nullable (see above)  */
 } mx_moe_layout;
 
 /* Per-call options (all optional; pass NULL for the plain block). */
@@ -296,6 +315,26 @@ MX_API mx_status mx_moe_stack_forward(void *x_io, int T, int n_layers, const mx_
                                float rms_eps, void *stream, void *ws, size_t ws_bytes);
 
 MX_API size_t mx_moe_stack_workspace_bytes(const mx_moe_layout *layout, int T);
+
+/*
+ * Packed down-projection scale and bias words (layout field down_sb, version
+ * 3; format above).  mx_moe_down_sb_bytes returns the size of the table for
+ * `layout` (0 if the layout is invalid).  mx_moe_pack_down_sb writes it:
+ *   layout       a valid layout (its own down_sb is not read)
+ *   blob         device expert blob of that layout
+ *   shared_down  the layer's shared down projection [D][S] (its scales and
+ *                biases are read)
+ *   out          device, 16-byte aligned, mx_moe_down_sb_bytes(layout) bytes,
+ *                owned by the caller, not overlapping the blob
+ *   stream       CUDA stream (NULL = the legacy default stream); the copy is
+ *                asynchronous on it
+ * Errors: MX_ERR_INVALID_ARG for null pointers or a bad layout, MX_ERR_ALIGNMENT
+ * for a misaligned `out`, MX_ERR_CUDA if the launch fails.  A table is a pure
+ * rearrangement of BF16 values the blob already holds (no arithmetic).
+ */
+MX_API size_t mx_moe_down_sb_bytes(const mx_moe_layout *layout);
+MX_API mx_status mx_moe_pack_down_sb(const mx_moe_layout *layout, const void *blob, const mx_qlinear *shared_down,
+                                     uint32_t *out, void *stream);
 
 /*
  * Per-stage timing, after the stage-timing profiler of the gem "Native

@@ -85,7 +85,7 @@ def test_valid_call_with_zero_tokens_is_a_noop(L):
 
 @pytest.mark.parametrize("field,value,status", [
     ("magic", 0x12345678, INVALID),
-    ("version", 3, INVALID),
+    ("version", 4, INVALID),
     ("version", 0, INVALID),
     ("group", 32, UNSUP),
     ("bits", 8, UNSUP),
@@ -196,7 +196,8 @@ def test_stack_rejections(L):
 
 LAYOUT_FIELDS = ("magic", "version", "d_model", "d_expert", "n_experts", "top_k", "d_shared", "group", "bits",
                  "record_stride", "gate", "up", "down", "act_dtype", "layer_scalar", "per_expert_scale",
-                 "expert_slot", "n_slots", "router_scale", "post_norm", "post_eps", "shared_expert_gate")
+                 "expert_slot", "n_slots", "router_scale", "post_norm", "post_eps", "shared_expert_gate",
+                 "down_sb")
 
 
 def test_layout_struct_matches_the_header(tmp_path):
@@ -229,6 +230,7 @@ def test_version_one_layout_is_accepted(L):
     ("router_scale", FAKE + 8, ALIGN),
     ("post_norm", FAKE + 2, ALIGN),
     ("shared_expert_gate", FAKE + 4, ALIGN),
+    ("down_sb", FAKE + 8, ALIGN),
 ])
 def test_optional_part_alignment(L, field, value, status):
     lay = layout(**{field: value})
@@ -264,3 +266,37 @@ def test_route_entry_rejects_router_scale(L):
     rc = L.mx_moe_route(FAKE, 4, C.byref(r), C.byref(lay), FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, FAKE,
                         1 << 30)
     assert rc == UNSUP
+
+
+# ------------------------------------------------ layout version 3 (packed down words)
+
+def test_version_two_layout_is_accepted(L):
+    """A version-2 caller's struct ends at shared_expert_gate: down_sb is not read."""
+    lay = layout(version=2)
+    lay.down_sb = FAKE + 8
+    assert call(L, lay, T=0) == OK
+
+
+def test_down_sb_bytes(L):
+    """Column-major (scale | bias << 16) words: every record's I/64 groups of D
+    rows, then the shared expert's S/64 groups."""
+    lay = layout()
+    assert L.mx_moe_down_sb_bytes(C.byref(lay)) == (E * (I // 64) + S // 64) * D * 4
+    lay = layout(expert_slot=FAKE, n_slots=5)
+    assert L.mx_moe_down_sb_bytes(C.byref(lay)) == (5 * (I // 64) + S // 64) * D * 4
+    assert L.mx_moe_down_sb_bytes(C.byref(layout(magic=1))) == 0
+
+
+def test_pack_down_sb_host_checks(L):
+    """Rejections that come before any launch."""
+    lay = layout()
+    sd = q(D, S, 4)
+    out = FAKE + 0x8000000
+    assert L.mx_moe_pack_down_sb(C.byref(layout(magic=1)), FAKE, C.byref(sd), out, None) == INVALID
+    assert L.mx_moe_pack_down_sb(C.byref(lay), None, C.byref(sd), out, None) == INVALID
+    assert L.mx_moe_pack_down_sb(C.byref(lay), FAKE, None, out, None) == INVALID
+    assert L.mx_moe_pack_down_sb(C.byref(lay), FAKE, C.byref(sd), None, None) == INVALID
+    assert L.mx_moe_pack_down_sb(C.byref(lay), FAKE, C.byref(q(S, D, 4)), out, None) != OK  # transposed shape
+    assert L.mx_moe_pack_down_sb(C.byref(lay), FAKE, C.byref(sd), out + 4, None) == ALIGN
+    assert L.mx_moe_pack_down_sb(C.byref(lay), FAKE, C.byref(sd), FAKE + 0x1000, None) == INVALID  # inside the blob
+    assert len(L.mx_last_error_string()) > 0
