@@ -528,8 +528,8 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
 // words (even columns of a word, then odd).  Lane (gid, c) takes columns
 // 16c .. 16c + 15 of rows gid (gate) and gid (up): per group 16 byte dot
 // products, exact in int32 (|sum| < 2^23, so exact in fp32 too); then the
-// group's scale and bias terms in fp32, the bias term once per row (lane c =
-// 0), and the four lanes of a row added by shuffles.  fo = 2^-k1.  The warp
+// group's scale term in fp32, the bias term once per row and group (lane c
+// takes every fourth group), and the four lanes of a row added by shuffles.  fo = 2^-k1.  The warp
 // takes groups [g0, g1) of the item.  Lane output: that part of the gate and
 // up dot products of row gid (every lane of the row).
 __device__ __forceinline__ void gu_item_t1(const uint8_t *st, int G, int g0, int g1, const uint8_t *xp, float fo,
@@ -539,8 +539,14 @@ __device__ __forceinline__ void gu_item_t1(const uint8_t *st, int G, int g0, int
     const uint8_t *gt = st + gid * 32 + c * 8, *ut = gt + 256 * G;
     const uint16_t *sc = reinterpret_cast<const uint16_t *>(st + 512 * G) + gid * G;
     const uint16_t *sg = sc, *bg = sc + 8 * G, *su = sc + 16 * G, *bu = sc + 24 * G;
-    const float bsel = c == 0 ? 1.f : 0.f;
-    float pg[2] = {0.f, 0.f}, pu[2] = {0.f, 0.f}, qg[2] = {0.f, 0.f}, qu[2] = {0.f, 0.f};
+    float pg[2] = {0.f, 0.f}, pu[2] = {0.f, 0.f}, qg = 0.f, qu = 0.f;
+    // the bias terms b_g X_g of the row, once per group: lane c takes groups
+    // g0 + c, g0 + c + 4, ... (the shuffles below add the four lanes)
+    for (int g = g0 + c; g < g1; g += 4) {
+        const float X = xg[g];
+        qg = fmaf(bf2f(bg[g]), X, qg);
+        qu = fmaf(bf2f(bu[g]), X, qu);
+    }
 #pragma unroll 2
     for (int n = 0; n < g1 - g0; ++n) {
         const int g = g0 + n, h = n & 1;
@@ -576,14 +582,11 @@ __device__ __forceinline__ void gu_item_t1(const uint8_t *st, int G, int g0, int
             u1 = dp4a_us(lo, x1.z, u1);
             u1 = dp4a_us(hi, x1.w, u1);
         }
-        const float X = xg[g] * bsel;
         pg[h] = fmaf(bf2f(sg[g]), (float)(g1 * 256 + g0), pg[h]);
-        qg[h] = fmaf(bf2f(bg[g]), X, qg[h]);
         pu[h] = fmaf(bf2f(su[g]), (float)(u1 * 256 + u0), pu[h]);
-        qu[h] = fmaf(bf2f(bu[g]), X, qu[h]);
     }
-    float ag = fo * (pg[0] + pg[1]) + (qg[0] + qg[1]);
-    float au = fo * (pu[0] + pu[1]) + (qu[0] + qu[1]);
+    float ag = fo * (pg[0] + pg[1]) + qg;
+    float au = fo * (pu[0] + pu[1]) + qu;
     ag += __shfl_xor_sync(0xffffffffu, ag, 1);
     au += __shfl_xor_sync(0xffffffffu, au, 1);
     ag += __shfl_xor_sync(0xffffffffu, ag, 2);
@@ -1120,8 +1123,25 @@ __device__ void route_tables(const PdParams &p, const PdLayer &L, const Smem &s,
                 L.topk_idx[t * K + lane] = mye;
                 L.topk_w[t * K + lane] = x;
             }
+            if (T == 1) {
+                // one token: K distinct experts with one slot each, active in
+                // top-k order (any fixed order of the active experts will do:
+                // it only assigns units to CTAs)
+                rt.act_e[lane] = mye;
+                if constexpr (EXT)
+                    act_r(rt, E)[lane] = expert_record(L.slot, L.n_slots, mye, p.err);
+                rt.act_n[lane] = 1;
+                rt.act_slot[4 * lane] = lane;
+                rt.emap[mye] = lane;
+            }
         }
+        if (T == 1 && lane == 0)
+            *rt.n_act = K;
         PD_STAMP(l, 29);
+    }
+    if (E <= 128 && T == 1) {
+        csync();
+        return;
     }
     if (E > 128) {
         // more than 128 experts: each logit's rank by a scan of its row
